@@ -1,0 +1,72 @@
+"""The ring-ordered fold written per output element (oracle).
+
+TEST INFRASTRUCTURE ONLY -- see ``oracle/__init__.py``.
+
+Following the ring of "Networks and Collective Communication" section 5.1
+with the readings of ``oracle/ring.py``: element i lies in chunk c; chunk c's
+partial starts at rank c+1 and collects ranks c+2, ..., p-1, 0, ..., c in that
+order, each receiver combining the received partial with its own value.  The
+all-gather phase only copies, so every rank's output at i is that fold.
+
+This evaluates the fold for an explicit set of indices, so that huge buffers
+can be checked at sampled positions.  It is checked against the literal
+simulator ``oracle.ring`` in ``tests/test_oracle_ring.py``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .bf16 import bf16_to_f32, f32_to_bf16_rne
+from .ring import chunk_bounds, combine
+
+
+def chunk_of(p: int, n: int, idx: np.ndarray) -> np.ndarray:
+    """Chunk number of each index (by scanning the chunk table)."""
+    bounds = chunk_bounds(p, n)
+    starts = np.array([off for off, _ in bounds], dtype=np.int64)
+    ends = np.array([off + ln for off, ln in bounds], dtype=np.int64)
+    idx = np.asarray(idx, dtype=np.int64)
+    if idx.size and (idx.min() < 0 or idx.max() >= n):
+        raise IndexError("index out of range")
+    out = np.empty(idx.shape, dtype=np.int64)
+    for c in range(p):
+        if ends[c] > starts[c]:
+            sel = (idx >= starts[c]) & (idx < ends[c])
+            out[sel] = c
+    return out
+
+
+def fold_at(x: list[np.ndarray], idx: np.ndarray, dtype: str = "f32", op: str = "sum"):
+    """Reduced value at each index in ``idx`` (fp32/int32 accumulator, unrounded)."""
+    p, n = len(x), len(x[0])
+    idx = np.asarray(idx, dtype=np.int64)
+    chunks = chunk_of(p, n, idx)
+    acc_dtype = np.int32 if dtype == "i32" else np.float32
+    out = np.empty(idx.shape, dtype=acc_dtype)
+
+    def value(rank, sel):
+        v = x[rank][sel]
+        return bf16_to_f32(v) if dtype == "bf16" else v.astype(acc_dtype, copy=True)
+
+    for c in range(p):
+        mask = chunks == c
+        if not mask.any():
+            continue
+        sel = idx[mask]
+        acc = value((c + 1) % p, sel)
+        for j in range(2, p + 1):
+            acc = combine(acc, value((c + j) % p, sel), op)
+        out[mask] = acc
+    return out
+
+
+def allreduce_at(x: list[np.ndarray], idx: np.ndarray, dtype: str = "f32", op: str = "sum"):
+    """All-reduce output (any rank) at the given indices, in the output dtype."""
+    acc = fold_at(x, idx, dtype, op)
+    return f32_to_bf16_rne(acc) if dtype == "bf16" else acc
+
+
+def bucket_at(grads: list[np.ndarray], idx: np.ndarray, scale: float):
+    """DDP bucket output (any rank) at the given indices: bf16(fold * scale)."""
+    acc = fold_at(grads, idx, "f32", "sum")
+    return f32_to_bf16_rne(acc * np.float32(scale))
