@@ -1,0 +1,296 @@
+"""Thin Python binding of ``libccl.so`` (include/ccl.h), same names as the C ABI.
+
+Argument marshalling only: each function checks tensor devices, dtypes and
+sizes (the C side trusts sizes), packs the per-rank device pointers into
+host arrays and calls the library on the current torch stream.  Every
+computation runs in the library's CUDA kernels; there is no CPU fallback.
+Importing this module fails loudly when the library is missing.
+
+Tensors are the p per-rank buffers of a collective: lists of contiguous CUDA
+tensors (torch only provides the device memory and the stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+# CCL_LIBRARY overrides the in-tree library (e.g. a build kept elsewhere)
+LIB_PATH = os.environ.get("CCL_LIBRARY") or os.path.join(_PKG, "lib", "libccl.so")
+
+CCL_OK, CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED, CCL_ERR_CUDA = 0, 1, 2, 3
+CCL_F32, CCL_BF16, CCL_I32 = 0, 1, 2
+CCL_SUM, CCL_MAX, CCL_MIN = 0, 1, 2
+CCL_KIND_ALLREDUCE, CCL_KIND_REDUCE_SCATTER, CCL_KIND_ALL_GATHER = 0, 1, 2
+CCL_MAX_RANKS = 128
+
+_DTYPES = {torch.float32: CCL_F32, torch.bfloat16: CCL_BF16, torch.int32: CCL_I32}
+_OPS = {"sum": CCL_SUM, "max": CCL_MAX, "min": CCL_MIN}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m a2a_ring_ordered_gb300.build` "
+            "(there is no fallback path)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    st = ctypes.c_int
+    sigs = {
+        "ccl_abi_version": (i32, []),
+        "ccl_status_string": (ctypes.c_char_p, [st]),
+        "ccl_last_error": (ctypes.c_char_p, []),
+        "ccl_kernel_launch_count": (u64, []),
+        "ccl_chunk_bounds": (st, [i32, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
+        "ccl_allreduce": (st, [pp, pp, i32, sz, i32, i32, vp]),
+        "ccl_reduce_scatter": (st, [pp, pp, i32, sz, i32, i32, vp]),
+        "ccl_all_gather": (st, [pp, pp, i32, sz, i32, vp]),
+        "ccl_bucket_allreduce_scale_cast": (st, [pp, pp, i32, sz, ctypes.c_float, vp]),
+        "ccl_all_to_allv": (st, [pp, ctypes.POINTER(sz), pp, i32, sz, i32, vp]),
+        "ccl_ring_literal_workspace_bytes": (sz, [i32, i32, sz, i32]),
+        "ccl_ring_allreduce_literal": (st, [pp, pp, i32, sz, i32, i32, ctypes.POINTER(u64), vp, sz, vp]),
+        "ccl_ring_reduce_scatter_literal": (st, [pp, pp, i32, sz, i32, i32, ctypes.POINTER(u64), vp, sz, vp]),
+        "ccl_ring_all_gather_literal": (st, [pp, pp, i32, sz, i32, ctypes.POINTER(u64), vp]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if lib.ccl_abi_version() != 1:
+        raise ImportError("libccl.so ABI version mismatch; rebuild it")
+    return lib
+
+
+LIB = _load()
+
+
+class CclError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        detail = LIB.ccl_last_error().decode()
+        super().__init__(f"{what}: {LIB.ccl_status_string(status).decode()}"
+                         + (f" -- {detail}" if detail else ""))
+
+
+def _check(status: int, what: str) -> None:
+    if status != CCL_OK:
+        raise CclError(status, what)
+
+
+# ----------------------------------------------------------------- marshalling
+def _ptr_array(ptrs: Sequence[int]):
+    arr = (ctypes.c_void_p * len(ptrs))()
+    for i, v in enumerate(ptrs):
+        arr[i] = v
+    return arr
+
+
+def _tensors(ts: Sequence[torch.Tensor], name: str) -> list[torch.Tensor]:
+    ts = list(ts)
+    if not 1 <= len(ts) <= CCL_MAX_RANKS:
+        raise ValueError(f"{name}: need 1..{CCL_MAX_RANKS} rank buffers, got {len(ts)}")
+    dev = ts[0].device
+    for i, t in enumerate(ts):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name}[{i}] must be a CUDA tensor")
+        if t.device != dev:
+            raise ValueError(f"{name}[{i}] is on {t.device}, expected {dev}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}[{i}] must be contiguous")
+        if t.dtype != ts[0].dtype:
+            raise ValueError(f"{name}[{i}] has dtype {t.dtype}, expected {ts[0].dtype}")
+    return ts
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype} (float32, bfloat16, int32)") from None
+
+
+def _op_code(op: str) -> int:
+    try:
+        return _OPS[op]
+    except KeyError:
+        raise ValueError(f"op must be one of {sorted(_OPS)}") from None
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _chunk(p: int, n: int, c: int) -> tuple[int, int]:
+    return ccl_chunk_bounds(p, n, c)
+
+
+def _numel_check(ts, want, name):
+    for i, (t, w) in enumerate(zip(ts, want)):
+        if t.numel() != w:
+            raise ValueError(f"{name}[{i}] has {t.numel()} elements, expected {w}")
+
+
+# ------------------------------------------------------------------ utilities
+def ccl_abi_version() -> int:
+    return LIB.ccl_abi_version()
+
+
+def ccl_status_string(status: int) -> str:
+    return LIB.ccl_status_string(status).decode()
+
+
+def ccl_last_error() -> str:
+    return LIB.ccl_last_error().decode()
+
+
+def ccl_kernel_launch_count() -> int:
+    return LIB.ccl_kernel_launch_count()
+
+
+def ccl_chunk_bounds(p: int, n: int, c: int) -> tuple[int, int]:
+    off, ln = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(LIB.ccl_chunk_bounds(p, n, c, ctypes.byref(off), ctypes.byref(ln)), "ccl_chunk_bounds")
+    return off.value, ln.value
+
+
+# ------------------------------------------------------------- fused calls
+def ccl_allreduce(send, recv, op: str = "sum", stream=None) -> None:
+    """Every recv[r] gets the ring-ordered reduction of send[0..p-1] (in place allowed)."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    if len(recv) != p or recv[0].dtype != send[0].dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [n] * p, "recv")
+    _check(LIB.ccl_allreduce(_ptr_array([t.data_ptr() for t in send]),
+                             _ptr_array([t.data_ptr() for t in recv]), p, n,
+                             _dtype_code(send[0]), _op_code(op), _stream(stream, send[0].device)),
+           "ccl_allreduce")
+
+
+def ccl_reduce_scatter(send, recv, op: str = "sum", stream=None) -> None:
+    """recv[k] (len(k) elements) gets chunk k of the ring-ordered reduction."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    if len(recv) != p or recv[0].dtype != send[0].dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [_chunk(p, n, k)[1] for k in range(p)], "recv")
+    _check(LIB.ccl_reduce_scatter(_ptr_array([t.data_ptr() for t in send]),
+                                  _ptr_array([t.data_ptr() for t in recv]), p, n,
+                                  _dtype_code(send[0]), _op_code(op), _stream(stream, send[0].device)),
+           "ccl_reduce_scatter")
+
+
+def ccl_all_gather(send, recv, stream=None) -> None:
+    """send[k] is block k (len(k) elements); every recv[r] gets the concatenation."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p = len(send)
+    n = sum(t.numel() for t in send)
+    if len(recv) != p or recv[0].dtype != send[0].dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    _numel_check(send, [_chunk(p, n, k)[1] for k in range(p)], "send")
+    _numel_check(recv, [n] * p, "recv")
+    _check(LIB.ccl_all_gather(_ptr_array([t.data_ptr() for t in send]),
+                              _ptr_array([t.data_ptr() for t in recv]), p, n,
+                              _dtype_code(send[0]), _stream(stream, send[0].device)),
+           "ccl_all_gather")
+
+
+def ccl_bucket_allreduce_scale_cast(grads, out_bf16, scale: float | None = None, stream=None) -> None:
+    """out_bf16[r] = bf16(ring_sum(grads) * scale); scale defaults to 1/p."""
+    grads, out = _tensors(grads, "grads"), _tensors(out_bf16, "out_bf16")
+    p, n = len(grads), grads[0].numel()
+    if grads[0].dtype != torch.float32 or out[0].dtype != torch.bfloat16 or len(out) != p:
+        raise ValueError("grads must be p float32 buffers and out_bf16 p bfloat16 buffers")
+    _numel_check(grads, [n] * p, "grads")
+    _numel_check(out, [n] * p, "out_bf16")
+    s = float(1.0 / p) if scale is None else float(scale)
+    _check(LIB.ccl_bucket_allreduce_scale_cast(_ptr_array([t.data_ptr() for t in grads]),
+                                               _ptr_array([t.data_ptr() for t in out]), p, n, s,
+                                               _stream(stream, grads[0].device)),
+           "ccl_bucket_allreduce_scale_cast")
+
+
+def ccl_all_to_allv(send, counts, recv, row_elems: int, stream=None) -> None:
+    """MoE dispatch/combine: counts[s][d] rows of row_elems go from send[s] to recv[d]."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p = len(send)
+    rows = [[int(counts[s][d]) for d in range(p)] for s in range(p)]
+    if len(recv) != p or recv[0].dtype != send[0].dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    _numel_check(send, [sum(rows[s]) * row_elems for s in range(p)], "send")
+    _numel_check(recv, [sum(rows[s][d] for s in range(p)) * row_elems for d in range(p)], "recv")
+    flat = (ctypes.c_size_t * (p * p))(*[rows[s][d] for s in range(p) for d in range(p)])
+    _check(LIB.ccl_all_to_allv(_ptr_array([t.data_ptr() for t in send]), flat,
+                               _ptr_array([t.data_ptr() for t in recv]), p, row_elems,
+                               _dtype_code(send[0]), _stream(stream, send[0].device)),
+           "ccl_all_to_allv")
+
+
+# ------------------------------------------------------- literal ring engine
+def ccl_ring_literal_workspace_bytes(kind: int, p: int, n: int, dtype: torch.dtype) -> int:
+    return LIB.ccl_ring_literal_workspace_bytes(kind, p, n, _DTYPES[dtype])
+
+
+def _workspace(kind, p, n, t, workspace):
+    need = ccl_ring_literal_workspace_bytes(kind, p, n, t.dtype)
+    if need == 0:
+        return None, 0
+    if workspace is None:  # caller-owned scratch, allocated by torch
+        workspace = torch.empty(need, dtype=torch.uint8, device=t.device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def ccl_ring_allreduce_literal(send, recv, op: str = "sum", workspace=None, stream=None) -> list[int]:
+    """The 2(p-1)-step ring, one launch per step; returns bytes sent per rank."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [n] * p, "recv")
+    ws, ws_bytes = _workspace(CCL_KIND_ALLREDUCE, p, n, send[0], workspace)
+    sent = (ctypes.c_uint64 * p)()
+    _check(LIB.ccl_ring_allreduce_literal(_ptr_array([t.data_ptr() for t in send]),
+                                          _ptr_array([t.data_ptr() for t in recv]), p, n,
+                                          _dtype_code(send[0]), _op_code(op), sent,
+                                          None if ws is None else ws.data_ptr(), ws_bytes,
+                                          _stream(stream, send[0].device)),
+           "ccl_ring_allreduce_literal")
+    return list(sent)
+
+
+def ccl_ring_reduce_scatter_literal(send, recv, op: str = "sum", workspace=None, stream=None) -> list[int]:
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [_chunk(p, n, k)[1] for k in range(p)], "recv")
+    ws, ws_bytes = _workspace(CCL_KIND_REDUCE_SCATTER, p, n, send[0], workspace)
+    sent = (ctypes.c_uint64 * p)()
+    _check(LIB.ccl_ring_reduce_scatter_literal(_ptr_array([t.data_ptr() for t in send]),
+                                               _ptr_array([t.data_ptr() for t in recv]), p, n,
+                                               _dtype_code(send[0]), _op_code(op), sent,
+                                               None if ws is None else ws.data_ptr(), ws_bytes,
+                                               _stream(stream, send[0].device)),
+           "ccl_ring_reduce_scatter_literal")
+    return list(sent)
+
+
+def ccl_ring_all_gather_literal(send, recv, stream=None) -> list[int]:
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p = len(send)
+    n = sum(t.numel() for t in send)
+    _numel_check(send, [_chunk(p, n, k)[1] for k in range(p)], "send")
+    _numel_check(recv, [n] * p, "recv")
+    sent = (ctypes.c_uint64 * p)()
+    _check(LIB.ccl_ring_all_gather_literal(_ptr_array([t.data_ptr() for t in send]),
+                                           _ptr_array([t.data_ptr() for t in recv]), p, n,
+                                           _dtype_code(send[0]), sent,
+                                           _stream(stream, send[0].device)),
+           "ccl_ring_all_gather_literal")
+    return list(sent)

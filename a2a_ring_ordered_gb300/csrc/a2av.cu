@@ -1,0 +1,145 @@
+// a2av.cu -- all-to-all(v) block transpose: MoE dispatch / combine
+// ("Networks and Collective Communication" section 4.1: device i's block j
+// goes to device j, a transpose; section 7.4: MoE dispatch and combine).
+//
+// The host turns the p x p row counts into a list of contiguous byte blocks
+// (source s's block for d -> destination d's block from s).  Blocks are cut
+// into 32 KB tiles measured in destination space, and one CTA copies one
+// tile, so the work is balanced by bytes however skewed the counts are (a
+// Zipf-hot expert receives far more rows than the others).
+//
+// Inside a tile, whole 16-byte destination units are copied with 16-byte
+// loads and stores.  When source and destination differ in 16-byte phase
+// (rows whose size is not a multiple of 16 bytes), each lane of a warp loads
+// the aligned 16-byte source granule under its unit, takes the next granule
+// from its neighbour with a warp shuffle, and funnel-shifts the pair into the
+// destination's alignment; the few bytes before the first and after the last
+// whole unit are copied one by one.  Every load touches only aligned granules
+// that hold at least one source byte of the block.
+// HBM traffic: one read and one write of every moved byte.
+#include "device_common.cuh"
+
+namespace ccl {
+namespace {
+
+constexpr int kUnitsPerThread = static_cast<int>(kA2ATileBytes / 16 / kThreads);  // 8
+
+__device__ __forceinline__ void copy_byte(uintptr_t dst, intptr_t shift) {
+  const unsigned char b = __ldg(reinterpret_cast<const unsigned char*>(dst + shift));
+  *reinterpret_cast<unsigned char*>(dst) = b;
+}
+
+// Bytes [delta, delta+16) of the 32-byte pair (lo, hi), little-endian.
+__device__ __forceinline__ uint4 realign(const uint4 lo, const uint4 hi, int delta) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const uint32_t sh = 8u * static_cast<uint32_t>(delta & 3);
+  uint4 o;
+#define CCL_REALIGN(Q)                             \
+  o.x = __funnelshift_r(w[Q + 0], w[Q + 1], sh);   \
+  o.y = __funnelshift_r(w[Q + 1], w[Q + 2], sh);   \
+  o.z = __funnelshift_r(w[Q + 2], w[Q + 3], sh);   \
+  o.w = __funnelshift_r(w[Q + 3], w[Q + 4], sh);
+  switch (delta >> 2) {
+    case 0: CCL_REALIGN(0) break;
+    case 1: CCL_REALIGN(1) break;
+    case 2: CCL_REALIGN(2) break;
+    default: CCL_REALIGN(3) break;
+  }
+#undef CCL_REALIGN
+  return o;
+}
+
+// Copy destination bytes [lo, hi); the source byte of destination byte x is
+// x + shift.  Called by all threads of the CTA with the same arguments.
+__device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
+  const int tid = threadIdx.x;
+  const uintptr_t ua = (lo + 15) & ~static_cast<uintptr_t>(15);
+  const uintptr_t ub = hi & ~static_cast<uintptr_t>(15);
+  if (ua >= ub) {  // no whole destination unit: byte by byte
+    for (uintptr_t x = lo + tid; x < hi; x += kThreads) copy_byte(x, shift);
+    return;
+  }
+  const uint64_t m = (ub - ua) / 16;  // whole 16-byte destination units
+  const int delta = static_cast<int>(static_cast<uintptr_t>(shift) & 15);
+  if (delta == 0) {
+    for (uint64_t u0 = 0; u0 < m; u0 += static_cast<uint64_t>(kThreads) * kUnitsPerThread) {
+      uint4 v[kUnitsPerThread];
+#pragma unroll
+      for (int j = 0; j < kUnitsPerThread; ++j) {
+        const uint64_t u = u0 + static_cast<uint64_t>(j) * kThreads + tid;
+        if (u < m) v[j] = ld_once16(reinterpret_cast<const void*>(ua + 16 * u + shift));
+      }
+#pragma unroll
+      for (int j = 0; j < kUnitsPerThread; ++j) {
+        const uint64_t u = u0 + static_cast<uint64_t>(j) * kThreads + tid;
+        if (u < m) st_stream16(reinterpret_cast<void*>(ua + 16 * u), v[j]);
+      }
+    }
+  } else {
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    // source granule under unit u: ua + 16u + shift - delta (16-byte aligned)
+    const uintptr_t g0 = ua + shift - delta;
+    for (uint64_t k0 = static_cast<uint64_t>(warp) * 32; k0 < m; k0 += kThreads) {
+      const uint64_t u = k0 + lane;
+      uint4 cur = make_uint4(0, 0, 0, 0);
+      uint4 extra = make_uint4(0, 0, 0, 0);
+      // granule u holds bytes of unit u (u < m) or the last bytes of unit u-1 (u == m)
+      if (u <= m) cur = ld_once16(reinterpret_cast<const void*>(g0 + 16 * u));
+      if (lane == 31 && u < m) extra = ld_once16(reinterpret_cast<const void*>(g0 + 16 * (u + 1)));
+      uint4 nxt;
+      nxt.x = __shfl_down_sync(0xFFFFFFFFu, cur.x, 1);
+      nxt.y = __shfl_down_sync(0xFFFFFFFFu, cur.y, 1);
+      nxt.z = __shfl_down_sync(0xFFFFFFFFu, cur.z, 1);
+      nxt.w = __shfl_down_sync(0xFFFFFFFFu, cur.w, 1);
+      if (lane == 31) nxt = extra;
+      if (u < m) st_stream16(reinterpret_cast<void*>(ua + 16 * u), realign(cur, nxt, delta));
+    }
+  }
+  // bytes before the first and after the last whole unit (at most 15 + 15)
+  const int n_head = static_cast<int>(ua - lo);
+  const int n_edge = n_head + static_cast<int>(hi - ub);
+  if (tid < n_edge) copy_byte(tid < n_head ? lo + tid : ub + (tid - n_head), shift);
+}
+
+__global__ void __launch_bounds__(kThreads) a2av_kernel(const __grid_constant__ A2AArgs a) {
+  for (uint64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
+    // the block that owns tile t: the last one whose first tile is <= t
+    int lo = 0, hi = a.ndesc - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.d[mid].tile0 <= t) lo = mid; else hi = mid - 1;
+    }
+    const A2ADesc& d = a.d[lo];
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(d.dst);
+    const uintptr_t d_end = d0 + d.bytes;
+    const uintptr_t base = d0 & ~static_cast<uintptr_t>(15);
+    const uint64_t k = t - d.tile0;
+    uintptr_t tlo = base + k * kA2ATileBytes;
+    uintptr_t thi = tlo + kA2ATileBytes;
+    if (tlo < d0) tlo = d0;
+    if (thi > d_end) thi = d_end;
+    const intptr_t shift = reinterpret_cast<intptr_t>(d.src) - reinterpret_cast<intptr_t>(d.dst);
+    copy_tile(tlo, thi, shift);
+  }
+}
+
+}  // namespace
+
+uint64_t a2a_tiles_for(const char* dst, uint64_t bytes) {
+  if (bytes == 0) return 0;
+  const uint64_t lead = reinterpret_cast<uintptr_t>(dst) & 15;
+  return (lead + bytes + kA2ATileBytes - 1) / kA2ATileBytes;
+}
+
+cudaError_t launch_a2av(const A2AArgs& a, cudaStream_t s) {
+  if (a.total_tiles == 0 || a.ndesc == 0) return cudaSuccess;
+  uint64_t g = a.total_tiles;
+  if (g > (1u << 30)) g = 1u << 30;
+  a2av_kernel<<<static_cast<unsigned>(g), kThreads, 0, s>>>(a);
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) note_launch();
+  return err;
+}
+
+}  // namespace ccl

@@ -1,0 +1,604 @@
+// ccl_api.cu -- the C ABI (include/ccl.h): argument checks, aliasing rules,
+// kernel selection, and the literal ring engine's step loop.
+//
+// Everything here is host code.  Invalid arguments are rejected before any
+// CUDA call, so the checks run (and are tested) on machines without a GPU.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "ccl_internal.h"
+
+namespace ccl {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int current_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+namespace {
+
+thread_local char t_error[512];
+
+void clear_error() { t_error[0] = '\0'; }
+
+ccl_status_t fail(ccl_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_error, sizeof(t_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+ccl_status_t cuda_fail(cudaError_t err, const char* what) {
+  return fail(CCL_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(err), cudaGetErrorName(err));
+}
+
+constexpr uint64_t kMaxElems = 1ull << 48;
+
+size_t elem_bytes(int dt) {
+  switch (dt) {
+    case CCL_F32: return 4;
+    case CCL_BF16: return 2;
+    case CCL_I32: return 4;
+    default: return 0;
+  }
+}
+
+bool valid_op(int op) { return op == CCL_SUM || op == CCL_MAX || op == CCL_MIN; }
+
+void chunk(int p, uint64_t n, int c, uint64_t* off, uint64_t* len) {
+  const uint64_t q = n / static_cast<uint64_t>(p), rem = n % static_cast<uint64_t>(p);
+  const uint64_t uc = static_cast<uint64_t>(c);
+  *off = uc * q + (uc < rem ? uc : rem);
+  *len = q + (uc < rem ? 1 : 0);
+}
+
+struct Span {
+  uintptr_t lo, hi;  // [lo, hi); empty when lo == hi
+  bool empty() const { return lo == hi; }
+};
+Span span(const void* p, uint64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Span{a, a + bytes};
+}
+bool overlaps(const Span& a, const Span& b) {
+  return !a.empty() && !b.empty() && a.lo < b.hi && b.lo < a.hi;
+}
+
+ccl_status_t check_p(int p) {
+  if (p < 1 || p > CCL_MAX_RANKS) return fail(CCL_ERR_INVALID_ARG, "p=%d outside 1..%d", p, CCL_MAX_RANKS);
+  return CCL_OK;
+}
+
+// Per-buffer checks: a buffer that holds bytes needs a non-NULL pointer
+// aligned to its element size.
+ccl_status_t check_buffers(const char* name, const void* const* ptrs, int p,
+                           const uint64_t* bytes, size_t align) {
+  if (ptrs == nullptr) return fail(CCL_ERR_INVALID_ARG, "%s is NULL", name);
+  for (int r = 0; r < p; ++r) {
+    if (bytes[r] == 0) continue;
+    if (ptrs[r] == nullptr) return fail(CCL_ERR_INVALID_ARG, "%s[%d] is NULL", name, r);
+    if (reinterpret_cast<uintptr_t>(ptrs[r]) % align != 0)
+      return fail(CCL_ERR_INVALID_ARG, "%s[%d] is not aligned to its %zu-byte elements", name, r, align);
+  }
+  return CCL_OK;
+}
+
+// Aliasing: outputs must not overlap one another; an output may overlap an
+// input only in the one in-place form the call allows (in_place[k] true when
+// recv[k] sits exactly where that form puts it relative to send[k]).
+ccl_status_t check_aliasing(const Span* in, const Span* out, const bool* in_place, int p) {
+  for (int i = 0; i < p; ++i) {
+    for (int j = i + 1; j < p; ++j)
+      if (overlaps(out[i], out[j]))
+        return fail(CCL_ERR_INVALID_ARG, "output buffers %d and %d overlap", i, j);
+    for (int j = 0; j < p; ++j) {
+      if (!overlaps(out[i], in[j])) continue;
+      if (i == j && in_place != nullptr && in_place[i]) continue;
+      return fail(CCL_ERR_INVALID_ARG, "output buffer %d overlaps input buffer %d", i, j);
+    }
+  }
+  return CCL_OK;
+}
+
+bool all_aligned16(const void* const* a, int p, const void* const* b) {
+  for (int r = 0; r < p; ++r) {
+    if (reinterpret_cast<uintptr_t>(a[r]) & 15) return false;
+    if (reinterpret_cast<uintptr_t>(b[r]) & 15) return false;
+  }
+  return true;
+}
+
+// Shared front half of the reducing calls: argument checks for AR / RS.
+// kind: 0 all-reduce, 1 reduce-scatter.
+ccl_status_t check_reduce(int kind, const void* const* send, void* const* recv, int p, size_t n,
+                          int dt, int op) {
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (!valid_op(op)) return fail(CCL_ERR_INVALID_ARG, "unknown op %d", op);
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  if (send == nullptr || recv == nullptr) return fail(CCL_ERR_INVALID_ARG, "send or recv array is NULL");
+  uint64_t in_bytes[CCL_MAX_RANKS], out_bytes[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  bool in_place[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    uint64_t off, len;
+    chunk(p, n, r, &off, &len);
+    in_bytes[r] = n * e;
+    out_bytes[r] = (kind == 0 ? n : len) * e;
+    in[r] = span(send[r], in_bytes[r]);
+    out[r] = span(recv[r], out_bytes[r]);
+    const uintptr_t where = reinterpret_cast<uintptr_t>(send[r]) + (kind == 0 ? 0 : off * e);
+    in_place[r] = reinterpret_cast<uintptr_t>(recv[r]) == where;
+  }
+  if ((st = check_buffers("send", send, p, in_bytes, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", const_cast<const void* const*>(recv), p, out_bytes, e)) != CCL_OK) return st;
+  return check_aliasing(in, out, in_place, p);
+}
+
+ccl_status_t check_gather(const void* const* send, void* const* recv, int p, size_t n, int dt) {
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  if (send == nullptr || recv == nullptr) return fail(CCL_ERR_INVALID_ARG, "send or recv array is NULL");
+  uint64_t in_bytes[CCL_MAX_RANKS], out_bytes[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  bool in_place[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    uint64_t off, len;
+    chunk(p, n, r, &off, &len);
+    in_bytes[r] = len * e;
+    out_bytes[r] = n * e;
+    in[r] = span(send[r], in_bytes[r]);
+    out[r] = span(recv[r], out_bytes[r]);
+    in_place[r] = reinterpret_cast<uintptr_t>(send[r]) == reinterpret_cast<uintptr_t>(recv[r]) + off * e;
+  }
+  if ((st = check_buffers("send", send, p, in_bytes, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", const_cast<const void* const*>(recv), p, out_bytes, e)) != CCL_OK) return st;
+  return check_aliasing(in, out, in_place, p);
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+}  // namespace ccl
+
+using namespace ccl;
+
+// ================================================================ utilities
+extern "C" int ccl_abi_version(void) { return CCL_ABI_VERSION; }
+
+extern "C" const char* ccl_status_string(ccl_status_t status) {
+  switch (status) {
+    case CCL_OK: return "CCL_OK";
+    case CCL_ERR_INVALID_ARG: return "CCL_ERR_INVALID_ARG: invalid argument";
+    case CCL_ERR_UNSUPPORTED: return "CCL_ERR_UNSUPPORTED: not implemented for these arguments";
+    case CCL_ERR_CUDA: return "CCL_ERR_CUDA: a CUDA call failed";
+    default: return "unknown ccl_status_t";
+  }
+}
+
+extern "C" const char* ccl_last_error(void) { return t_error; }
+
+extern "C" uint64_t ccl_kernel_launch_count(void) {
+  return g_launches.load(std::memory_order_relaxed);
+}
+
+extern "C" ccl_status_t ccl_chunk_bounds(int p, size_t n, int c, size_t* off, size_t* len) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  if (c < 0 || c >= p) return fail(CCL_ERR_INVALID_ARG, "chunk %d outside 0..%d", c, p - 1);
+  if (off == nullptr || len == nullptr) return fail(CCL_ERR_INVALID_ARG, "NULL output pointer");
+  uint64_t o, l;
+  chunk(p, n, c, &o, &l);
+  *off = static_cast<size_t>(o);
+  *len = static_cast<size_t>(l);
+  return CCL_OK;
+}
+
+// ====================================================== fused single-pass calls
+namespace {
+ccl_status_t fused_reduce(int mode, const void* const* send, void* const* recv, int p, size_t n,
+                          int dt, int op, void* stream) {
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.send[r] = send[r];
+    a.recv[r] = recv[r];
+  }
+  a.p = p;
+  a.q = n / static_cast<uint64_t>(p);
+  a.rem = n % static_cast<uint64_t>(p);
+  a.scale = 1.0f;
+  const bool vec = all_aligned16(send, p, const_cast<const void* const*>(recv));
+  cudaError_t err = launch_fold(mode, dt, op, vec, a, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "fold kernel launch");
+  return CCL_OK;
+}
+}  // namespace
+
+extern "C" ccl_status_t ccl_allreduce(const void* const* send, void* const* recv, int p, size_t n,
+                                      ccl_dtype_t dt, ccl_op_t op, void* stream) {
+  clear_error();
+  ccl_status_t st = check_reduce(0, send, recv, p, n, dt, op);
+  if (st != CCL_OK || n == 0) return st;
+  return fused_reduce(kModeAllReduce, send, recv, p, n, dt, op, stream);
+}
+
+extern "C" ccl_status_t ccl_reduce_scatter(const void* const* send, void* const* recv, int p,
+                                           size_t n, ccl_dtype_t dt, ccl_op_t op, void* stream) {
+  clear_error();
+  ccl_status_t st = check_reduce(1, send, recv, p, n, dt, op);
+  if (st != CCL_OK || n == 0) return st;
+  return fused_reduce(kModeReduceScatter, send, recv, p, n, dt, op, stream);
+}
+
+extern "C" ccl_status_t ccl_all_gather(const void* const* send, void* const* recv, int p, size_t n,
+                                       ccl_dtype_t dt, void* stream) {
+  clear_error();
+  ccl_status_t st = check_gather(send, recv, p, n, dt);
+  if (st != CCL_OK || n == 0) return st;
+  GatherArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.send[r] = send[r];
+    a.recv[r] = recv[r];
+  }
+  a.p = p;
+  a.q = n / static_cast<uint64_t>(p);
+  a.rem = n % static_cast<uint64_t>(p);
+  const bool vec = all_aligned16(send, p, const_cast<const void* const*>(recv));
+  cudaError_t err = launch_gather(dt, vec, a, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "all-gather kernel launch");
+  return CCL_OK;
+}
+
+extern "C" ccl_status_t ccl_bucket_allreduce_scale_cast(const float* const* grads,
+                                                        void* const* out_bf16, int p, size_t n,
+                                                        float scale, void* stream) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  if (grads == nullptr || out_bf16 == nullptr)
+    return fail(CCL_ERR_INVALID_ARG, "grads or out_bf16 array is NULL");
+  if (n == 0) return CCL_OK;
+  const void* const* send = reinterpret_cast<const void* const*>(grads);
+  uint64_t in_bytes[CCL_MAX_RANKS], out_bytes[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    in_bytes[r] = n * 4;
+    out_bytes[r] = n * 2;
+    in[r] = span(send[r], in_bytes[r]);
+    out[r] = span(out_bf16[r], out_bytes[r]);
+  }
+  if ((st = check_buffers("grads", send, p, in_bytes, 4)) != CCL_OK) return st;
+  if ((st = check_buffers("out_bf16", const_cast<const void* const*>(out_bf16), p, out_bytes, 2)) != CCL_OK)
+    return st;
+  if ((st = check_aliasing(in, out, nullptr, p)) != CCL_OK) return st;
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.send[r] = send[r];
+    a.recv[r] = out_bf16[r];
+  }
+  a.p = p;
+  a.q = n / static_cast<uint64_t>(p);
+  a.rem = n % static_cast<uint64_t>(p);
+  a.scale = scale;
+  const bool vec = all_aligned16(send, p, const_cast<const void* const*>(out_bf16));
+  cudaError_t err = launch_fold(kModeBucket, CCL_F32, CCL_SUM, vec, a, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "bucket kernel launch");
+  return CCL_OK;
+}
+
+// ============================================================== all-to-allv
+extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts,
+                                        void* const* recv, int p, size_t row_elems,
+                                        ccl_dtype_t dt, void* stream) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (send == nullptr || recv == nullptr || counts == nullptr)
+    return fail(CCL_ERR_INVALID_ARG, "send, recv or counts is NULL");
+  if (row_elems > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "row_elems=%zu too large", row_elems);
+  const uint64_t row_bytes = row_elems * e;
+  uint64_t in_rows[CCL_MAX_RANKS] = {0}, out_rows[CCL_MAX_RANKS] = {0};
+  for (int s = 0; s < p; ++s) {
+    for (int d = 0; d < p; ++d) {
+      const uint64_t c = counts[s * p + d];
+      if (c > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "counts[%d][%d] too large", s, d);
+      in_rows[s] += c;
+      out_rows[d] += c;
+    }
+  }
+  uint64_t in_bytes[CCL_MAX_RANKS], out_bytes[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    if (row_bytes != 0 && (in_rows[r] > kMaxElems / row_bytes || out_rows[r] > kMaxElems / row_bytes))
+      return fail(CCL_ERR_INVALID_ARG, "rank %d buffer too large", r);
+    in_bytes[r] = in_rows[r] * row_bytes;
+    out_bytes[r] = out_rows[r] * row_bytes;
+    in[r] = span(send[r], in_bytes[r]);
+    out[r] = span(recv[r], out_bytes[r]);
+  }
+  if ((st = check_buffers("send", send, p, in_bytes, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", const_cast<const void* const*>(recv), p, out_bytes, e)) != CCL_OK) return st;
+  if ((st = check_aliasing(in, out, nullptr, p)) != CCL_OK) return st;
+  if (row_bytes == 0) return CCL_OK;
+
+  // exclusive prefix sums: source s's block for d, destination d's block from s
+  uint64_t recv_row[CCL_MAX_RANKS] = {0};  // next free row of each destination
+  A2AArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int s = 0; s < p; ++s) {
+    uint64_t send_row = 0;
+    for (int d = 0; d < p; ++d) {
+      const uint64_t rows = counts[s * p + d];
+      if (rows != 0) {
+        A2ADesc& desc = a.d[a.ndesc];
+        desc.src = static_cast<const char*>(send[s]) + send_row * row_bytes;
+        desc.dst = static_cast<char*>(recv[d]) + recv_row[d] * row_bytes;
+        desc.bytes = rows * row_bytes;
+        desc.tile0 = a.total_tiles;
+        a.total_tiles += a2a_tiles_for(desc.dst, desc.bytes);
+        if (++a.ndesc == kA2AMaxDesc) {
+          cudaError_t err = launch_a2av(a, as_stream(stream));
+          if (err != cudaSuccess) return cuda_fail(err, "all-to-allv kernel launch");
+          memset(&a, 0, sizeof(a));
+        }
+      }
+      send_row += rows;
+      recv_row[d] += rows;
+    }
+  }
+  cudaError_t err = launch_a2av(a, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "all-to-allv kernel launch");
+  return CCL_OK;
+}
+
+// ====================================================== literal ring engine
+namespace {
+
+// Byte pointers to each rank's working buffer of n elements.
+struct Work {
+  char* b[CCL_MAX_RANKS];
+};
+
+ccl_status_t run_xfer(int kind, int dt, int op, const XferArgs& x, cudaStream_t s) {
+  cudaError_t err = launch_xfer(kind, dt, op, x, s);
+  if (err != cudaSuccess) return cuda_fail(err, "ring step launch");
+  return CCL_OK;
+}
+
+// Reduce-scatter phase: p-1 steps on working buffers of the accumulator type
+// (4-byte fp32 or int32).  Step s: rank r sends its partial of chunk
+// (r-s-1) mod p to rank r+1, which combines it with its own.
+ccl_status_t rs_phase(const Work& w, int p, uint64_t n, int acc_dt, int op, uint64_t* sent,
+                      cudaStream_t s) {
+  for (int step = 0; step < p - 1; ++step) {
+    XferArgs x;
+    memset(&x, 0, sizeof(x));
+    x.p = p;
+    for (int r = 0; r < p; ++r) {
+      const int c = ((r - step - 1) % p + p) % p;
+      uint64_t off, len;
+      chunk(p, n, c, &off, &len);
+      x.src[r] = w.b[r] + off * 4;
+      x.dst[r] = w.b[(r + 1) % p] + off * 4;
+      x.len[r] = len;
+      sent[r] += len * 4;
+    }
+    ccl_status_t st = run_xfer(kXferCombine, acc_dt, op, x, s);
+    if (st != CCL_OK) return st;
+  }
+  return CCL_OK;
+}
+
+// All-gather phase: p-1 steps on the output buffers.  Step s: rank r sends
+// chunk (r-s) mod p to rank r+1.
+ccl_status_t ag_phase(const Work& w, int p, uint64_t n, int dt, uint64_t* sent, cudaStream_t s) {
+  const size_t e = elem_bytes(dt);
+  for (int step = 0; step < p - 1; ++step) {
+    XferArgs x;
+    memset(&x, 0, sizeof(x));
+    x.p = p;
+    for (int r = 0; r < p; ++r) {
+      const int c = ((r - step) % p + p) % p;
+      uint64_t off, len;
+      chunk(p, n, c, &off, &len);
+      x.src[r] = w.b[r] + off * e;
+      x.dst[r] = w.b[(r + 1) % p] + off * e;
+      x.len[r] = len;
+      sent[r] += len * e;
+    }
+    ccl_status_t st = run_xfer(kXferCopy, dt, CCL_SUM, x, s);
+    if (st != CCL_OK) return st;
+  }
+  return CCL_OK;
+}
+
+// One launch of p per-rank moves: src[r] + src_off(r) -> dst[r] + dst_off(r).
+// `whole` true: n elements at offset 0; false: rank r's own chunk r.
+ccl_status_t per_rank_move(int kind, int dt, const char* const* src, bool src_chunk_off,
+                           char* const* dst, bool dst_chunk_off, bool whole, int p, uint64_t n,
+                           size_t src_e, size_t dst_e, cudaStream_t s) {
+  XferArgs x;
+  memset(&x, 0, sizeof(x));
+  x.p = p;
+  for (int r = 0; r < p; ++r) {
+    uint64_t off, len;
+    chunk(p, n, r, &off, &len);
+    x.src[r] = src[r] + (src_chunk_off ? off * src_e : 0);
+    x.dst[r] = dst[r] + (dst_chunk_off ? off * dst_e : 0);
+    x.len[r] = whole ? n : len;
+  }
+  return run_xfer(kind, dt, CCL_SUM, x, s);
+}
+
+ccl_status_t check_workspace(void* ws, size_t ws_bytes, size_t need, const void* const* send,
+                             const uint64_t* in_bytes, void* const* recv, const uint64_t* out_bytes,
+                             int p) {
+  if (need == 0) return CCL_OK;
+  if (ws == nullptr) return fail(CCL_ERR_INVALID_ARG, "workspace is NULL (%zu bytes needed)", need);
+  if (ws_bytes < need)
+    return fail(CCL_ERR_INVALID_ARG, "workspace has %zu bytes, %zu needed", ws_bytes, need);
+  if (reinterpret_cast<uintptr_t>(ws) % 4 != 0)
+    return fail(CCL_ERR_INVALID_ARG, "workspace is not 4-byte aligned");
+  const Span w = span(ws, need);
+  for (int r = 0; r < p; ++r) {
+    if (overlaps(w, span(send[r], in_bytes[r])) || overlaps(w, span(recv[r], out_bytes[r])))
+      return fail(CCL_ERR_INVALID_ARG, "workspace overlaps the buffers of rank %d", r);
+  }
+  return CCL_OK;
+}
+
+void write_sent(uint64_t* out, const uint64_t* sent, int p) {
+  if (out == nullptr) return;
+  for (int r = 0; r < p; ++r) out[r] = sent[r];
+}
+
+size_t literal_ws(int kind, int p, size_t n, int dt) {
+  if (p < 1 || p > CCL_MAX_RANKS || elem_bytes(dt) == 0 || n > kMaxElems) return 0;
+  if (kind == CCL_KIND_ALLREDUCE) return dt == CCL_BF16 ? static_cast<size_t>(p) * n * 4 : 0;
+  if (kind == CCL_KIND_REDUCE_SCATTER) return static_cast<size_t>(p) * n * 4;
+  return 0;
+}
+
+}  // namespace
+
+extern "C" size_t ccl_ring_literal_workspace_bytes(ccl_kind_t kind, int p, size_t n,
+                                                   ccl_dtype_t dt) {
+  return literal_ws(kind, p, n, dt);
+}
+
+extern "C" ccl_status_t ccl_ring_allreduce_literal(const void* const* send, void* const* recv,
+                                                   int p, size_t n, ccl_dtype_t dt, ccl_op_t op,
+                                                   uint64_t* bytes_sent, void* workspace,
+                                                   size_t workspace_bytes, void* stream) {
+  clear_error();
+  ccl_status_t st = check_reduce(0, send, recv, p, n, dt, op);
+  if (st != CCL_OK) return st;
+  uint64_t sent[CCL_MAX_RANKS] = {0};
+  if (n == 0) {
+    write_sent(bytes_sent, sent, p);
+    return CCL_OK;
+  }
+  const size_t e = elem_bytes(dt);
+  uint64_t nb[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) nb[r] = n * e;
+  const size_t need = literal_ws(CCL_KIND_ALLREDUCE, p, n, dt);
+  if ((st = check_workspace(workspace, workspace_bytes, need, send, nb, recv, nb, p)) != CCL_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  Work out;
+  for (int r = 0; r < p; ++r) out.b[r] = static_cast<char*>(recv[r]);
+  const char* const* src = reinterpret_cast<const char* const*>(send);
+
+  if (dt == CCL_BF16) {
+    // partials travel in fp32: widen into the workspace, reduce there, then the
+    // owner of each chunk rounds it once into its output buffer
+    Work ws;
+    for (int r = 0; r < p; ++r) ws.b[r] = static_cast<char*>(workspace) + static_cast<size_t>(r) * n * 4;
+    if ((st = per_rank_move(kXferWiden, CCL_BF16, src, false, ws.b, false, true, p, n, 2, 4, s)) != CCL_OK) return st;
+    if ((st = rs_phase(ws, p, n, CCL_F32, op, sent, s)) != CCL_OK) return st;
+    if ((st = per_rank_move(kXferNarrow, CCL_BF16, ws.b, true, out.b, true, false, p, n, 4, 2, s)) != CCL_OK) return st;
+  } else {
+    bool in_place = true;
+    for (int r = 0; r < p; ++r) in_place = in_place && (send[r] == recv[r]);
+    if (!in_place) {
+      if ((st = per_rank_move(kXferCopy, dt, src, false, out.b, false, true, p, n, e, e, s)) != CCL_OK) return st;
+    }
+    if ((st = rs_phase(out, p, n, dt, op, sent, s)) != CCL_OK) return st;
+  }
+  if ((st = ag_phase(out, p, n, dt, sent, s)) != CCL_OK) return st;
+  write_sent(bytes_sent, sent, p);
+  return CCL_OK;
+}
+
+extern "C" ccl_status_t ccl_ring_reduce_scatter_literal(const void* const* send, void* const* recv,
+                                                        int p, size_t n, ccl_dtype_t dt,
+                                                        ccl_op_t op, uint64_t* bytes_sent,
+                                                        void* workspace, size_t workspace_bytes,
+                                                        void* stream) {
+  clear_error();
+  ccl_status_t st = check_reduce(1, send, recv, p, n, dt, op);
+  if (st != CCL_OK) return st;
+  uint64_t sent[CCL_MAX_RANKS] = {0};
+  if (n == 0) {
+    write_sent(bytes_sent, sent, p);
+    return CCL_OK;
+  }
+  const size_t e = elem_bytes(dt);
+  uint64_t in_b[CCL_MAX_RANKS], out_b[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    uint64_t off, len;
+    chunk(p, n, r, &off, &len);
+    in_b[r] = n * e;
+    out_b[r] = len * e;
+  }
+  const size_t need = literal_ws(CCL_KIND_REDUCE_SCATTER, p, n, dt);
+  if ((st = check_workspace(workspace, workspace_bytes, need, send, in_b, recv, out_b, p)) != CCL_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  Work ws;
+  for (int r = 0; r < p; ++r) ws.b[r] = static_cast<char*>(workspace) + static_cast<size_t>(r) * n * 4;
+  char* out[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) out[r] = static_cast<char*>(recv[r]);
+  const char* const* src = reinterpret_cast<const char* const*>(send);
+  const int acc_dt = (dt == CCL_I32) ? CCL_I32 : CCL_F32;
+  if (dt == CCL_BF16) {
+    if ((st = per_rank_move(kXferWiden, CCL_BF16, src, false, ws.b, false, true, p, n, 2, 4, s)) != CCL_OK) return st;
+  } else {
+    if ((st = per_rank_move(kXferCopy, dt, src, false, ws.b, false, true, p, n, 4, 4, s)) != CCL_OK) return st;
+  }
+  if ((st = rs_phase(ws, p, n, acc_dt, op, sent, s)) != CCL_OK) return st;
+  // rank k's finished chunk k -> its shard
+  const int finish = (dt == CCL_BF16) ? kXferNarrow : kXferCopy;
+  if ((st = per_rank_move(finish, dt, ws.b, true, out, false, false, p, n, 4, e, s)) != CCL_OK) return st;
+  write_sent(bytes_sent, sent, p);
+  return CCL_OK;
+}
+
+extern "C" ccl_status_t ccl_ring_all_gather_literal(const void* const* send, void* const* recv,
+                                                    int p, size_t n, ccl_dtype_t dt,
+                                                    uint64_t* bytes_sent, void* stream) {
+  clear_error();
+  ccl_status_t st = check_gather(send, recv, p, n, dt);
+  if (st != CCL_OK) return st;
+  uint64_t sent[CCL_MAX_RANKS] = {0};
+  if (n == 0) {
+    write_sent(bytes_sent, sent, p);
+    return CCL_OK;
+  }
+  const size_t e = elem_bytes(dt);
+  cudaStream_t s = as_stream(stream);
+  Work out;
+  for (int r = 0; r < p; ++r) out.b[r] = static_cast<char*>(recv[r]);
+  bool in_place = true;
+  for (int r = 0; r < p; ++r) {
+    uint64_t off, len;
+    chunk(p, n, r, &off, &len);
+    in_place = in_place && (static_cast<const char*>(send[r]) == out.b[r] + off * e || len == 0);
+  }
+  if (!in_place) {
+    const char* const* src = reinterpret_cast<const char* const*>(send);
+    if ((st = per_rank_move(kXferCopy, dt, src, false, out.b, true, false, p, n, e, e, s)) != CCL_OK) return st;
+  }
+  if ((st = ag_phase(out, p, n, dt, sent, s)) != CCL_OK) return st;
+  write_sent(bytes_sent, sent, p);
+  return CCL_OK;
+}

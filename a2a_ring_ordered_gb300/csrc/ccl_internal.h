@@ -1,0 +1,86 @@
+// ccl_internal.h -- parameter blocks and kernel launchers behind the C ABI.
+//
+// Every kernel receives its rank pointers by value in a __grid_constant__
+// parameter block (at most 4 KB), so a call needs no device memory of its own.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ccl.h"
+
+namespace ccl {
+
+// ------------------------------------------------ fused fold (AR / RS / bucket)
+enum FoldMode : int {
+  kModeAllReduce = 0,      // fold, write the result to every rank's buffer
+  kModeReduceScatter = 1,  // fold, write chunk c only to rank c's shard
+  kModeBucket = 2          // fold fp32, scale, round to bf16, write to every rank
+};
+
+struct FoldArgs {
+  const void* send[CCL_MAX_RANKS];
+  void* recv[CCL_MAX_RANKS];
+  uint64_t q;    // floor(n / p)
+  uint64_t rem;  // n mod p
+  int p;
+  float scale;   // bucket mode only
+};
+
+// `vec`: every pointer is 16-byte aligned, so 16-byte vectors may be used.
+cudaError_t launch_fold(int mode, int dt, int op, bool vec, const FoldArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- all-gather
+struct GatherArgs {
+  const void* send[CCL_MAX_RANKS];  // rank k's block (len(k) elements)
+  void* recv[CCL_MAX_RANKS];        // full n-element outputs
+  uint64_t q, rem;
+  int p;
+};
+cudaError_t launch_gather(int dt, bool vec, const GatherArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------- all-to-allv
+// One contiguous byte block src -> dst.  Blocks are cut into tiles of
+// kA2ATileBytes measured from dst rounded down to 16 bytes; tile0 is the
+// index of the block's first tile in the launch.
+struct A2ADesc {
+  const char* src;
+  char* dst;
+  uint64_t bytes;
+  uint64_t tile0;
+};
+constexpr int kA2AMaxDesc = 112;  // 112 * 32 B + header < 4 KB of parameters
+constexpr uint64_t kA2ATileBytes = 32768;
+struct A2AArgs {
+  uint64_t total_tiles;
+  int ndesc;
+  A2ADesc d[kA2AMaxDesc];
+};
+uint64_t a2a_tiles_for(const char* dst, uint64_t bytes);
+cudaError_t launch_a2av(const A2AArgs& a, cudaStream_t s);
+
+// ------------------------------------------------- literal ring engine steps
+// One launch moves p independent transfers, transfer r: src[r] -> dst[r],
+// len[r] elements.  Kinds:
+enum XferKind : int {
+  kXferCopy = 0,     // dst = src (element type dt)
+  kXferCombine = 1,  // dst = combine(src, dst): received partial (+) own value
+  kXferWiden = 2,    // bf16 src -> fp32 dst (exact)
+  kXferNarrow = 3    // fp32 src -> bf16 dst (round to nearest even)
+};
+struct XferArgs {
+  const char* src[CCL_MAX_RANKS];
+  char* dst[CCL_MAX_RANKS];
+  uint64_t len[CCL_MAX_RANKS];
+  int p;
+};
+cudaError_t launch_xfer(int kind, int dt, int op, const XferArgs& a, cudaStream_t s);
+
+// Records one successful kernel launch (ccl_kernel_launch_count).
+void note_launch();
+
+// Streaming multiprocessors of the current device (0 if unknown).
+int current_sm_count();
+
+}  // namespace ccl

@@ -1,0 +1,177 @@
+// device_common.cuh -- element types, streaming memory access and the fold
+// operator shared by the ring-ordered collective kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "ccl_internal.h"
+
+namespace ccl {
+
+constexpr int kThreads = 256;  // threads per CTA for every streaming kernel
+
+// ------------------------------------------------------------ element types
+// Element type tags.  Acc is the register type partial sums travel in: fp32
+// for fp32 and bf16 data, int32 for int32 data.
+enum Dt : int { kF32 = CCL_F32, kBF16 = CCL_BF16, kI32 = CCL_I32 };
+
+template <int DT> struct Elem;
+template <> struct Elem<kF32> { using Acc = float; static constexpr int kBytes = 4; };
+template <> struct Elem<kBF16> { using Acc = float; static constexpr int kBytes = 2; };
+template <> struct Elem<kI32> { using Acc = int32_t; static constexpr int kBytes = 4; };
+
+// ------------------------------------------------------- global memory access
+// Every input element is read exactly once, so loads bypass L1 and use the
+// read-only path; outputs are written once and never re-read, so stores are
+// marked streaming (evict-first).
+__device__ __forceinline__ uint4 ld_once16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_once4(const void* p) {
+  uint32_t v;
+  asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_once2(const void* p) {
+  unsigned short v;
+  asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_stream2(void* p, uint32_t v) {
+  unsigned short h = static_cast<unsigned short>(v);
+  asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(h) : "memory");
+}
+
+// Load VEC consecutive elements starting at element `i` of `base` as raw
+// 32-bit words (VEC * bytes / 4 words; a lone bf16 occupies the low half).
+// VEC > 1 requires a 16-byte aligned address and VEC * bytes % 16 == 0.
+template <int DT, int VEC>
+__device__ __forceinline__ void load_raw(const void* base, uint64_t i, uint32_t* w) {
+  constexpr int B = Elem<DT>::kBytes;
+  const char* p = static_cast<const char*>(base) + i * B;
+  if constexpr (VEC * B >= 16) {
+#pragma unroll
+    for (int k = 0; k < VEC * B / 16; ++k) {
+      uint4 v = ld_once16(p + 16 * k);
+      w[4 * k + 0] = v.x;
+      w[4 * k + 1] = v.y;
+      w[4 * k + 2] = v.z;
+      w[4 * k + 3] = v.w;
+    }
+  } else {
+    static_assert(VEC == 1, "sub-16-byte loads are element-wise");
+    w[0] = (B == 4) ? ld_once4(p) : ld_once2(p);
+  }
+}
+
+// Element e of a raw word array, widened exactly to the accumulator type.
+template <int DT>
+__device__ __forceinline__ typename Elem<DT>::Acc widen(const uint32_t* w, int e) {
+  if constexpr (DT == kF32) {
+    return __uint_as_float(w[e]);
+  } else if constexpr (DT == kI32) {
+    return static_cast<int32_t>(w[e]);
+  } else {
+    // bf16 is the top half of a binary32: append 16 zero bits.
+    const uint32_t word = w[e >> 1];
+    return __uint_as_float((e & 1) ? (word & 0xFFFF0000u) : (word << 16));
+  }
+}
+
+// ---------------------------------------------------------------- the fold
+// What a receiving rank computes from the partial it got (`acc`) and its own
+// value (`x`).  SUM: IEEE fp32 add (round to nearest even) or wrapping int32
+// add.  MAX / MIN: keep `x` only when strictly greater / smaller.
+template <int OP, typename T>
+__device__ __forceinline__ T combine(T acc, T x) {
+  if constexpr (OP == CCL_SUM) {
+    if constexpr (std::is_floating_point<T>::value) {
+      return __fadd_rn(acc, x);
+    } else {
+      return static_cast<T>(static_cast<uint32_t>(acc) + static_cast<uint32_t>(x));
+    }
+  } else if constexpr (OP == CCL_MAX) {
+    return (x > acc) ? x : acc;
+  } else {
+    return (x < acc) ? x : acc;
+  }
+}
+
+// Pack accumulator values into output raw words (VEC * out_bytes / 4 words).
+// bf16 output rounds each fp32 value to nearest even.
+template <int DT_OUT, int VEC, typename Acc>
+__device__ __forceinline__ void pack_out(const Acc* acc, uint32_t* w) {
+  if constexpr (DT_OUT == kF32) {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) w[e] = __float_as_uint(acc[e]);
+  } else if constexpr (DT_OUT == kI32) {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) w[e] = static_cast<uint32_t>(acc[e]);
+  } else {
+    if constexpr (VEC == 1) {
+      w[0] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[0]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; e += 2) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(acc[e], acc[e + 1]);
+        w[e >> 1] = *reinterpret_cast<uint32_t*>(&h);
+      }
+    }
+  }
+}
+
+// Store VEC elements (raw words) at element `i` of `base`.
+template <int DT_OUT, int VEC>
+__device__ __forceinline__ void store_raw(void* base, uint64_t i, const uint32_t* w) {
+  constexpr int B = Elem<DT_OUT>::kBytes;
+  char* p = static_cast<char*>(base) + i * B;
+  if constexpr (VEC * B >= 16) {
+#pragma unroll
+    for (int k = 0; k < VEC * B / 16; ++k)
+      st_stream16(p + 16 * k, make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]));
+  } else {
+    static_assert(VEC == 1, "sub-16-byte stores are element-wise");
+    if constexpr (B == 4) st_stream4(p, w[0]); else st_stream2(p, w[0]);
+  }
+}
+
+// Store element e of a raw word array (element-wise edge path).
+template <int DT_OUT>
+__device__ __forceinline__ void store_one(void* base, uint64_t i, const uint32_t* w, int e) {
+  constexpr int B = Elem<DT_OUT>::kBytes;
+  char* p = static_cast<char*>(base) + i * B;
+  if constexpr (B == 4) {
+    st_stream4(p, w[e]);
+  } else {
+    st_stream2(p, (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
+  }
+}
+
+// ------------------------------------------------------------- chunk rule
+// Chunk c of an n-element buffer split p ways: the first n mod p chunks hold
+// one extra element (numpy's array_split).
+struct Chunk {
+  uint64_t off, len;
+};
+__device__ __forceinline__ Chunk chunk_of(int c, uint64_t q, uint64_t rem) {
+  const uint64_t uc = static_cast<uint64_t>(c);
+  return Chunk{uc * q + (uc < rem ? uc : rem), q + (uc < rem ? 1u : 0u)};
+}
+
+}  // namespace ccl

@@ -1,0 +1,175 @@
+// fold.cu -- fused single-pass ring-ordered reduction kernels.
+//
+// The ring all-reduce ("Networks and Collective Communication" section 5.1;
+// "dist_train", Ring Algorithm) moves chunk c's partial sum once around the
+// ring, starting at rank c+1 and ending at rank c, then copies the finished
+// chunk to every rank.  On one GPU every rank's buffer is in the same HBM, so
+// one thread can play the whole walk for its elements: it loads the p ranks'
+// values of one 16-byte vector in ring order, folds them in that order in
+// fp32 (int32) registers and writes the result once per output.  The fold
+// order, and therefore every bit of the result, is the ring's.
+//
+// Grid: blockIdx.y = chunk c, so the starting rank is uniform per CTA;
+// blockIdx.x strides over the chunk's 16-byte-aligned vectors.  The few
+// elements of a chunk that do not fill a whole aligned vector (chunk edges
+// when p does not divide n, or a ragged tail) are folded element by element
+// by CTA (0, c).
+//
+// HBM traffic per element index: p reads of the input type, plus p writes
+// (all-reduce, bucket) or 1 write (reduce-scatter) of the output type --
+// exactly the primitives' minimum bytes.
+#include "device_common.cuh"
+
+namespace ccl {
+namespace {
+
+template <int DT_IN, int DT_OUT>
+__host__ __device__ constexpr int vec_width() {
+  // 16 bytes of input per rank (two 16-byte loads when fp32 is cast to bf16,
+  // so that the bf16 output is also a whole 16-byte store)
+  return (DT_IN == kF32 && DT_OUT == kBF16) ? 8 : 16 / Elem<DT_IN>::kBytes;
+}
+
+__host__ __device__ constexpr int words_for(int vec, int bytes) { return (vec * bytes + 3) / 4; }
+
+// Fold VEC elements starting at element i, in ring order from rank `first`.
+template <int DT_IN, int VEC, int OP>
+__device__ __forceinline__ void fold_elements(const FoldArgs& a, int p, int first, uint64_t i,
+                                              typename Elem<DT_IN>::Acc* acc) {
+  constexpr int WI = words_for(VEC, Elem<DT_IN>::kBytes);
+  // ranks whose loads are issued together before any of them is folded
+  constexpr int BATCH = (WI >= 8) ? 8 : 16;
+  int r = first;
+  for (int j0 = 0; j0 < p; j0 += BATCH) {
+    uint32_t raw[BATCH][WI];
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      if (j0 + b < p) {
+        load_raw<DT_IN, VEC>(a.send[r], i, raw[b]);
+        r = (r + 1 == p) ? 0 : r + 1;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      if (j0 + b < p) {
+        if (j0 + b == 0) {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[e] = widen<DT_IN>(raw[b], e);
+        } else {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[e] = combine<OP>(acc[e], widen<DT_IN>(raw[b], e));
+        }
+      }
+    }
+  }
+}
+
+// Write the folded values of elements [i, i+VEC) of chunk c.
+template <int DT_OUT, int VEC, int MODE, typename Acc>
+__device__ __forceinline__ void emit(const FoldArgs& a, int p, int c, const Chunk& ch,
+                                     uint64_t i, Acc* acc) {
+  if constexpr (MODE == kModeBucket) {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = __fmul_rn(acc[e], a.scale);
+  }
+  uint32_t w[words_for(VEC, Elem<DT_OUT>::kBytes)];
+  pack_out<DT_OUT, VEC>(acc, w);
+  if constexpr (MODE == kModeReduceScatter) {
+    const uint64_t j = i - ch.off;  // position in rank c's shard
+    if (VEC == 1 || (ch.off % VEC) == 0) {
+      store_raw<DT_OUT, VEC>(a.recv[c], j, w);
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) store_one<DT_OUT>(a.recv[c], j + e, w, e);
+    }
+  } else {
+    for (int r = 0; r < p; ++r) store_raw<DT_OUT, VEC>(a.recv[r], i, w);
+  }
+}
+
+template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE>
+__global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ FoldArgs a) {
+  using Acc = typename Elem<DT_IN>::Acc;
+  const int p = a.p;
+  const int c = blockIdx.y;
+  const Chunk ch = chunk_of(c, a.q, a.rem);
+  const uint64_t end = ch.off + ch.len;
+  const uint64_t v_lo = (ch.off + VEC - 1) / VEC;  // first whole vector inside chunk c
+  const uint64_t v_hi = end / VEC;                 // one past the last
+  const int first = (c + 1 == p) ? 0 : c + 1;      // the rank that starts chunk c
+
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  for (uint64_t v = v_lo + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi;
+       v += stride) {
+    Acc acc[VEC];
+    fold_elements<DT_IN, VEC, OP>(a, p, first, v * VEC, acc);
+    emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc);
+  }
+
+  if (VEC > 1 && blockIdx.x == 0) {
+    // element-wise edges: [off, head_end) and [tail_begin, end)
+    const uint64_t head_end = (v_lo * VEC < end) ? v_lo * VEC : end;
+    const uint64_t tail_begin = (v_hi * VEC > head_end) ? v_hi * VEC : head_end;
+    const uint64_t n_head = head_end - ch.off;
+    const uint64_t n_edge = n_head + (end - tail_begin);
+    for (uint64_t t = threadIdx.x; t < n_edge; t += kThreads) {
+      const uint64_t i = (t < n_head) ? ch.off + t : tail_begin + (t - n_head);
+      Acc acc[1];
+      fold_elements<DT_IN, 1, OP>(a, p, first, i, acc);
+      emit<DT_OUT, 1, MODE>(a, p, c, ch, i, acc);
+    }
+  }
+}
+
+constexpr int kVectorsPerThread = 2;
+
+template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE>
+cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
+  const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
+  uint64_t gx = (per_chunk + kThreads * kVectorsPerThread - 1) / (kThreads * kVectorsPerThread);
+  if (gx < 1) gx = 1;
+  if (gx > (1u << 30)) gx = 1u << 30;
+  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.p));
+  fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE><<<grid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DT_IN, int DT_OUT, int OP, int MODE>
+cudaError_t launch_typed(bool vec, const FoldArgs& a, cudaStream_t s) {
+  if (vec) return launch_one<DT_IN, DT_OUT, vec_width<DT_IN, DT_OUT>(), OP, MODE>(a, s);
+  return launch_one<DT_IN, DT_OUT, 1, OP, MODE>(a, s);
+}
+
+template <int MODE>
+cudaError_t launch_mode(int dt, int op, bool vec, const FoldArgs& a, cudaStream_t s) {
+#define CCL_FOLD_CASE(DT, OP)                                     \
+  if (dt == DT && op == OP) return launch_typed<DT, DT, OP, MODE>(vec, a, s);
+  CCL_FOLD_CASE(kF32, CCL_SUM)
+  CCL_FOLD_CASE(kF32, CCL_MAX)
+  CCL_FOLD_CASE(kF32, CCL_MIN)
+  CCL_FOLD_CASE(kBF16, CCL_SUM)
+  CCL_FOLD_CASE(kBF16, CCL_MAX)
+  CCL_FOLD_CASE(kBF16, CCL_MIN)
+  CCL_FOLD_CASE(kI32, CCL_SUM)
+  CCL_FOLD_CASE(kI32, CCL_MAX)
+  CCL_FOLD_CASE(kI32, CCL_MIN)
+#undef CCL_FOLD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_fold(int mode, int dt, int op, bool vec, const FoldArgs& a, cudaStream_t s) {
+  cudaError_t err = cudaErrorInvalidValue;
+  if (mode == kModeAllReduce) {
+    err = launch_mode<kModeAllReduce>(dt, op, vec, a, s);
+  } else if (mode == kModeReduceScatter) {
+    err = launch_mode<kModeReduceScatter>(dt, op, vec, a, s);
+  } else if (mode == kModeBucket) {
+    err = launch_typed<kF32, kBF16, CCL_SUM, kModeBucket>(vec, a, s);
+  }
+  if (err == cudaSuccess) note_launch();
+  return err;
+}
+
+}  // namespace ccl

@@ -1,0 +1,102 @@
+// gather.cu -- all-gather: rank k's block is copied to offset off(k) of every
+// rank's output ("Networks and Collective Communication" section 4.1: each
+// device contributes one block and everyone gets the whole concatenation).
+//
+// The ring's all-gather phase forwards each finished chunk p-1 times; on one
+// GPU the same result is one read of block k and p writes of it.  Grid:
+// blockIdx.y = block k; vectors are aligned in output space, and the source
+// side uses 16-byte loads too whenever off(k) keeps it aligned.
+// HBM traffic: n reads + p*n writes of the element type.
+#include "device_common.cuh"
+
+namespace ccl {
+namespace {
+
+// Load VEC elements one at a time into packed raw words (unaligned source).
+template <int DT, int VEC>
+__device__ __forceinline__ void load_elems(const void* base, uint64_t i, uint32_t* w) {
+  constexpr int B = Elem<DT>::kBytes;
+  if constexpr (B == 4) {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) load_raw<DT, 1>(base, i + e, &w[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < VEC; e += 2) {
+      uint32_t lo, hi;
+      load_raw<DT, 1>(base, i + e, &lo);
+      load_raw<DT, 1>(base, i + e + 1, &hi);
+      w[e >> 1] = (lo & 0xFFFFu) | (hi << 16);
+    }
+  }
+}
+
+template <int DT, int VEC>
+__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
+  constexpr int W = (VEC * Elem<DT>::kBytes + 3) / 4;
+  const int p = a.p;
+  const int k = blockIdx.y;
+  const Chunk ch = chunk_of(k, a.q, a.rem);
+  const uint64_t end = ch.off + ch.len;
+  const uint64_t v_lo = (ch.off + VEC - 1) / VEC;
+  const uint64_t v_hi = end / VEC;
+  const void* src = a.send[k];
+  const bool src_aligned = (ch.off % VEC) == 0;
+
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  for (uint64_t v = v_lo + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi;
+       v += stride) {
+    const uint64_t i = v * VEC;
+    uint32_t w[W];
+    if (VEC == 1 || src_aligned) {
+      load_raw<DT, VEC>(src, i - ch.off, w);
+    } else {
+      load_elems<DT, VEC>(src, i - ch.off, w);
+    }
+    for (int r = 0; r < p; ++r) store_raw<DT, VEC>(a.recv[r], i, w);
+  }
+
+  if (VEC > 1 && blockIdx.x == 0) {
+    const uint64_t head_end = (v_lo * VEC < end) ? v_lo * VEC : end;
+    const uint64_t tail_begin = (v_hi * VEC > head_end) ? v_hi * VEC : head_end;
+    const uint64_t n_head = head_end - ch.off;
+    const uint64_t n_edge = n_head + (end - tail_begin);
+    for (uint64_t t = threadIdx.x; t < n_edge; t += kThreads) {
+      const uint64_t i = (t < n_head) ? ch.off + t : tail_begin + (t - n_head);
+      uint32_t w[1];
+      load_raw<DT, 1>(src, i - ch.off, w);
+      for (int r = 0; r < p; ++r) store_raw<DT, 1>(a.recv[r], i, w);
+    }
+  }
+}
+
+constexpr int kVectorsPerThread = 2;
+
+template <int DT, int VEC>
+cudaError_t launch_one(const GatherArgs& a, cudaStream_t s) {
+  const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
+  uint64_t gx = (per_chunk + kThreads * kVectorsPerThread - 1) / (kThreads * kVectorsPerThread);
+  if (gx < 1) gx = 1;
+  if (gx > (1u << 30)) gx = 1u << 30;
+  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.p));
+  gather_kernel<DT, VEC><<<grid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_typed(bool vec, const GatherArgs& a, cudaStream_t s) {
+  if (vec) return launch_one<DT, 16 / Elem<DT>::kBytes>(a, s);
+  return launch_one<DT, 1>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gather(int dt, bool vec, const GatherArgs& a, cudaStream_t s) {
+  cudaError_t err = cudaErrorInvalidValue;
+  // a copy only needs the element width: fp32 and int32 share one kernel
+  if (dt == kF32 || dt == kI32) err = launch_typed<kF32>(vec, a, s);
+  else if (dt == kBF16) err = launch_typed<kBF16>(vec, a, s);
+  if (err == cudaSuccess) note_launch();
+  return err;
+}
+
+}  // namespace ccl

@@ -1,0 +1,187 @@
+/*
+ * ccl.h -- ring-ordered collectives over p virtual ranks on one GB300 GPU.
+ *
+ * A "rank" is a buffer in this GPU's HBM.  Every collective takes HOST arrays
+ * of p DEVICE pointers (one buffer per virtual rank), the element count, the
+ * element type and the reduction, and enqueues its kernels on `stream`.
+ *
+ * Primitive semantics follow "Networks and Collective Communication"
+ * (section 4.1, what each collective does; section 4.2, identities) and
+ * "dist_train" (section "Collective Communication Primitives").  Reductions
+ * follow the ring of "Networks and Collective Communication" section 5.1 and
+ * "dist_train" section "Ring Algorithm": each chunk's partial sum walks the
+ * ring once, and its fold order is fixed by that walk (see CHUNKS AND ORDER).
+ *
+ * CHUNKS AND ORDER.  A rank buffer of n elements is cut into p chunks; chunk c
+ * has len(c) = floor(n/p) + (c < n mod p) elements and starts at
+ * off(c) = c*floor(n/p) + min(c, n mod p)  (ccl_chunk_bounds).  Rank r passes
+ * to rank r+1 (mod p).  Chunk c's partial starts at rank c+1 and visits ranks
+ * c+2, ..., p-1, 0, ..., c, each adding its own value: for SUM the result is
+ * ((x[c+1] + x[c+2]) + ...) + x[c], in fp32 for fp32 and bf16 data (bf16 is
+ * widened exactly, summed in fp32 and rounded once, to nearest even) and in
+ * wrapping two's-complement int32 for int32 data.  Rank k ends the
+ * reduce-scatter phase owning chunk k.  Every entry point that reduces gives
+ * results bit-identical to that walk.
+ *
+ * OWNERSHIP.  The caller owns every buffer.  The library keeps no state
+ * between calls and allocates no device memory; pointer arrays are copied
+ * into kernel parameters before a call returns, so they may be reused at
+ * once.  Calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream); nothing synchronises unless the caller does.
+ *
+ * ERRORS.  Every entry point returns a ccl_status_t and never aborts.
+ * Argument errors are detected on the host before anything is enqueued;
+ * ccl_last_error() then gives a one-line reason (per calling thread).
+ * Device pointers must be device-accessible and aligned to their element
+ * size; 16-byte alignment of every pointer selects the vectorised kernels,
+ * any other element-aligned pointer runs the element-wise kernels.
+ */
+#ifndef CCL_H_
+#define CCL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CCL_ABI_VERSION 1
+#define CCL_MAX_RANKS 128
+
+typedef enum {
+  CCL_OK = 0,
+  CCL_ERR_INVALID_ARG = 1, /* bad p, pointer, size, alignment or aliasing */
+  CCL_ERR_UNSUPPORTED = 2, /* valid arguments this build does not implement */
+  CCL_ERR_CUDA = 3         /* a CUDA call or kernel launch failed */
+} ccl_status_t;
+
+typedef enum { CCL_F32 = 0, CCL_BF16 = 1, CCL_I32 = 2 } ccl_dtype_t;
+
+/* SUM is the pages' reduction.  MAX / MIN are extras: the receiving rank keeps
+ * its own value when it is strictly greater (smaller) than the partial it got,
+ * so ties and NaNs resolve in ring order too. */
+typedef enum { CCL_SUM = 0, CCL_MAX = 1, CCL_MIN = 2 } ccl_op_t;
+
+typedef enum {
+  CCL_KIND_ALLREDUCE = 0,
+  CCL_KIND_REDUCE_SCATTER = 1,
+  CCL_KIND_ALL_GATHER = 2
+} ccl_kind_t;
+
+/* ------------------------------------------------------------- utilities */
+
+/* CCL_ABI_VERSION of the loaded library. */
+int ccl_abi_version(void);
+
+/* Static text for a status code; never NULL. */
+const char* ccl_status_string(ccl_status_t status);
+
+/* One-line reason for the last non-OK status returned to this thread ("" if
+ * none).  The pointer stays valid until this thread's next call. */
+const char* ccl_last_error(void);
+
+/* Number of kernels this library has launched in this process (all threads). */
+uint64_t ccl_kernel_launch_count(void);
+
+/* Chunk c of an n-element buffer cut into p chunks (the rule under CHUNKS AND
+ * ORDER; numpy's array_split).  Host only.  Errors: p outside 1..CCL_MAX_RANKS,
+ * c outside 0..p-1, or a NULL output pointer -> CCL_ERR_INVALID_ARG. */
+ccl_status_t ccl_chunk_bounds(int p, size_t n, int c, size_t* off, size_t* len);
+
+/* -------------------------------------------------- fused single-pass kernels
+ * One kernel reads every rank's element once, folds in ring order in fp32
+ * (int32) registers and writes each output once.  Results are bit-identical
+ * to the step-by-step ring. */
+
+/* All-reduce ("Networks and Collective Communication" 4.1: everyone gets the
+ * element-wise sum; 5.1: ring = reduce-scatter then all-gather).
+ *   send[r]  p device pointers, each n elements of dt.
+ *   recv[r]  p device pointers, each n elements of dt; recv[r] == send[r] is
+ *            allowed (in place); any other overlap -> CCL_ERR_INVALID_ARG.
+ * Every recv[r] receives the same ring-ordered reduction.  n == 0 is a no-op. */
+ccl_status_t ccl_allreduce(const void* const* send, void* const* recv, int p, size_t n,
+                           ccl_dtype_t dt, ccl_op_t op, void* stream);
+
+/* Reduce-scatter ("dist_train": process k gets sum_i x_i^(k); ZeRO's key op).
+ *   send[r]  p device pointers, each n elements.
+ *   recv[k]  p device pointers; recv[k] holds len(k) elements: chunk k of the
+ *            ring-ordered reduction.  In place is allowed only as
+ *            recv[k] == send[k] + off(k) elements; other overlaps are errors. */
+ccl_status_t ccl_reduce_scatter(const void* const* send, void* const* recv, int p, size_t n,
+                                ccl_dtype_t dt, ccl_op_t op, void* stream);
+
+/* All-gather ("Networks and Collective Communication" 4.1: each device
+ * contributes one block and everyone gets the whole concatenation).
+ *   send[k]  p device pointers; send[k] holds len(k) elements (block k).
+ *   recv[r]  p device pointers, each n elements; block k lands at off(k).
+ *            In place is allowed only as send[k] == recv[k] + off(k)
+ *            elements.  Pure copy: bit-exact for every dtype. */
+ccl_status_t ccl_all_gather(const void* const* send, void* const* recv, int p, size_t n,
+                            ccl_dtype_t dt, void* stream);
+
+/* DDP gradient-bucket all-reduce with the average and the cast fused in
+ * ("dist_train", Communication-Computation Overlap: DDP cuts gradients into
+ * buckets of bucket_cap_mb = 25 and all-reduces each finished bucket).
+ *   grads[r]    p device pointers, n fp32 gradients each.
+ *   out_bf16[r] p device pointers, n bf16 each; no overlap with any grads
+ *               buffer or other output is allowed (the cast halves the width).
+ * out = bf16_round_nearest_even( fp32(ring_sum) * scale ); pass scale = 1/p
+ * for the DDP average. */
+ccl_status_t ccl_bucket_allreduce_scale_cast(const float* const* grads, void* const* out_bf16,
+                                             int p, size_t n, float scale, void* stream);
+
+/* All-to-all with per-pair counts: the MoE dispatch / combine block transpose
+ * ("Networks and Collective Communication" 4.1: device i's block j goes to
+ * device j; 7.4: MoE dispatch and combine).
+ *   counts     HOST array of p*p row counts, counts[s*p + d] = rows that
+ *              source s sends to destination d.
+ *   send[s]    sum_d counts[s][d] rows of row_elems elements; the block for d
+ *              starts at row sum_{d' < d} counts[s][d'].
+ *   recv[d]    sum_s counts[s][d] rows; the block from s lands at row
+ *              sum_{s' < s} counts[s'][d].
+ * Combine is the same call on the received buffers with counts transposed.
+ * Buffers must not overlap.  Bit-exact copy for every dtype. */
+ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts, void* const* recv,
+                             int p, size_t row_elems, ccl_dtype_t dt, void* stream);
+
+/* ------------------------------------------------------- literal ring engine
+ * Executes the ring schedule as written: the reduce-scatter phase's p-1 steps
+ * (rank r sends its partial of chunk (r-s-1) mod p to rank r+1, which adds its
+ * own) and the all-gather phase's p-1 steps (rank r sends chunk (r-s) mod p),
+ * one kernel launch per step, and counts the bytes each rank sends
+ * ("Networks and Collective Communication" 5.1 and 4.3; "dist_train", Ring
+ * Algorithm).  Results equal the fused entry points bit for bit.
+ *
+ * bytes_sent  HOST array of p entries, overwritten with the bytes each rank
+ *             sent in this call (reduce-scatter partials travel as 4-byte
+ *             fp32/int32; all-gather chunks travel in dt).  May be NULL.
+ * workspace   device scratch for the working buffers; its required size is
+ *             ccl_ring_literal_workspace_bytes(kind, p, n, dt) (0 -> may be
+ *             NULL).  It must not overlap any send or recv buffer.
+ * Buffers follow the same layout and aliasing rules as the fused calls. */
+
+/* Bytes of workspace a literal call needs: all-reduce p*n*4 for bf16 (fp32
+ * partials), else 0; reduce-scatter p*n*4; all-gather 0.  Returns 0 for
+ * invalid arguments. */
+size_t ccl_ring_literal_workspace_bytes(ccl_kind_t kind, int p, size_t n, ccl_dtype_t dt);
+
+ccl_status_t ccl_ring_allreduce_literal(const void* const* send, void* const* recv, int p,
+                                        size_t n, ccl_dtype_t dt, ccl_op_t op,
+                                        uint64_t* bytes_sent, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+ccl_status_t ccl_ring_reduce_scatter_literal(const void* const* send, void* const* recv, int p,
+                                             size_t n, ccl_dtype_t dt, ccl_op_t op,
+                                             uint64_t* bytes_sent, void* workspace,
+                                             size_t workspace_bytes, void* stream);
+
+ccl_status_t ccl_ring_all_gather_literal(const void* const* send, void* const* recv, int p,
+                                         size_t n, ccl_dtype_t dt, uint64_t* bytes_sent,
+                                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCL_H_ */

@@ -36,33 +36,47 @@ def chunk_of(p: int, n: int, idx: np.ndarray) -> np.ndarray:
     return out
 
 
-def fold_at(x: list[np.ndarray], idx: np.ndarray, dtype: str = "f32", op: str = "sum"):
-    """Reduced value at each index in ``idx`` (fp32/int32 accumulator, unrounded)."""
-    p, n = len(x), len(x[0])
+def fold_columns(cols: list[np.ndarray], idx: np.ndarray, n: int, dtype: str = "f32",
+                 op: str = "sum"):
+    """The fold at indices ``idx`` of n-element rank buffers, given only the
+    sampled values: ``cols[r][j]`` is rank r's element ``idx[j]``."""
+    p = len(cols)
     idx = np.asarray(idx, dtype=np.int64)
     chunks = chunk_of(p, n, idx)
     acc_dtype = np.int32 if dtype == "i32" else np.float32
     out = np.empty(idx.shape, dtype=acc_dtype)
 
-    def value(rank, sel):
-        v = x[rank][sel]
+    def value(rank, mask):
+        v = cols[rank][mask]
         return bf16_to_f32(v) if dtype == "bf16" else v.astype(acc_dtype, copy=True)
 
     for c in range(p):
         mask = chunks == c
         if not mask.any():
             continue
-        sel = idx[mask]
-        acc = value((c + 1) % p, sel)
+        acc = value((c + 1) % p, mask)
         for j in range(2, p + 1):
-            acc = combine(acc, value((c + j) % p, sel), op)
+            acc = combine(acc, value((c + j) % p, mask), op)
         out[mask] = acc
     return out
+
+
+def fold_at(x: list[np.ndarray], idx: np.ndarray, dtype: str = "f32", op: str = "sum"):
+    """Reduced value at each index in ``idx`` (fp32/int32 accumulator, unrounded)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    return fold_columns([xr[idx] for xr in x], idx, len(x[0]), dtype, op)
 
 
 def allreduce_at(x: list[np.ndarray], idx: np.ndarray, dtype: str = "f32", op: str = "sum"):
     """All-reduce output (any rank) at the given indices, in the output dtype."""
     acc = fold_at(x, idx, dtype, op)
+    return f32_to_bf16_rne(acc) if dtype == "bf16" else acc
+
+
+def allreduce_at_columns(cols: list[np.ndarray], idx: np.ndarray, n: int, dtype: str = "f32",
+                         op: str = "sum"):
+    """All-reduce output at ``idx`` from sampled columns (see ``fold_columns``)."""
+    acc = fold_columns(cols, idx, n, dtype, op)
     return f32_to_bf16_rne(acc) if dtype == "bf16" else acc
 
 

@@ -1,0 +1,427 @@
+"""GPU parity: every entry point of libccl against the CPU oracle.
+
+Small and medium cases compare every element with the literal ring oracle;
+the full-size workloads compare sampled outputs with the pointwise oracle and
+check size-independent properties on the device.  Floating point results are
+bit-exact (fp32 ring order; bf16 within the stated 1-ulp contract, asserted
+exact); copies and integer sums are bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from a2a_ring_ordered_gb300 import workloads
+from gpu_util import (GUARD, Guarded, assert_bf16_close, assert_equal, ccl, sample_indices,
+                      to_dev, to_host)
+from oracle import collectives, pointwise, ring
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ccl()
+
+
+def make_inputs(dtype, p, n, seed):
+    if dtype == "i32":
+        return workloads.integer_valued(p, n, seed, lo=-2**31, hi=2**31 - 1, dtype="i32")
+    return workloads.normal(p, n, 1.0, seed, dtype=dtype)
+
+
+def guarded_outputs(p, sizes, dtype, offset=GUARD):
+    return [Guarded(s, dtype, offset) for s in sizes]
+
+
+# --------------------------------------------------------- worked example
+def test_worked_example_on_gpu(lib, worked_example):
+    g = worked_example
+    x = workloads.worked_example(4)
+    send = [to_dev(v, "f32") for v in x]
+    recv = [torch.empty(4, device="cuda") for _ in range(4)]
+    lib.ccl_allreduce(send, recv)
+    for r in recv:
+        assert to_host(r).tolist() == g["allreduce"]
+    shards = [torch.empty(1, device="cuda") for _ in range(4)]
+    lib.ccl_reduce_scatter(send, shards)
+    for k in range(4):
+        assert to_host(shards[k]).tolist() == g[f"reduce_scatter {k}"]
+    contrib = [to_dev(x[d][d:d + 1].copy(), "f32") for d in range(4)]
+    out = [torch.empty(4, device="cuda") for _ in range(4)]
+    lib.ccl_all_gather(contrib, out)
+    for o in out:
+        assert to_host(o).tolist() == g["all_gather"]
+    # all-to-all: one element per block, counts all 1
+    recv_a2a = [torch.empty(4, device="cuda") for _ in range(4)]
+    lib.ccl_all_to_allv(send, np.ones((4, 4), dtype=np.int64), recv_a2a, 1)
+    for j in range(4):
+        assert to_host(recv_a2a[j]).tolist() == g[f"all_to_all {j}"]
+
+
+# ------------------------------------------------ p=4 fp32 case, full size
+def test_p4_fp32_million_all_primitives(lib):
+    p, n = 4, 1 << 20
+    x = workloads.normal(p, n, 1.0, seed=0)
+    send = [to_dev(v, "f32") for v in x]
+    want_ar, _, _ = ring.ring_allreduce(x, "f32", "sum")
+    recv = [torch.empty(n, device="cuda") for _ in range(p)]
+    lib.ccl_allreduce(send, recv)
+    for r in range(p):
+        assert_equal(to_host(recv[r]), want_ar[r], "f32", f"AR rank {r}")
+    want_rs, _ = ring.ring_reduce_scatter(x, "f32", "sum")
+    shards = [torch.empty(n // p, device="cuda") for _ in range(p)]
+    lib.ccl_reduce_scatter(send, shards)
+    for k in range(p):
+        assert_equal(to_host(shards[k]), want_rs[k], "f32", f"RS rank {k}")
+    out = [torch.empty(n, device="cuda") for _ in range(p)]
+    lib.ccl_all_gather(shards, out)
+    for r in range(p):
+        assert_equal(to_host(out[r]), want_ar[r], "f32", f"AG(RS) rank {r}")
+    want_a2a = collectives.all_to_all(x)
+    counts = np.full((p, p), n // p, dtype=np.int64)
+    recv_a2a = [torch.empty(n, device="cuda") for _ in range(p)]
+    lib.ccl_all_to_allv(send, counts, recv_a2a, 1)
+    for r in range(p):
+        assert_equal(to_host(recv_a2a[r]), want_a2a[r], "f32", f"A2A rank {r}")
+
+
+# ------------------------------------------------- dtype x op x shape sweep
+SHAPES = [(1, 1000), (2, 4099), (3, 1001), (4, 13), (5, 3), (6, 13), (8, 70001),
+          (16, 65543), (72, 10000), (128, 1000)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+@pytest.mark.parametrize("p,n", SHAPES)
+def test_allreduce_and_reduce_scatter_match_oracle(lib, dtype, op, p, n):
+    x = make_inputs(dtype, p, n, seed=p * 1000 + n)
+    send = [to_dev(v, dtype) for v in x]
+    want, _, _ = ring.ring_allreduce(x, dtype, op)
+    outs = guarded_outputs(p, [n] * p, dtype)
+    lib.ccl_allreduce(send, [o.view for o in outs], op=op)
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"AR {dtype} {op} p={p} n={n} rank {r}")
+        assert outs[r].guards_intact()
+    want_rs, _ = ring.ring_reduce_scatter(x, dtype, op)
+    sizes = [ln for _, ln in ring.chunk_bounds(p, n)]
+    shards = guarded_outputs(p, sizes, dtype)
+    lib.ccl_reduce_scatter(send, [s.view for s in shards], op=op)
+    for k in range(p):
+        assert_equal(to_host(shards[k].view), want_rs[k], dtype, f"RS rank {k}")
+        assert shards[k].guards_intact()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,n", SHAPES)
+def test_all_gather_matches_oracle(lib, dtype, p, n):
+    x = make_inputs(dtype, p, n, seed=7 + p + n)
+    bounds = ring.chunk_bounds(p, n)
+    blocks = [x[k][off:off + ln].copy() for k, (off, ln) in enumerate(bounds)]
+    want, _ = ring.ring_all_gather(blocks, dtype)
+    send = [to_dev(b, dtype) for b in blocks]
+    outs = guarded_outputs(p, [n] * p, dtype)
+    lib.ccl_all_gather(send, [o.view for o in outs])
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"AG rank {r}")
+        assert outs[r].guards_intact()
+
+
+# -------------------------------------------- alignment and in-place forms
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("p,n", [(4, 1027), (8, 4096), (3, 50001)])
+def test_unaligned_buffers_take_the_elementwise_path(lib, dtype, p, n):
+    x = make_inputs(dtype, p, n, seed=3)
+    ins = [Guarded(n, dtype, offset=GUARD + 1) for _ in range(p)]  # 4 or 2 bytes off 16
+    for g, v in zip(ins, x):
+        g.view.copy_(to_dev(v, dtype))
+    want, _, _ = ring.ring_allreduce(x, dtype, "sum")
+    outs = guarded_outputs(p, [n] * p, dtype, offset=GUARD + (1 if p % 2 else 0))
+    lib.ccl_allreduce([g.view for g in ins], [o.view for o in outs])
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"unaligned AR rank {r}")
+        assert outs[r].guards_intact()
+    want_rs, _ = ring.ring_reduce_scatter(x, dtype, "sum")
+    shards = guarded_outputs(p, [ln for _, ln in ring.chunk_bounds(p, n)], dtype, offset=GUARD + 1)
+    lib.ccl_reduce_scatter([g.view for g in ins], [s.view for s in shards])
+    for k in range(p):
+        assert_equal(to_host(shards[k].view), want_rs[k], dtype, f"unaligned RS rank {k}")
+        assert shards[k].guards_intact()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,n", [(4, 1 << 16), (5, 12345), (16, 1000)])
+def test_in_place_forms(lib, dtype, p, n):
+    x = make_inputs(dtype, p, n, seed=11)
+    want, _, _ = ring.ring_allreduce(x, dtype, "sum")
+    bufs = [to_dev(v, dtype) for v in x]
+    lib.ccl_allreduce(bufs, bufs)
+    for r in range(p):
+        assert_equal(to_host(bufs[r]), want[r], dtype, f"in-place AR rank {r}")
+    # reduce-scatter in place: rank k's shard is chunk k of its own input
+    bufs = [to_dev(v, dtype) for v in x]
+    bounds = ring.chunk_bounds(p, n)
+    shards = [bufs[k][off:off + ln] for k, (off, ln) in enumerate(bounds)]
+    want_rs, _ = ring.ring_reduce_scatter(x, dtype, "sum")
+    lib.ccl_reduce_scatter(bufs, shards)
+    for k in range(p):
+        assert_equal(to_host(shards[k]), want_rs[k], dtype, f"in-place RS rank {k}")
+    # all-gather in place: block k already sits at off(k) of rank k's output
+    outs = [torch.zeros(n, dtype=bufs[0].dtype, device="cuda") for _ in range(p)]
+    blocks = []
+    for k, (off, ln) in enumerate(bounds):
+        outs[k][off:off + ln].copy_(to_dev(want_rs[k], dtype))
+        blocks.append(outs[k][off:off + ln])
+    lib.ccl_all_gather(blocks, outs)
+    for r in range(p):
+        assert_equal(to_host(outs[r]), want[r], dtype, f"in-place AG rank {r}")
+
+
+def test_zero_length_and_single_rank(lib):
+    z = [torch.empty(0, device="cuda") for _ in range(3)]
+    lib.ccl_allreduce(z, z)
+    x = workloads.normal(1, 777, 1.0, seed=1)
+    send = [to_dev(x[0], "f32")]
+    recv = [torch.empty(777, device="cuda")]
+    lib.ccl_allreduce(send, recv)
+    assert_equal(to_host(recv[0]), x[0], "f32", "p=1")
+
+
+def test_launch_counter_counts_one_fused_launch(lib):
+    p, n = 4, 4096
+    send = [torch.randn(n, device="cuda") for _ in range(p)]
+    recv = [torch.empty(n, device="cuda") for _ in range(p)]
+    before = lib.ccl_kernel_launch_count()
+    lib.ccl_allreduce(send, recv)
+    torch.cuda.synchronize()
+    assert lib.ccl_kernel_launch_count() == before + 1
+
+
+def test_fold_order_discriminator_on_gpu(lib):
+    """Per chunk: x_{c+1} = 2^24, x_{c+2} = x_{c+3} = 1, x_c = -2^24; only the
+    ring order (start at c+1, walk forward) yields 0."""
+    p, n = 8, 8 * 1024
+    bounds = ring.chunk_bounds(p, n)
+    x = [np.zeros(n, dtype=np.float32) for _ in range(p)]
+    for c, (off, ln) in enumerate(bounds):
+        sl = slice(off, off + ln)
+        x[(c + 1) % p][sl] = 2.0**24
+        x[(c + 2) % p][sl] = 1.0
+        x[(c + 3) % p][sl] = 1.0
+        x[c][sl] = -(2.0**24)
+    send = [to_dev(v, "f32") for v in x]
+    recv = [torch.empty(n, device="cuda") for _ in range(p)]
+    lib.ccl_allreduce(send, recv)
+    for r in range(p):
+        assert (to_host(recv[r]) == 0).all()
+
+
+# ------------------------------------------------------------- DDP bucket
+def test_ddp_bucket_full_size(lib):
+    """25 MB fp32 bucket per rank, p=8, N(0, 1e-3), scale 1/8 -> bf16."""
+    p, n = 8, 6_553_600
+    g = workloads.normal(p, n, 1e-3, seed=1)
+    want = ring.bucket_allreduce_scale_cast(g, 1.0 / 8)
+    send = [to_dev(v, "f32") for v in g]
+    outs = guarded_outputs(p, [n] * p, "bf16")
+    lib.ccl_bucket_allreduce_scale_cast(send, [o.view for o in outs], scale=1.0 / 8)
+    for r in range(p):
+        assert_bf16_close(to_host(outs[r].view), want[r], f"bucket rank {r}")
+        assert outs[r].guards_intact()
+
+
+@pytest.mark.parametrize("p,n,scale", [(3, 1001, 1 / 3), (8, 13, 0.125), (16, 70001, 1 / 16),
+                                       (7, 4099, 1 / 7), (72, 5000, 1 / 72)])
+def test_ddp_bucket_shapes(lib, p, n, scale):
+    g = workloads.normal(p, n, 1e-3, seed=p)
+    want = ring.bucket_allreduce_scale_cast(g, float(np.float32(scale)))
+    send = [to_dev(v, "f32") for v in g]
+    outs = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    lib.ccl_bucket_allreduce_scale_cast(send, outs, scale=float(np.float32(scale)))
+    for r in range(p):
+        assert_bf16_close(to_host(outs[r]), want[r], f"bucket p={p} rank {r}")
+
+
+# ------------------------------------------------------- ZeRO, full size
+def test_zero_rs_then_ag_full_size(lib):
+    """p=16, 192 MiB bf16 per rank, N(0, 1e-2): RS (fp32 accumulation) then AG.
+    Sampled outputs against the pointwise oracle; AG(RS) == AR on the device."""
+    p, n = 16, 100_663_296
+    idx = sample_indices(n, p, 1 << 20, seed=2)
+    rng = np.random.default_rng(2)
+    send, cols = [], []
+    for _ in range(p):  # same stream as workloads.normal(p, n, 1e-2, 2, "bf16")
+        v = rng.standard_normal(n, dtype=np.float32)
+        v *= np.float32(1e-2)
+        b = workloads.to_bf16_bits(v)
+        cols.append(b[idx])
+        send.append(to_dev(b, "bf16"))
+        del v, b
+    want = pointwise.allreduce_at_columns(cols, idx, n, "bf16")
+    bounds = ring.chunk_bounds(p, n)
+    shards = [torch.empty(ln, dtype=torch.bfloat16, device="cuda") for _, ln in bounds]
+    lib.ccl_reduce_scatter(send, shards)
+    gathered = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    lib.ccl_all_gather(shards, gathered)
+    torch.cuda.synchronize()
+    idx_t = torch.from_numpy(idx).cuda()
+    for r in (0, 7, 15):
+        assert_bf16_close(to_host(gathered[r][idx_t]), want, f"ZeRO AG(RS) rank {r}")
+    # shard k at sampled positions of chunk k
+    chunk = pointwise.chunk_of(p, n, idx)
+    for k in (0, 5, 15):
+        sel = chunk == k
+        local = torch.from_numpy(idx[sel] - bounds[k][0]).cuda()
+        assert_bf16_close(to_host(shards[k][local]), want[sel], f"ZeRO shard {k}")
+    # properties at full size, on the device: every rank identical; AG(RS) == AR
+    for r in range(1, p):
+        assert torch.equal(gathered[r].view(torch.int16), gathered[0].view(torch.int16))
+    ar = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    lib.ccl_allreduce(send, ar + gathered[2:])  # gathered[0] still holds AG(RS)
+    assert torch.equal(ar[0].view(torch.int16), gathered[0].view(torch.int16))
+    assert torch.equal(gathered[2].view(torch.int16), gathered[0].view(torch.int16))
+
+
+# ------------------------------------------------------------ all-to-allv
+def test_moe_dispatch_combine_full_size(lib):
+    """p=8, 16,384 tokens of 4096 bf16 per rank, Zipf(1.2) counts, seed 3."""
+    hidden = 4096
+    counts, rng = workloads.moe_counts(p=8, tokens_per_rank=16384, seed=3)
+    tokens = workloads.moe_tokens(counts, hidden, rng, dtype="bf16")
+    want = collectives.all_to_allv(tokens, counts, hidden)
+    send = [to_dev(t, "bf16") for t in tokens]
+    recv_rows = counts.sum(axis=0)
+    recv = [torch.empty(int(r) * hidden, dtype=torch.bfloat16, device="cuda") for r in recv_rows]
+    lib.ccl_all_to_allv(send, counts, recv, hidden)
+    for d in range(8):
+        assert_equal(to_host(recv[d]), want[d], "bf16", f"dispatch rank {d}")
+    back = [torch.empty_like(s) for s in send]
+    lib.ccl_all_to_allv(recv, counts.T, back, hidden)
+    for s in range(8):
+        assert torch.equal(back[s].view(torch.int16), send[s].view(torch.int16)), f"combine {s}"
+
+
+@pytest.mark.parametrize("row_elems,dtype", [(7, "bf16"), (1, "bf16"), (3, "f32"), (13, "bf16"),
+                                             (8, "bf16"), (33, "f32")])
+@pytest.mark.parametrize("p", [2, 5, 8])
+def test_all_to_allv_ragged_rows(lib, row_elems, dtype, p):
+    """Rows whose byte size is not a multiple of 16: source and destination
+    blocks differ in 16-byte phase, which takes the shuffle realignment path."""
+    rng = np.random.default_rng(row_elems * 10 + p)
+    counts = rng.integers(0, 300, size=(p, p))
+    counts[p - 1, :] = 0
+    counts[0, 1 % p] = 5000
+    send_np = [make_inputs(dtype, 1, int(counts[s].sum()) * row_elems, seed=s)[0] for s in range(p)]
+    want = collectives.all_to_allv(send_np, counts, row_elems)
+    send = [to_dev(v, dtype) for v in send_np]
+    outs = [Guarded(int(counts[:, d].sum()) * row_elems, dtype, offset=GUARD + d % 3)
+            for d in range(p)]
+    lib.ccl_all_to_allv(send, counts, [o.view for o in outs], row_elems)
+    for d in range(p):
+        assert_equal(to_host(outs[d].view), want[d], dtype, f"a2av rank {d}")
+        assert outs[d].guards_intact()
+
+
+def test_all_to_allv_many_blocks_spans_launches(lib):
+    """p=16 -> 256 blocks: more than one launch's worth of block descriptors."""
+    p, row = 16, 64
+    rng = np.random.default_rng(5)
+    counts = rng.integers(1, 40, size=(p, p))
+    x = [workloads.normal(1, int(counts[s].sum()) * row, 1.0, seed=s, dtype="bf16")[0] for s in range(p)]
+    want = collectives.all_to_allv(x, counts, row)
+    recv = [torch.empty(int(counts[:, d].sum()) * row, dtype=torch.bfloat16, device="cuda")
+            for d in range(p)]
+    lib.ccl_all_to_allv([to_dev(v, "bf16") for v in x], counts, recv, row)
+    for d in range(p):
+        assert_equal(to_host(recv[d]), want[d], "bf16", f"rank {d}")
+
+
+# -------------------------------------------------------- literal engine
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,n", [(1, 100), (2, 4099), (4, 1 << 16), (5, 13), (8, 70001), (16, 1000)])
+def test_literal_engine_matches_oracle_and_counts_bytes(lib, dtype, p, n):
+    x = make_inputs(dtype, p, n, seed=p + n)
+    send = [to_dev(v, dtype) for v in x]
+    want, rs_bytes, ag_bytes = ring.ring_allreduce(x, dtype, "sum")
+    recv = [torch.empty(n, dtype=send[0].dtype, device="cuda") for _ in range(p)]
+    sent = lib.ccl_ring_allreduce_literal(send, recv)
+    for r in range(p):
+        assert_equal(to_host(recv[r]), want[r], dtype, f"literal AR rank {r}")
+    assert sent == [a + b for a, b in zip(rs_bytes, ag_bytes)]
+    # the fused kernel gives the same bits
+    fused = [torch.empty_like(t) for t in recv]
+    lib.ccl_allreduce(send, fused)
+    for r in range(p):
+        assert torch.equal(fused[r].view(torch.int16 if dtype == "bf16" else torch.int32),
+                           recv[r].view(torch.int16 if dtype == "bf16" else torch.int32))
+    want_rs, rs_only = ring.ring_reduce_scatter(x, dtype, "sum")
+    shards = [torch.empty(ln, dtype=send[0].dtype, device="cuda") for _, ln in ring.chunk_bounds(p, n)]
+    sent_rs = lib.ccl_ring_reduce_scatter_literal(send, shards)
+    for k in range(p):
+        assert_equal(to_host(shards[k]), want_rs[k], dtype, f"literal RS rank {k}")
+    assert sent_rs == rs_only
+    gathered = [torch.empty(n, dtype=send[0].dtype, device="cuda") for _ in range(p)]
+    sent_ag = lib.ccl_ring_all_gather_literal(shards, gathered)
+    _, ag_only = ring.ring_all_gather(want_rs, dtype)
+    for r in range(p):
+        assert_equal(to_host(gathered[r]), want[r], dtype, f"literal AG rank {r}")
+    assert sent_ag == ag_only
+
+
+@pytest.mark.parametrize("op", ["max", "min"])
+def test_literal_engine_max_min_in_place(lib, op):
+    p, n = 6, 10007
+    x = workloads.normal(p, n, 1.0, seed=4)
+    want, _, _ = ring.ring_allreduce(x, "f32", op)
+    bufs = [to_dev(v, "f32") for v in x]
+    lib.ccl_ring_allreduce_literal(bufs, bufs, op=op)
+    for r in range(p):
+        assert_equal(to_host(bufs[r]), want[r], "f32", f"literal {op} rank {r}")
+
+
+# ------------------------------------------------- message-size sweep
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("p", [2, 4, 8, 16])
+def test_sweep_sizes_small_full_compare(lib, dtype, p):
+    """1 KiB .. 4 MiB per rank (powers of two), U(-1, 1), every element."""
+    e = 4 if dtype == "f32" else 2
+    for kib in [1 << k for k in range(0, 13)]:
+        n = kib * 1024 // e
+        x = workloads.uniform(p, n, seed=4, dtype=dtype)
+        want, _, _ = ring.ring_allreduce(x, dtype, "sum")
+        send = [to_dev(v, dtype) for v in x]
+        recv = [torch.empty_like(s) for s in send]
+        lib.ccl_allreduce(send, recv)
+        for r in (0, p - 1):
+            assert_equal(to_host(recv[r]), want[r], dtype, f"sweep {kib} KiB p={p} rank {r}")
+
+
+@pytest.mark.parametrize("dtype,p,mib", [("f32", 16, 1024), ("bf16", 16, 1024), ("f32", 72, 256),
+                                         ("bf16", 72, 256), ("f32", 2, 1024)])
+def test_sweep_largest_sizes_sampled(lib, dtype, p, mib):
+    """The sweep's largest messages: sampled elements against the pointwise
+    oracle; all ranks identical on the device.  At these sizes the U(-1, 1)
+    inputs are drawn on the device by torch's seeded generator (drawing up to
+    16 GiB on the host would take minutes); the oracle reads the values at the
+    sampled positions."""
+    e = 4 if dtype == "f32" else 2
+    n = mib * (1 << 20) // e
+    idx = sample_indices(n, p, 1 << 18, seed=p)
+    idx_t = torch.from_numpy(idx).cuda()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4)
+    send, cols = [], []
+    for _ in range(p):
+        v = torch.rand(n, generator=gen, device="cuda", dtype=torch.float32) * 2.0 - 1.0
+        v = v.to(torch.bfloat16) if dtype == "bf16" else v
+        cols.append(to_host(v[idx_t]))
+        send.append(v)
+    recv = [torch.empty_like(s) for s in send]
+    lib.ccl_allreduce(send, recv)
+    want = pointwise.allreduce_at_columns(cols, idx, n, dtype)
+    for r in (0, p // 2, p - 1):
+        assert_equal(to_host(recv[r][idx_t]), want, dtype, f"sweep {mib} MiB p={p} rank {r}")
+    view = torch.int16 if dtype == "bf16" else torch.int32
+    for r in range(1, p):
+        assert torch.equal(recv[r].view(view), recv[0].view(view))
