@@ -181,6 +181,7 @@ class Bucket(Workload):
 
     def __init__(self, p=8, n=6_553_600, sigma=1e-3, seed=1):
         self.p, self.n, self.sigma, self.seed = p, n, sigma, seed
+        self.scale = float(np.float32(1.0 / p))
         self.kernel_key = f"fold_bucket_f32_bf16_p{p}_n{n}"
 
     def config(self):
@@ -202,7 +203,6 @@ class Bucket(Workload):
         self.x = self.host_inputs()
         self.send = [torch.from_numpy(v).to(device) for v in self.x]
         self.recv = [torch.empty(self.n, dtype=torch.bfloat16, device=device) for _ in range(self.p)]
-        self.scale = float(np.float32(1.0 / self.p))
         # pinned host copies for the end-to-end path
         self.h_in = [torch.from_numpy(v).pin_memory() for v in self.x]
         self.h_out = [torch.empty(self.n, dtype=torch.bfloat16).pin_memory() for _ in range(self.p)]
@@ -451,6 +451,8 @@ def run_reference(a, wl: Workload, rank: int, world: int) -> dict | None:
     if rank != 0:
         return None
     budget_s = 90.0
+    if a.steps <= 0:
+        a.steps = 20
     # first sample sizes the rest: aim for the whole run within ~budget_s
     wl_host = wl
     if not hasattr(wl_host, "x"):
@@ -510,9 +512,16 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
     wl.setup(lib, torch, device)
     stream = torch.cuda.current_stream(device)
 
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
     for _ in range(a.warmup):
         wl.step(stream)
+    w1.record(stream)
     torch.cuda.synchronize(device)
+    if a.steps <= 0:  # auto: about one second of timed device work
+        ms_warm = w0.elapsed_time(w1) / a.warmup
+        a.steps = int(max(50, min(200000, round(1000.0 / max(ms_warm, 1e-3)))))
+        a.steps = int(max_over_ranks(float(a.steps), world, device))
 
     sampler = ClockSampler(local)
     time.sleep(0.05)
@@ -611,7 +620,9 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (default: enough for ~1 s of device time, so the "
+                         "200 ms clock sampler sees the timed region)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bucket",

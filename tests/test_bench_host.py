@@ -1,0 +1,96 @@
+"""bench.py's host logic on CPU: the replica aggregation over ranks (gloo,
+world size 2), the reference arm's rank handling, and the clock summary."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, q):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # each replica timed its own steps; the job takes the slowest
+        t = bench.max_over_ranks(1.0 + rank * 0.5, world)
+        bench.barrier(world)
+        q.put((rank, t))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=5) for _ in range(2))
+    assert got == {0: 1.5, 1: 1.5}
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    class A:
+        steps, warmup = 5, 3
+    assert bench.run_reference(A(), bench.Bucket(), rank=1, world=2) is None
+
+
+def test_reference_arm_prints_one_line_on_rank0():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                       env=env, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["unit"] == "GB/s" and out["value"] > 0
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["cores"] >= 1
+    assert out["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_nonzero_rank_prints_nothing():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                       env=env, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_clock_summary_parses_samples():
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.samples = [(10.0, ["1900", "2070", "800.5", "Not Active", "Not Active", "Not Active", "Active"]),
+                 (10.2, ["1950", "2070", "810.0", "Not Active", "Not Active", "Not Active", "Not Active"]),
+                 (99.0, ["300", "2070", "90", "Not Active", "Not Active", "Not Active", "Not Active"])]
+    out = s.summary(9.9, 10.3)
+    assert out["sm_mhz"] == 1925 and out["sm_max_mhz"] == 2070
+    assert out["reasons"] == ["sw_power_cap"] and out["samples"] == 2
+    short = s.summary(50.0, 50.01)  # region shorter than the period: nearest sample
+    assert short["samples"] == 1
+
+
+def test_warmup_below_three_is_rejected():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2", "--impl", "reference"])
