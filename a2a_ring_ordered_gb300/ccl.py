@@ -294,3 +294,30 @@ def ccl_ring_all_gather_literal(send, recv, stream=None) -> list[int]:
                                            _stream(stream, send[0].device)),
            "ccl_ring_all_gather_literal")
     return list(sent)
+
+
+# ---------------------------------------------- allocation-free reduce-scatter
+def ccl_ring_reduce_scatter_literal_noalloc(send, recv, op: str = "sum", stream=None) -> list[int]:
+    """ccl_ring_reduce_scatter_literal without a workspace argument.
+
+    For callers that cannot allocate device memory (for instance code running
+    inside an allocator callback, or under a host that owns all device
+    memory): the library's built-in static scratch holds the working buffers,
+    so p*n must not exceed 8,388,608 elements.  The first call on a device
+    looks up the scratch address, so make it before any stream capture; calls
+    that overlap on the GPU share the scratch and must be serialised.
+    """
+    fn = LIB.ccl_ring_reduce_scatter_literal_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), ctypes.c_int,
+                   ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64),
+                   ctypes.c_void_p]
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [_chunk(p, n, k)[1] for k in range(p)], "recv")
+    sent = (ctypes.c_uint64 * p)()
+    _check(fn(_ptr_array([t.data_ptr() for t in send]), _ptr_array([t.data_ptr() for t in recv]),
+              p, n, _dtype_code(send[0]), _op_code(op), sent, _stream(stream, send[0].device)),
+           "ccl_ring_reduce_scatter_literal_noalloc")
+    return list(sent)

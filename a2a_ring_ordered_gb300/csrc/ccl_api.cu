@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "ccl_internal.h"
 
@@ -601,4 +602,72 @@ extern "C" ccl_status_t ccl_ring_all_gather_literal(const void* const* send, voi
   if ((st = ag_phase(out, p, n, dt, sent, s)) != CCL_OK) return st;
   write_sent(bytes_sent, sent, p);
   return CCL_OK;
+}
+
+// ============================================ allocation-free reduce-scatter
+// The literal reduce-scatter needs p*n*4 bytes of device scratch for the
+// ranks' working buffers.  Some callers cannot allocate that themselves, so
+// this entry point uses a fixed scratch array that lives inside the library
+// (in this translation unit's module) instead of a caller workspace.
+
+// File-scope scratch, CCL_STATIC_SCRATCH_BYTES on every GPU that loads the
+// library, held until the process exits.  Host code must not use the
+// symbol's host-side name as a device address; the address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char ccl_static_scratch[CCL_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxScratchDevices = 256;
+std::mutex g_scratch_mutex;
+void* g_scratch_address[kMaxScratchDevices];  // per device; NULL until looked up
+
+// Device address of the static scratch on the current device.  Looked up once
+// per device, on the first call made with that device current.
+ccl_status_t static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxScratchDevices)
+    return fail(CCL_ERR_UNSUPPORTED, "device %d beyond the %d devices the static scratch tracks",
+                dev, kMaxScratchDevices);
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_address[dev] == nullptr) {
+    void* addr = nullptr;
+    err = cudaGetSymbolAddress(&addr, ccl_static_scratch);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaGetSymbolAddress(static scratch)");
+    g_scratch_address[dev] = addr;
+  }
+  *out = g_scratch_address[dev];
+  return CCL_OK;
+}
+
+}  // namespace
+
+extern "C" ccl_status_t ccl_ring_reduce_scatter_literal_noalloc(const void* const* send,
+                                                                void* const* recv, int p, size_t n,
+                                                                ccl_dtype_t dt, ccl_op_t op,
+                                                                uint64_t* bytes_sent,
+                                                                void* stream) {
+  clear_error();
+  ccl_status_t st = check_reduce(1, send, recv, p, n, dt, op);
+  if (st != CCL_OK) return st;
+  const size_t need = literal_ws(CCL_KIND_REDUCE_SCATTER, p, n, dt);
+  if (need > CCL_STATIC_SCRATCH_BYTES)
+    return fail(CCL_ERR_INVALID_ARG,
+                "p*n*4 = %zu bytes of scratch needed; the static scratch holds %zu "
+                "(p*n must not exceed %zu)",
+                need, static_cast<size_t>(CCL_STATIC_SCRATCH_BYTES),
+                static_cast<size_t>(CCL_STATIC_SCRATCH_BYTES / 4));
+  if (n == 0) {
+    uint64_t zero[CCL_MAX_RANKS] = {0};
+    write_sent(bytes_sent, zero, p);
+    return CCL_OK;
+  }
+  void* scratch = nullptr;
+  if ((st = static_scratch_address(&scratch)) != CCL_OK) return st;
+  // Nothing in the scratch has to start at zero: the call's first launch
+  // overwrites every byte that later launches read.
+  return ccl_ring_reduce_scatter_literal(send, recv, p, n, dt, op, bytes_sent, scratch,
+                                         CCL_STATIC_SCRATCH_BYTES, stream);
 }

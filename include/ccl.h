@@ -180,6 +180,38 @@ ccl_status_t ccl_ring_all_gather_literal(const void* const* send, void* const* r
                                          size_t n, ccl_dtype_t dt, uint64_t* bytes_sent,
                                          void* stream);
 
+/* ------------------------------------------- allocation-free reduce-scatter
+ * The pages have no counterpart to this call; it exists for callers of this
+ * library that cannot allocate device memory for the workspace that
+ * ccl_ring_reduce_scatter_literal needs: code that runs inside a custom
+ * allocator or memory-pool callback (allocating there would re-enter the
+ * allocator), a host application that owns all device memory and does not let
+ * libraries allocate, or a process that reserved its memory budget up front
+ * and must not fail or fragment later.
+ *
+ * Same arguments, results and byte counts as ccl_ring_reduce_scatter_literal,
+ * without the workspace: the p*n*4 bytes of working buffers come from a
+ * scratch array built into the library (a file-scope static __device__ array
+ * of CCL_STATIC_SCRATCH_BYTES).  Every GPU that loads the library holds that
+ * array until the process exits.  The call allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine).
+ *   - p*n*4 > CCL_STATIC_SCRATCH_BYTES (p*n above 8,388,608 elements)
+ *     -> CCL_ERR_INVALID_ARG, checked before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero: each call overwrites every byte
+ *     it reads).  Calls whose GPU work overlaps -- on different streams, or
+ *     from host threads that do not order their streams -- race on the array;
+ *     the caller must serialise them. */
+#define CCL_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+ccl_status_t ccl_ring_reduce_scatter_literal_noalloc(const void* const* send, void* const* recv,
+                                                     int p, size_t n, ccl_dtype_t dt,
+                                                     ccl_op_t op, uint64_t* bytes_sent,
+                                                     void* stream);
+
 #ifdef __cplusplus
 }
 #endif
