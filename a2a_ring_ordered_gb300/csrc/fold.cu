@@ -121,6 +121,100 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ 
   }
 }
 
+// ------------------------------------------------------------- small p
+// With few ranks a thread of fold_kernel has only p loads in flight, far too
+// few to cover HBM latency at the occupancy its registers allow.  This kernel
+// gives each thread U vectors (t, t + kThreads, ...) and issues the loads of
+// all BATCH >= p ranks x U vectors before folding any of them, so a thread
+// keeps about 256 bytes of loads in flight whatever p is.  The fold order of
+// each element is the same ring walk as in fold_kernel.
+template <int DT_IN, int VEC, int OP, int BATCH, int U>
+__device__ __forceinline__ void fold_vectors(const FoldArgs& a, int p, int first, uint64_t v0,
+                                             uint64_t v_hi,
+                                             typename Elem<DT_IN>::Acc (&acc)[U][VEC]) {
+  constexpr int WI = words_for(VEC, Elem<DT_IN>::kBytes);
+  uint32_t raw[BATCH][U][WI];
+  int r = first;
+#pragma unroll
+  for (int b = 0; b < BATCH; ++b) {
+    if (b < p) {
+      const void* src = a.send[r];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = v0 + static_cast<uint64_t>(u) * kThreads;
+        if (v < v_hi) load_raw<DT_IN, VEC>(src, v * VEC, raw[b][u]);
+      }
+      r = (r + 1 == p) ? 0 : r + 1;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[u][e] = widen<DT_IN>(raw[0][u], e);
+  }
+#pragma unroll
+  for (int b = 1; b < BATCH; ++b) {
+    if (b < p) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[u][e] = combine<OP>(acc[u][e], widen<DT_IN>(raw[b][u], e));
+      }
+    }
+  }
+}
+
+// Requires p <= BATCH and 16-byte aligned pointers; chunk edges are folded
+// element-wise by CTA (0, c) exactly as in fold_kernel.
+template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE, int BATCH, int U>
+__global__ void __launch_bounds__(kThreads) fold_unrolled_kernel(const __grid_constant__ FoldArgs a) {
+  using Acc = typename Elem<DT_IN>::Acc;
+  const int p = a.p;
+  const int c = blockIdx.y;
+  const Chunk ch = chunk_of(c, a.q, a.rem);
+  const uint64_t end = ch.off + ch.len;
+  const uint64_t v_lo = (ch.off + VEC - 1) / VEC;
+  const uint64_t v_hi = end / VEC;
+  const int first = (c + 1 == p) ? 0 : c + 1;
+
+  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  for (uint64_t base = v_lo + static_cast<uint64_t>(blockIdx.x) * kSpan; base < v_hi;
+       base += static_cast<uint64_t>(gridDim.x) * kSpan) {
+    Acc acc[U][VEC];
+    fold_vectors<DT_IN, VEC, OP, BATCH, U>(a, p, first, base + threadIdx.x, v_hi, acc);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+      if (v < v_hi) emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc[u]);
+    }
+  }
+
+  if (blockIdx.x == 0) {
+    const uint64_t head_end = (v_lo * VEC < end) ? v_lo * VEC : end;
+    const uint64_t tail_begin = (v_hi * VEC > head_end) ? v_hi * VEC : head_end;
+    const uint64_t n_head = head_end - ch.off;
+    const uint64_t n_edge = n_head + (end - tail_begin);
+    for (uint64_t t = threadIdx.x; t < n_edge; t += kThreads) {
+      const uint64_t i = (t < n_head) ? ch.off + t : tail_begin + (t - n_head);
+      Acc acc[1];
+      fold_elements<DT_IN, 1, OP>(a, p, first, i, acc);
+      emit<DT_OUT, 1, MODE>(a, p, c, ch, i, acc);
+    }
+  }
+}
+
+template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE, int BATCH, int U>
+cudaError_t launch_unrolled(const FoldArgs& a, cudaStream_t s) {
+  const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
+  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  uint64_t gx = (per_chunk + kSpan - 1) / kSpan;
+  if (gx < 1) gx = 1;
+  if (gx > (1u << 30)) gx = 1u << 30;
+  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.p));
+  fold_unrolled_kernel<DT_IN, DT_OUT, VEC, OP, MODE, BATCH, U><<<grid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 constexpr int kVectorsPerThread = 2;
 
 template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE>
@@ -134,10 +228,24 @@ cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Small p (sums only) goes to fold_unrolled_kernel with (ranks per batch,
+// vectors per thread) = (2, 8), (4, 4) or (8, 2) for 16-byte fp32 / int32
+// vectors.  A bf16 vector widens to 8 fp32 accumulators and a bucket vector
+// is 32 bytes, so those use (2, 4) and (4, 2) and leave p > 4 to fold_kernel
+// (at most 32 accumulators per thread either way).
 template <int DT_IN, int DT_OUT, int OP, int MODE>
 cudaError_t launch_typed(bool vec, const FoldArgs& a, cudaStream_t s) {
-  if (vec) return launch_one<DT_IN, DT_OUT, vec_width<DT_IN, DT_OUT>(), OP, MODE>(a, s);
-  return launch_one<DT_IN, DT_OUT, 1, OP, MODE>(a, s);
+  if (!vec) return launch_one<DT_IN, DT_OUT, 1, OP, MODE>(a, s);
+  constexpr int VEC = vec_width<DT_IN, DT_OUT>();
+  if constexpr (OP == CCL_SUM) {
+    constexpr bool kHalve = VEC > 4;
+    if (a.p <= 2) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 2, kHalve ? 4 : 8>(a, s);
+    if (a.p <= 4) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 4, kHalve ? 2 : 4>(a, s);
+    if constexpr (!kHalve) {
+      if (a.p <= 8) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 8, 2>(a, s);
+    }
+  }
+  return launch_one<DT_IN, DT_OUT, VEC, OP, MODE>(a, s);
 }
 
 template <int MODE>

@@ -30,7 +30,7 @@ __device__ __forceinline__ void load_elems(const void* base, uint64_t i, uint32_
   }
 }
 
-template <int DT, int VEC>
+template <int DT, int VEC, int U>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
   constexpr int W = (VEC * Elem<DT>::kBytes + 3) / 4;
   const int p = a.p;
@@ -42,17 +42,30 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
   const void* src = a.send[k];
   const bool src_aligned = (ch.off % VEC) == 0;
 
-  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
-  for (uint64_t v = v_lo + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi;
-       v += stride) {
-    const uint64_t i = v * VEC;
-    uint32_t w[W];
-    if (VEC == 1 || src_aligned) {
-      load_raw<DT, VEC>(src, i - ch.off, w);
-    } else {
-      load_elems<DT, VEC>(src, i - ch.off, w);
+  // U vectors per thread (t, t + kThreads, ...): their loads are issued
+  // together, then each is stored to the p outputs
+  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  for (uint64_t base = v_lo + static_cast<uint64_t>(blockIdx.x) * kSpan; base < v_hi;
+       base += static_cast<uint64_t>(gridDim.x) * kSpan) {
+    uint32_t w[U][W];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+      if (v < v_hi) {
+        if (VEC == 1 || src_aligned) {
+          load_raw<DT, VEC>(src, v * VEC - ch.off, w[u]);
+        } else {
+          load_elems<DT, VEC>(src, v * VEC - ch.off, w[u]);
+        }
+      }
     }
-    for (int r = 0; r < p; ++r) store_raw<DT, VEC>(a.recv[r], i, w);
+    for (int r = 0; r < p; ++r) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+        if (v < v_hi) store_raw<DT, VEC>(a.recv[r], v * VEC, w[u]);
+      }
+    }
   }
 
   if (VEC > 1 && blockIdx.x == 0) {
@@ -69,23 +82,22 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
   }
 }
 
-constexpr int kVectorsPerThread = 2;
-
-template <int DT, int VEC>
+template <int DT, int VEC, int U>
 cudaError_t launch_one(const GatherArgs& a, cudaStream_t s) {
   const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
-  uint64_t gx = (per_chunk + kThreads * kVectorsPerThread - 1) / (kThreads * kVectorsPerThread);
+  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  uint64_t gx = (per_chunk + kSpan - 1) / kSpan;
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.p));
-  gather_kernel<DT, VEC><<<grid, kThreads, 0, s>>>(a);
+  gather_kernel<DT, VEC, U><<<grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 template <int DT>
 cudaError_t launch_typed(bool vec, const GatherArgs& a, cudaStream_t s) {
-  if (vec) return launch_one<DT, 16 / Elem<DT>::kBytes>(a, s);
-  return launch_one<DT, 1>(a, s);
+  if (vec) return launch_one<DT, 16 / Elem<DT>::kBytes, 4>(a, s);
+  return launch_one<DT, 1, 1>(a, s);
 }
 
 }  // namespace
