@@ -144,6 +144,28 @@ KERNEL_SOURCES = {
 }
 
 
+def host_prefix(tensors, m: int) -> list[np.ndarray]:
+    """First m elements of each device rank buffer as numpy (bf16 as uint16 bits)."""
+    import torch
+    out = []
+    for t in tensors:
+        h = t[:m].detach().cpu()
+        out.append(h.view(torch.int16).numpy().view(np.uint16).copy() if h.dtype == torch.bfloat16
+                   else h.numpy().copy())
+    return out
+
+
+def oracle_prefix_sample(tensors, n: int, frac: float, fn, bytes_per_elem_index: float, what: str):
+    """Time ``fn`` (an oracle call) on the first frac*n elements of every rank."""
+    p = len(tensors)
+    m = max(p, int(n * frac))
+    xs = host_prefix(tensors, m)
+    t0 = time.perf_counter()
+    fn(xs)
+    dt = time.perf_counter() - t0
+    return dt, int(m * bytes_per_elem_index), f"{what} on the first {m} of {n} elements of each of the {p} ranks"
+
+
 class Workload:
     """One step of a collective on device-resident synthetic inputs."""
     name = ""
@@ -266,6 +288,12 @@ class AllReduce(Workload):
             need = lib.ccl_ring_literal_workspace_bytes(lib.CCL_KIND_ALLREDUCE, self.p, self.n, tdt)
             self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
 
+    def oracle_sample(self, frac):
+        from oracle import ring
+        return oracle_prefix_sample(self.send, self.n, frac,
+                                    lambda xs: ring.ring_allreduce(xs, self.dtype, self.op),
+                                    2 * self.p * self.e, "oracle ring all-reduce")
+
     def step(self, stream):
         if self.literal:
             self.lib.ccl_ring_allreduce_literal(self.send, self.recv, op=self.op,
@@ -296,6 +324,12 @@ class ReduceScatter(AllReduce):
     def step(self, stream):
         self.lib.ccl_reduce_scatter(self.send, self.shards, stream=stream)
 
+    def oracle_sample(self, frac):
+        from oracle import ring
+        return oracle_prefix_sample(self.send, self.n, frac,
+                                    lambda xs: ring.ring_reduce_scatter(xs, self.dtype, "sum"),
+                                    (self.p + 1) * self.e, "oracle ring reduce-scatter")
+
 
 class AllGather(ReduceScatter):
     kernel = "gather"
@@ -315,6 +349,16 @@ class AllGather(ReduceScatter):
 
     def step(self, stream):
         self.lib.ccl_all_gather(self.shards, self.recv, stream=stream)
+
+    def oracle_sample(self, frac):
+        from oracle import ring
+
+        def gather(xs):
+            m = len(xs[0])
+            blocks = [xs[k][off:off + ln] for k, (off, ln) in enumerate(ring.chunk_bounds(self.p, m))]
+            ring.ring_all_gather(blocks, self.dtype)
+        return oracle_prefix_sample(self.send, self.n, frac, gather, (self.p + 1) * self.e,
+                                    "oracle ring all-gather")
 
 
 class Zero(ReduceScatter):
@@ -348,6 +392,11 @@ class Zero(ReduceScatter):
     def step(self, stream):
         self.lib.ccl_reduce_scatter(self.send, self.shards, stream=stream)
         self.lib.ccl_all_gather(self.shards, self.recv, stream=stream)
+
+    def oracle_sample(self, frac):
+        from oracle import ring
+        return oracle_prefix_sample(self.send, self.n, frac, ring.zero_rs_then_ag,
+                                    2 * (self.p + 1) * 2, "oracle ZeRO RS then AG")
 
     def parts(self):
         rs = lambda s: self.lib.ccl_reduce_scatter(self.send, self.shards, stream=s)
@@ -389,6 +438,16 @@ class Moe(Workload):
     def step(self, stream):
         self.lib.ccl_all_to_allv(self.send, self.counts, self.mid, self.hidden, stream=stream)
         self.lib.ccl_all_to_allv(self.mid, self.counts.T, self.back, self.hidden, stream=stream)
+
+    def oracle_sample(self, frac):
+        from oracle import collectives
+        if not hasattr(self, "_host_tokens"):
+            self._host_tokens = host_prefix(self.send, max(t.numel() for t in self.send))
+        t0 = time.perf_counter()
+        mid = collectives.all_to_allv(self._host_tokens, self.counts, self.hidden)
+        collectives.all_to_allv(mid, self.counts.T, self.hidden)
+        dt = time.perf_counter() - t0
+        return dt, self.bytes_per_step(), "oracle all-to-allv dispatch + combine, full workload"
 
     def parts(self):
         half = self.bytes_per_step() // 2
@@ -485,22 +544,23 @@ def run_reference(a, wl: Workload, rank: int, world: int) -> dict | None:
 
 
 def cpu_baseline(wl: Workload) -> dict | None:
-    """Time the oracle on the host for ~10-30 s of work (rank 0, N=1 only)."""
-    if not hasattr(wl, "oracle_sample"):
-        return None
+    """Time the oracle on the host for ~10-30 s of work (rank 0, N=1 only): the
+    full workload when one pass takes under ~1 s, else a prefix sample."""
     try:
-        t_full, nb_full, desc = wl.oracle_sample(1.0)
+        t1, _, _ = wl.oracle_sample(0.01)
     except NotImplementedError:
         return None
-    reps = max(1, min(30, int(12.0 / max(t_full, 1e-6))))
-    times = [t_full]
+    frac = min(1.0, 0.01 * 1.0 / max(t1, 1e-6))  # one sample of about a second
+    t_s, nb, desc = wl.oracle_sample(frac)
+    reps = max(1, min(30, int(12.0 / max(t_s, 1e-6))))
+    times = [t_s]
     for _ in range(reps - 1):
-        dt, nb_full, desc = wl.oracle_sample(1.0)
+        dt, nb, desc = wl.oracle_sample(frac)
         times.append(dt)
     t = statistics.median(times)
-    return {"value": round(nb_full / t / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
-            "kind": "oracle", "sample": f"{desc}, full workload, median of {len(times)} runs",
-            "seconds_per_step": round(t, 4)}
+    return {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
+            "kind": "oracle", "sample": f"{desc}; median of {len(times)} runs",
+            "seconds_per_sample": round(t, 4)}
 
 
 def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
@@ -617,6 +677,78 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
     return out
 
 
+def run_sweep(a) -> int:
+    """Message-size sweep of the fused all-reduce: one JSON line per point.
+
+    Per point, K calls are captured in a CUDA graph (small messages are
+    launch-bound, and host-side call overhead would otherwise leave the GPU
+    idle between kernels) and the graph is replayed under CUDA events on the
+    replay stream.  The calls rotate over enough buffer sets that the rotated
+    footprint is at least twice the L2 where memory allows, so mid-size
+    messages are not served from L2 left by the previous call.
+    """
+    import torch
+    from a2a_ring_ordered_gb300 import ccl as lib
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    peak, peak_src = measured_peak_gbs()
+    dtypes = [a.dtype] if a.sweep_dtype_only else ["f32", "bf16"]
+    ps = [a.p] if a.p else [2, 4, 8, 16, 72]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(4)
+    s = torch.cuda.Stream(device)
+    for dt in dtypes:
+        e = 4 if dt == "f32" else 2
+        tdt = torch.float32 if dt == "f32" else torch.bfloat16
+        for p in ps:
+            top = 28 if p == 72 else 30  # p=72 up to 256 MiB per rank, else 1 GiB
+            for lg in range(10, top + 1, a.sweep_stride):
+                nbytes_rank = 1 << lg
+                n = nbytes_rank // e
+                foot = 2 * p * nbytes_rank
+                sets = int(min(64, max(1, -(-2 * L2_BYTES // foot))))
+                arena_in = (torch.rand(sets * p * n, generator=gen, device=device) * 2 - 1).to(tdt)
+                arena_out = torch.empty(sets * p * n, dtype=tdt, device=device)
+                views = [([arena_in[(j * p + r) * n:(j * p + r + 1) * n] for r in range(p)],
+                          [arena_out[(j * p + r) * n:(j * p + r + 1) * n] for r in range(p)])
+                         for j in range(sets)]
+                est_us = max(2.0, foot / (peak * 1e3))
+                k = int(min(4000, max(2 * sets, 20000.0 / est_us)))
+                with torch.cuda.stream(s):
+                    for j in range(min(sets, 3)):  # warm-up outside capture
+                        lib.ccl_allreduce(views[j][0], views[j][1], stream=s)
+                s.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    for i in range(k):
+                        snd, rcv = views[i % sets]
+                        lib.ccl_allreduce(snd, rcv, stream=s)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 3
+                with torch.cuda.stream(s):  # replay() launches on the current stream
+                    g.replay()
+                    e0.record(s)
+                    for _ in range(reps):
+                        g.replay()
+                    e1.record(s)
+                torch.cuda.synchronize(device)
+                ms = e0.elapsed_time(e1) / (reps * k)
+                algo = 2 * p * n * e
+                gbs = algo / (ms * 1e-3) / 1e9
+                print(json.dumps({
+                    "sweep": "allreduce", "dtype": dt, "p": p, "bytes_per_rank": nbytes_rank,
+                    "us_per_call": round(ms * 1e3, 3), "effective_gbs": round(gbs, 1),
+                    "frac_of_hbm": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src,
+                    "algbw_gbs": round(nbytes_rank / (ms * 1e-3) / 1e9, 2),
+                    "busbw_gbs": round(nbytes_rank / (ms * 1e-3) / 1e9 * 2 * (p - 1) / p, 2),
+                    "buffer_sets": sets, "rotated_footprint_mb": round(sets * foot / 1e6, 1),
+                    "calls_per_graph": k}), flush=True)
+                del g, views, arena_in, arena_out
+                torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -632,10 +764,16 @@ def main(argv=None) -> int:
     ap.add_argument("--mib", type=int, default=0)
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="all-reduce message-size sweep (1 KiB..1 GiB per rank), one line per point")
+    ap.add_argument("--sweep-stride", type=int, default=1, help="log2 step between sweep sizes")
+    ap.add_argument("--sweep-dtype-only", action="store_true", help="sweep only --dtype")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 
+    if a.sweep:
+        return run_sweep(a)
     rank, world, local = dist_env()
     wl = make_workload(a)
     if a.impl == "reference":
