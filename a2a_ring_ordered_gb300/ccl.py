@@ -52,6 +52,8 @@ def _load() -> ctypes.CDLL:
         "ccl_bucket_allreduce_scale_cast": (st, [pp, pp, i32, sz, ctypes.c_float, vp]),
         "ccl_all_to_allv": (st, [pp, ctypes.POINTER(sz), pp, i32, sz, i32, vp]),
         "ccl_ring_literal_workspace_bytes": (sz, [i32, i32, sz, i32]),
+        "ccl_plan_buckets": (st, [ctypes.POINTER(sz), sz, sz, sz, ctypes.POINTER(ctypes.c_uint32),
+                                  ctypes.POINTER(sz), ctypes.POINTER(sz), ctypes.POINTER(sz)]),
         "ccl_ring_allreduce_literal": (st, [pp, pp, i32, sz, i32, i32, ctypes.POINTER(u64), vp, sz, vp]),
         "ccl_ring_reduce_scatter_literal": (st, [pp, pp, i32, sz, i32, i32, ctypes.POINTER(u64), vp, sz, vp]),
         "ccl_ring_all_gather_literal": (st, [pp, pp, i32, sz, i32, ctypes.POINTER(u64), vp]),
@@ -157,6 +159,24 @@ def ccl_chunk_bounds(p: int, n: int, c: int) -> tuple[int, int]:
     off, ln = ctypes.c_size_t(), ctypes.c_size_t()
     _check(LIB.ccl_chunk_bounds(p, n, c, ctypes.byref(off), ctypes.byref(ln)), "ccl_chunk_bounds")
     return off.value, ln.value
+
+
+def ccl_plan_buckets(numel, elem_bytes: int = 4, cap_bytes: int = 25 * 1024 * 1024):
+    """DDP bucket plan: gradients (element counts, in ready order) -> buckets.
+
+    Returns (bucket_of, offset, bucket_numel): per gradient its bucket and
+    element offset in it, and per bucket its element count.
+    """
+    numel = [int(m) for m in numel]
+    count = len(numel)
+    arr = (ctypes.c_size_t * max(1, count))(*numel)
+    bucket_of = (ctypes.c_uint32 * max(1, count))()
+    offset = (ctypes.c_size_t * max(1, count))()
+    bucket_numel = (ctypes.c_size_t * max(1, count))()
+    nb = ctypes.c_size_t()
+    _check(LIB.ccl_plan_buckets(arr, count, elem_bytes, cap_bytes, bucket_of, offset, bucket_numel,
+                                ctypes.byref(nb)), "ccl_plan_buckets")
+    return list(bucket_of)[:count], list(offset)[:count], list(bucket_numel)[:nb.value]
 
 
 # ------------------------------------------------------------- fused calls

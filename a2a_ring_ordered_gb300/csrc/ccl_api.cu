@@ -174,6 +174,17 @@ ccl_status_t check_gather(const void* const* send, void* const* recv, int p, siz
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 }  // namespace
+
+void clear_last_error() { clear_error(); }
+
+ccl_status_t report_error(ccl_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_error, sizeof(t_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
 }  // namespace ccl
 
 using namespace ccl;

@@ -77,6 +77,11 @@ struct XferArgs {
 };
 cudaError_t launch_xfer(int kind, int dt, int op, const XferArgs& a, cudaStream_t s);
 
+// Reason text for ccl_last_error() (per calling thread), for entry points
+// that live outside ccl_api.cu.
+void clear_last_error();
+ccl_status_t report_error(ccl_status_t st, const char* fmt, ...);
+
 // Records one successful kernel launch (ccl_kernel_launch_count).
 void note_launch();
 

@@ -456,6 +456,107 @@ class Moe(Workload):
         return [("a2av", half, d), ("a2av", half, c)]
 
 
+class Ddp(Workload):
+    """DDP bucketed gradient all-reduce of a synthetic transformer's gradients:
+    p=8 ranks, 24 layers of width 1024 (+ embedding), 25 MiB buckets filled in
+    backprop order.  One step = every bucket's fused all-reduce + 1/p + bf16."""
+    name = "ddp_bucketed_allreduce"
+    kernel = "fold"
+
+    def __init__(self, p=8, layers=24, d=1024, vocab=50257):
+        self.p, self.layers, self.d, self.vocab = p, layers, d, vocab
+        shapes = [(vocab, d)]
+        for _ in range(layers):
+            shapes += [(3 * d, d), (3 * d,), (d, d), (d,), (d,), (d,), (4 * d, d), (4 * d,),
+                       (d, 4 * d), (d,), (d,), (d,)]
+        self.shapes = shapes + [(d,), (d,)]
+        self.kernel_key = f"fold_ddp_p{p}_l{layers}_d{d}"
+
+    def config(self):
+        return {"workload": f"DDP bucketed all-reduce: p={self.p} ranks, {len(self.shapes)} gradients of a "
+                            f"{self.layers}-layer d={self.d} transformer ({self.total} fp32 per rank) in "
+                            f"{len(self.gb.bucket_numel)} buckets of <= 25 MiB -> bf16",
+                "p": self.p, "params_per_rank": self.total, "buckets": len(self.gb.bucket_numel),
+                "inputs": "N(0,1e-3) drawn on the device (torch Philox, seed 1)"}
+
+    def setup(self, lib, torch, device):
+        from a2a_ring_ordered_gb300.ddp import GradBuckets, OverlappedReducer
+        self.lib, self.torch, self.device = lib, torch, device
+        self.gb = GradBuckets(self.shapes, self.p, device)
+        self.total = sum(self.gb.bucket_numel)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(1)
+        # the synthetic backward copies these into the gradient buckets
+        self.src = [[torch.randn(m, generator=gen, device=device) * 1e-3 for _ in range(self.p)]
+                    for m in self.gb.bucket_numel]
+        for b in range(self.gb.num_buckets):
+            for r in range(self.p):
+                self.gb.grads[b][r].copy_(self.src[b][r])
+        self.red = OverlappedReducer(self.gb)
+        self.producer = torch.cuda.Stream(device)
+
+    def bytes_per_step(self):
+        return self.p * self.total * 6
+
+    def step(self, stream):
+        for b in range(self.gb.num_buckets):
+            self.gb.reduce_bucket(b, stream=stream)
+
+    def parts(self):
+        big = max(range(self.gb.num_buckets), key=lambda b: self.gb.bucket_numel[b])
+        return [("fold", self.p * self.gb.bucket_numel[big] * 6,
+                 lambda s: self.gb.reduce_bucket(big, stream=s))]
+
+    def _backward_and_reduce(self, overlap: bool):
+        torch = self.torch
+        cur = torch.cuda.current_stream(self.device)
+        self.producer.wait_stream(cur)
+        self.red.comm.wait_stream(cur)
+        self.red.start_step()
+        with torch.cuda.stream(self.producer):
+            for b in range(self.gb.num_buckets):  # buckets fill in backprop order
+                for r in range(self.p):
+                    self.gb.grads[b][r].copy_(self.src[b][r])
+                if overlap:
+                    for q in self.gb.members[b]:
+                        self.red.mark_ready(q, self.producer)
+        if not overlap:
+            self.red.comm.wait_stream(self.producer)
+            for b in range(self.gb.num_buckets):
+                for q in self.gb.members[b]:
+                    self.red.mark_ready(q, self.red.comm)
+        self.red.finish(cur)
+        cur.wait_stream(self.producer)
+
+    def overlap_report(self, reps=5):
+        torch = self.torch
+        out = {}
+        for mode in ("serial", "overlapped"):
+            self._backward_and_reduce(mode == "overlapped")
+            torch.cuda.synchronize(self.device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            cur = torch.cuda.current_stream(self.device)
+            e0.record(cur)
+            for _ in range(reps):
+                self._backward_and_reduce(mode == "overlapped")
+            e1.record(cur)
+            torch.cuda.synchronize(self.device)
+            out[f"step_ms_{mode}"] = round(e0.elapsed_time(e1) / reps, 4)
+        out["note"] = ("synthetic backward = one device copy per bucket per rank; on one GPU it "
+                       "shares HBM with the all-reduce, so overlap hides launch gaps, not bandwidth")
+        return out
+
+    def oracle_sample(self, frac):
+        from oracle import ring
+        b = 0
+        m = max(self.p, int(self.gb.bucket_numel[b] * frac))
+        xs = host_prefix(self.gb.grads[b], m)
+        t0 = time.perf_counter()
+        ring.bucket_allreduce_scale_cast(xs, self.gb.scale)
+        dt = time.perf_counter() - t0
+        return dt, self.p * m * 6, f"oracle bucket all-reduce on the first {m} elements of bucket 0"
+
+
 def make_workload(a) -> Workload:
     if a.workload == "bucket":
         return Bucket()
@@ -471,6 +572,8 @@ def make_workload(a) -> Workload:
         return Zero()
     if a.workload == "moe":
         return Moe()
+    if a.workload == "ddp":
+        return Ddp()
     raise SystemExit(f"unknown workload {a.workload}")
 
 
@@ -672,6 +775,8 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
     }
     if e2e is not None:
         out["e2e"] = e2e
+    if hasattr(wl, "overlap_report"):
+        out["overlap"] = wl.overlap_report()
     if world == 1 and not a.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
     return out
@@ -759,7 +864,7 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bucket",
                     choices=["bucket", "allreduce", "reduce_scatter", "all_gather", "zero", "moe",
-                             "literal"])
+                             "literal", "ddp"])
     ap.add_argument("--p", type=int, default=0)
     ap.add_argument("--mib", type=int, default=0)
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])

@@ -145,6 +145,28 @@ ccl_status_t ccl_bucket_allreduce_scale_cast(const float* const* grads, void* co
 ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts, void* const* recv,
                              int p, size_t row_elems, ccl_dtype_t dt, void* stream);
 
+/* DDP gradient bucketing ("dist_train", Communication-Computation Overlap:
+ * with bucket_cap_mb = 25 the gradients are cut into buckets in the order
+ * backprop produces them, and a bucket is all-reduced as soon as all of its
+ * gradients are ready).  Host only; nothing is enqueued.
+ *   numel[i]      element count of gradient i, in the order gradients become
+ *                 ready (DDP: the reverse of parameter registration order).
+ *   elem_bytes    bytes per gradient element (4 for fp32).
+ *   cap_bytes     bucket capacity in bytes (25 MiB for bucket_cap_mb = 25).
+ *   bucket_of     out, count entries: bucket index of gradient i.
+ *   offset        out, count entries: element offset of gradient i in its
+ *                 bucket (a bucket is the contiguous concatenation of its
+ *                 gradients, in order).
+ *   bucket_numel  out, capacity count entries (may be NULL): elements per bucket.
+ *   num_buckets   out: number of buckets.
+ * Rule: a gradient joins the current bucket while the bucket stays within
+ * cap_bytes, else it starts the next bucket; a gradient larger than the cap
+ * gets a bucket of its own.  Errors: NULL outputs, elem_bytes == 0 or
+ * cap_bytes < elem_bytes -> CCL_ERR_INVALID_ARG. */
+ccl_status_t ccl_plan_buckets(const size_t* numel, size_t count, size_t elem_bytes,
+                              size_t cap_bytes, uint32_t* bucket_of, size_t* offset,
+                              size_t* bucket_numel, size_t* num_buckets);
+
 /* ------------------------------------------------------- literal ring engine
  * Executes the ring schedule as written: the reduce-scatter phase's p-1 steps
  * (rank r sends its partial of chunk (r-s-1) mod p to rank r+1, which adds its
