@@ -103,6 +103,7 @@ __device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
 }
 
 __global__ void __launch_bounds__(kThreads) a2av_kernel(const __grid_constant__ A2AArgs a) {
+  pdl_enter();
   for (uint64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
     // the block that owns tile t: the last one whose first tile is <= t
     int lo = 0, hi = a.ndesc - 1;
@@ -136,8 +137,7 @@ cudaError_t launch_a2av(const A2AArgs& a, cudaStream_t s) {
   if (a.total_tiles == 0 || a.ndesc == 0) return cudaSuccess;
   uint64_t g = a.total_tiles;
   if (g > (1u << 30)) g = 1u << 30;
-  a2av_kernel<<<static_cast<unsigned>(g), kThreads, 0, s>>>(a);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_kernel(a2av_kernel, dim3(static_cast<unsigned>(g)), dim3(kThreads), s, a);
   if (err == cudaSuccess) note_launch();
   return err;
 }

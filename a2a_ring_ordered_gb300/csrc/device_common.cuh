@@ -163,6 +163,39 @@ __device__ __forceinline__ void store_one(void* base, uint64_t i, const uint32_t
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Kernels are launched with programmatic stream serialisation, so a kernel
+// may be scheduled while the previous kernel in the stream is still draining.
+// pdl_enter() must run before the kernel touches global memory: it waits
+// until every earlier grid in the stream has completed and its writes are
+// visible, then lets the next grid be scheduled.  When the previous work is
+// not a programmatic launch both instructions cost nothing.
+#ifndef CCL_PDL
+#define CCL_PDL 1
+#endif
+__device__ __forceinline__ void pdl_enter() {
+#if CCL_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+template <typename Args>
+cudaError_t launch_kernel(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t s,
+                          const Args& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = CCL_PDL ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
 // ------------------------------------------------------------- chunk rule
 // Chunk c of an n-element buffer split p ways: the first n mod p chunks hold
 // one extra element (numpy's array_split).

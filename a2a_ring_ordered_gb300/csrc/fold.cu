@@ -90,6 +90,7 @@ __device__ __forceinline__ void emit(const FoldArgs& a, int p, int c, const Chun
 template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE>
 __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ FoldArgs a) {
   using Acc = typename Elem<DT_IN>::Acc;
+  pdl_enter();
   const int p = a.p;
   const int c = blockIdx.y;
   const Chunk ch = chunk_of(c, a.q, a.rem);
@@ -169,6 +170,7 @@ __device__ __forceinline__ void fold_vectors(const FoldArgs& a, int p, int first
 template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE, int BATCH, int U>
 __global__ void __launch_bounds__(kThreads) fold_unrolled_kernel(const __grid_constant__ FoldArgs a) {
   using Acc = typename Elem<DT_IN>::Acc;
+  pdl_enter();
   const int p = a.p;
   const int c = blockIdx.y;
   const Chunk ch = chunk_of(c, a.q, a.rem);
@@ -211,8 +213,8 @@ cudaError_t launch_unrolled(const FoldArgs& a, cudaStream_t s) {
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.p));
-  fold_unrolled_kernel<DT_IN, DT_OUT, VEC, OP, MODE, BATCH, U><<<grid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(fold_unrolled_kernel<DT_IN, DT_OUT, VEC, OP, MODE, BATCH, U>, grid,
+                       dim3(kThreads), s, a);
 }
 
 constexpr int kVectorsPerThread = 2;
@@ -224,8 +226,7 @@ cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.p));
-  fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE><<<grid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE>, grid, dim3(kThreads), s, a);
 }
 
 // Small p (sums only) goes to fold_unrolled_kernel with (ranks per batch,

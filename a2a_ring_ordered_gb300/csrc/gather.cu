@@ -33,6 +33,7 @@ __device__ __forceinline__ void load_elems(const void* base, uint64_t i, uint32_
 template <int DT, int VEC, int U>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
   constexpr int W = (VEC * Elem<DT>::kBytes + 3) / 4;
+  pdl_enter();
   const int p = a.p;
   const int k = blockIdx.y;
   const Chunk ch = chunk_of(k, a.q, a.rem);
@@ -90,8 +91,7 @@ cudaError_t launch_one(const GatherArgs& a, cudaStream_t s) {
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.p));
-  gather_kernel<DT, VEC, U><<<grid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(gather_kernel<DT, VEC, U>, grid, dim3(kThreads), s, a);
 }
 
 template <int DT>

@@ -53,6 +53,7 @@ template <int KIND, int DT, int OP>
 __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ XferArgs a) {
   using T = XferTypes<KIND, DT>;
   constexpr int VEC = T::kVec;
+  pdl_enter();
   const int r = blockIdx.y;
   const char* src = a.src[r];
   char* dst = a.dst[r];
@@ -74,8 +75,8 @@ cudaError_t launch_one(const XferArgs& a, cudaStream_t s) {
   uint64_t gx = (longest / VEC + 2 * kThreads - 1) / (2 * kThreads);
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
-  xfer_kernel<KIND, DT, OP><<<dim3(static_cast<unsigned>(gx), a.p), kThreads, 0, s>>>(a);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_kernel(xfer_kernel<KIND, DT, OP>, dim3(static_cast<unsigned>(gx), a.p),
+                                  dim3(kThreads), s, a);
   if (err == cudaSuccess) note_launch();
   return err;
 }
