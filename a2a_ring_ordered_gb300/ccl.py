@@ -25,6 +25,7 @@ CCL_OK, CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED, CCL_ERR_CUDA = 0, 1, 2, 3
 CCL_F32, CCL_BF16, CCL_I32 = 0, 1, 2
 CCL_SUM, CCL_MAX, CCL_MIN = 0, 1, 2
 CCL_KIND_ALLREDUCE, CCL_KIND_REDUCE_SCATTER, CCL_KIND_ALL_GATHER = 0, 1, 2
+SCHEDULES = {"ring": 0, "recursive_doubling": 1, "rabenseifner": 2, "binomial_tree": 3, "naive": 4}
 CCL_MAX_RANKS = 128
 
 _DTYPES = {torch.float32: CCL_F32, torch.bfloat16: CCL_BF16, torch.int32: CCL_I32}
@@ -47,6 +48,7 @@ def _load() -> ctypes.CDLL:
         "ccl_kernel_launch_count": (u64, []),
         "ccl_chunk_bounds": (st, [i32, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
         "ccl_allreduce": (st, [pp, pp, i32, sz, i32, i32, vp]),
+        "ccl_allreduce_schedule": (st, [pp, pp, i32, sz, i32, i32, i32, vp]),
         "ccl_reduce_scatter": (st, [pp, pp, i32, sz, i32, i32, vp]),
         "ccl_all_gather": (st, [pp, pp, i32, sz, i32, vp]),
         "ccl_bucket_allreduce_scale_cast": (st, [pp, pp, i32, sz, ctypes.c_float, vp]),
@@ -192,6 +194,24 @@ def ccl_allreduce(send, recv, op: str = "sum", stream=None) -> None:
                              _ptr_array([t.data_ptr() for t in recv]), p, n,
                              _dtype_code(send[0]), _op_code(op), _stream(stream, send[0].device)),
            "ccl_allreduce")
+
+
+def ccl_allreduce_schedule(send, recv, schedule: str = "ring", op: str = "sum", stream=None) -> None:
+    """All-reduce with the bits another schedule (recursive_doubling,
+    rabenseifner, binomial_tree, naive, ring) would give."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    if len(recv) != p or recv[0].dtype != send[0].dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    if schedule not in SCHEDULES:
+        raise ValueError(f"schedule must be one of {sorted(SCHEDULES)}")
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [n] * p, "recv")
+    _check(LIB.ccl_allreduce_schedule(_ptr_array([t.data_ptr() for t in send]),
+                                      _ptr_array([t.data_ptr() for t in recv]), p, n,
+                                      _dtype_code(send[0]), _op_code(op), SCHEDULES[schedule],
+                                      _stream(stream, send[0].device)),
+           "ccl_allreduce_schedule")
 
 
 def ccl_reduce_scatter(send, recv, op: str = "sum", stream=None) -> None:

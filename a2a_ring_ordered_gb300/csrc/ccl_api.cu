@@ -250,6 +250,39 @@ extern "C" ccl_status_t ccl_allreduce(const void* const* send, void* const* recv
   return fused_reduce(kModeAllReduce, send, recv, p, n, dt, op, stream);
 }
 
+extern "C" ccl_status_t ccl_allreduce_schedule(const void* const* send, void* const* recv, int p,
+                                               size_t n, ccl_dtype_t dt, ccl_op_t op,
+                                               ccl_schedule_t schedule, void* stream) {
+  clear_error();
+  if (schedule == CCL_SCHEDULE_RING) return ccl_allreduce(send, recv, p, n, dt, op, stream);
+  if (schedule < CCL_SCHEDULE_RECURSIVE_DOUBLING || schedule > CCL_SCHEDULE_NAIVE)
+    return fail(CCL_ERR_INVALID_ARG, "unknown schedule %d", static_cast<int>(schedule));
+  ccl_status_t st = check_reduce(0, send, recv, p, n, dt, op);
+  if (st != CCL_OK) return st;
+  if (op != CCL_SUM)
+    return fail(CCL_ERR_UNSUPPORTED, "schedules other than the ring are implemented for SUM only");
+  if ((schedule == CCL_SCHEDULE_RECURSIVE_DOUBLING || schedule == CCL_SCHEDULE_RABENSEIFNER) &&
+      (p & (p - 1)) != 0)
+    return fail(CCL_ERR_INVALID_ARG, "this schedule needs p to be a power of two (p=%d)", p);
+  if (n == 0) return CCL_OK;
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.send[r] = send[r];
+    a.recv[r] = recv[r];
+  }
+  a.p = p;
+  a.q = n / static_cast<uint64_t>(p);
+  a.rem = n % static_cast<uint64_t>(p);
+  a.scale = 1.0f;
+  const bool vec = all_aligned16(send, p, const_cast<const void* const*>(recv));
+  cudaError_t err = launch_schedule_fold(dt, schedule == CCL_SCHEDULE_NAIVE,
+                                         schedule == CCL_SCHEDULE_RABENSEIFNER, vec, a, n,
+                                         as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "schedule kernel launch");
+  return CCL_OK;
+}
+
 extern "C" ccl_status_t ccl_reduce_scatter(const void* const* send, void* const* recv, int p,
                                            size_t n, ccl_dtype_t dt, ccl_op_t op, void* stream) {
   clear_error();

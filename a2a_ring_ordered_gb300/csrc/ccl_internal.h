@@ -31,6 +31,12 @@ struct FoldArgs {
 // `vec`: every pointer is 16-byte aligned, so 16-byte vectors may be used.
 cudaError_t launch_fold(int mode, int dt, int op, bool vec, const FoldArgs& a, cudaStream_t s);
 
+// Fold in another schedule's order (schedule_fold.cu): `linear` = the naive
+// root's rank-order fold; otherwise the pairwise tree over ranks in identity
+// or (`reversed`) bit-reversed order.
+cudaError_t launch_schedule_fold(int dt, bool linear, bool reversed, bool vec, const FoldArgs& a,
+                                 uint64_t n, cudaStream_t s);
+
 // ---------------------------------------------------------------- all-gather
 struct GatherArgs {
   const void* send[CCL_MAX_RANKS];  // rank k's block (len(k) elements)

@@ -240,8 +240,23 @@ cudaError_t launch_typed(bool vec, const FoldArgs& a, cudaStream_t s) {
   constexpr int VEC = vec_width<DT_IN, DT_OUT>();
   if constexpr (OP == CCL_SUM) {
     constexpr bool kHalve = VEC > 4;
-    if (a.p <= 2) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 2, kHalve ? 4 : 8>(a, s);
-    if (a.p <= 4) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 4, kHalve ? 2 : 4>(a, s);
+    // Mid-size messages: with many vectors per thread the grid can be only one
+    // or two CTAs per SM, and the SMs that got two finish last.  Below about
+    // 8 CTAs per SM take fewer vectors per thread instead.
+    const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
+    const int sms = current_sm_count();
+    const uint64_t want_ctas = 8ull * static_cast<uint64_t>(sms > 0 ? sms : 1);
+    auto ctas = [&](int u) { return (per_chunk + kThreads * u - 1) / (kThreads * u) * a.p; };
+    if (a.p <= 2) {
+      if (ctas(kHalve ? 4 : 8) >= want_ctas)
+        return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 2, kHalve ? 4 : 8>(a, s);
+      return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 2, kHalve ? 1 : 2>(a, s);
+    }
+    if (a.p <= 4) {
+      if (ctas(kHalve ? 2 : 4) >= want_ctas)
+        return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 4, kHalve ? 2 : 4>(a, s);
+      return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 4, 1>(a, s);
+    }
     if constexpr (!kHalve) {
       if (a.p <= 8) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 8, 2>(a, s);
     }

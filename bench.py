@@ -255,8 +255,9 @@ class Bucket(Workload):
 class AllReduce(Workload):
     kernel = "fold"
 
-    def __init__(self, p=16, mib=256, dtype="f32", seed=4, op="sum", literal=False):
+    def __init__(self, p=16, mib=256, dtype="f32", seed=4, op="sum", literal=False, schedule="ring"):
         self.p, self.dtype, self.seed, self.op, self.literal = p, dtype, seed, op, literal
+        self.schedule = schedule
         self.e = 4 if dtype == "f32" else 2
         self.n = mib * (1 << 20) // self.e
         self.mib = mib
@@ -268,8 +269,8 @@ class AllReduce(Workload):
         self.launches_per_step = (2 * p - 1 + (1 if dtype == "bf16" else 0)) if literal else 1
 
     def config(self):
-        return {"workload": f"{'literal ring' if self.literal else 'fused'} all-reduce: p={self.p} ranks x "
-                            f"{self.mib} MiB {self.dtype} per rank",
+        kind = "literal ring" if self.literal else f"fused {self.schedule.replace('_', ' ')}"
+        return {"workload": f"{kind} all-reduce: p={self.p} ranks x {self.mib} MiB {self.dtype} per rank",
                 "p": self.p, "n_per_rank": self.n, "inputs": f"U(-1,1) seed {self.seed}"}
 
     def bytes_per_step(self):
@@ -289,7 +290,12 @@ class AllReduce(Workload):
             self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
 
     def oracle_sample(self, frac):
-        from oracle import ring
+        from oracle import ring, schedules
+        if self.schedule != "ring":
+            return oracle_prefix_sample(
+                self.send, self.n, frac,
+                lambda xs: schedules.allreduce(self.schedule, xs, self.dtype, self.op),
+                2 * self.p * self.e, f"oracle {self.schedule} all-reduce")
         return oracle_prefix_sample(self.send, self.n, frac,
                                     lambda xs: ring.ring_allreduce(xs, self.dtype, self.op),
                                     2 * self.p * self.e, "oracle ring all-reduce")
@@ -298,6 +304,9 @@ class AllReduce(Workload):
         if self.literal:
             self.lib.ccl_ring_allreduce_literal(self.send, self.recv, op=self.op,
                                                 workspace=self.ws, stream=stream)
+        elif self.schedule != "ring":
+            self.lib.ccl_allreduce_schedule(self.send, self.recv, self.schedule, op=self.op,
+                                            stream=stream)
         else:
             self.lib.ccl_allreduce(self.send, self.recv, op=self.op, stream=stream)
 
@@ -561,7 +570,7 @@ def make_workload(a) -> Workload:
     if a.workload == "bucket":
         return Bucket()
     if a.workload == "allreduce":
-        return AllReduce(p=a.p or 16, mib=a.mib or 256, dtype=a.dtype)
+        return AllReduce(p=a.p or 16, mib=a.mib or 256, dtype=a.dtype, schedule=a.schedule)
     if a.workload == "literal":
         return AllReduce(p=a.p or 8, mib=a.mib or 25, dtype=a.dtype, literal=True)
     if a.workload == "reduce_scatter":
@@ -868,6 +877,9 @@ def main(argv=None) -> int:
     ap.add_argument("--p", type=int, default=0)
     ap.add_argument("--mib", type=int, default=0)
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
+    ap.add_argument("--schedule", default="ring",
+                    choices=["ring", "recursive_doubling", "rabenseifner", "binomial_tree", "naive"],
+                    help="fold order of --workload allreduce")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="all-reduce message-size sweep (1 KiB..1 GiB per rank), one line per point")

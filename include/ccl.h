@@ -63,6 +63,16 @@ typedef enum { CCL_F32 = 0, CCL_BF16 = 1, CCL_I32 = 2 } ccl_dtype_t;
  * so ties and NaNs resolve in ring order too. */
 typedef enum { CCL_SUM = 0, CCL_MAX = 1, CCL_MIN = 2 } ccl_op_t;
 
+/* All-reduce schedules of "Networks and Collective Communication" section 5.2.
+ * Each fixes the order in which an element's p values are added. */
+typedef enum {
+  CCL_SCHEDULE_RING = 0,               /* the ring (ccl_allreduce) */
+  CCL_SCHEDULE_RECURSIVE_DOUBLING = 1, /* pairs at distance 1, 2, 4, ...; p a power of two */
+  CCL_SCHEDULE_RABENSEIFNER = 2,       /* halving: pairs at distance p/2, p/4, ...; p a power of two */
+  CCL_SCHEDULE_BINOMIAL_TREE = 3,      /* binomial reduce to rank 0 + broadcast; any p */
+  CCL_SCHEDULE_NAIVE = 4               /* rank 0 adds ranks 1..p-1 in order, then broadcasts */
+} ccl_schedule_t;
+
 typedef enum {
   CCL_KIND_ALLREDUCE = 0,
   CCL_KIND_REDUCE_SCATTER = 1,
@@ -102,6 +112,18 @@ ccl_status_t ccl_chunk_bounds(int p, size_t n, int c, size_t* off, size_t* len);
  * Every recv[r] receives the same ring-ordered reduction.  n == 0 is a no-op. */
 ccl_status_t ccl_allreduce(const void* const* send, void* const* recv, int p, size_t n,
                            ccl_dtype_t dt, ccl_op_t op, void* stream);
+
+/* All-reduce with the result another schedule would give, in one fused pass
+ * (same buffers and aliasing rules as ccl_allreduce).  Recursive doubling and
+ * the binomial tree add pairwise over ranks 0..p-1 (the same bits: IEEE
+ * addition commutes, so only the pairing matters); Rabenseifner adds pairwise
+ * over the ranks in bit-reversed order; naive adds in rank order from rank 0.
+ * CCL_SCHEDULE_RING is ccl_allreduce.  Errors: recursive doubling or
+ * Rabenseifner with p not a power of two -> CCL_ERR_INVALID_ARG; MAX / MIN
+ * with a schedule other than the ring -> CCL_ERR_UNSUPPORTED. */
+ccl_status_t ccl_allreduce_schedule(const void* const* send, void* const* recv, int p, size_t n,
+                                    ccl_dtype_t dt, ccl_op_t op, ccl_schedule_t schedule,
+                                    void* stream);
 
 /* Reduce-scatter ("dist_train": process k gets sum_i x_i^(k); ZeRO's key op).
  *   send[r]  p device pointers, each n elements.

@@ -425,3 +425,46 @@ def test_sweep_largest_sizes_sampled(lib, dtype, p, mib):
     view = torch.int16 if dtype == "bf16" else torch.int32
     for r in range(1, p):
         assert torch.equal(recv[r].view(view), recv[0].view(view))
+
+
+# ------------------------------------------------ other all-reduce schedules
+SCHED_CASES = [(s, p, n) for s in ("recursive_doubling", "rabenseifner") for p, n in
+               [(2, 4099), (4, 1000), (8, 70001), (16, 65536), (128, 1000)]] + \
+              [(s, p, n) for s in ("binomial_tree", "naive") for p, n in
+               [(1, 10), (2, 4099), (3, 1001), (5, 13), (7, 70001), (16, 65536), (72, 1000)]]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("schedule,p,n", SCHED_CASES)
+def test_allreduce_schedules_match_their_oracles(lib, dtype, schedule, p, n):
+    from oracle import schedules
+
+    x = make_inputs(dtype, p, n, seed=p + 31 * n)
+    want, _ = schedules.allreduce(schedule, x, dtype)
+    outs = guarded_outputs(p, [n] * p, dtype)
+    lib.ccl_allreduce_schedule([to_dev(v, dtype) for v in x], [o.view for o in outs], schedule)
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"{schedule} p={p} rank {r}")
+        assert outs[r].guards_intact()
+
+
+def test_schedule_discriminators_on_gpu(lib):
+    """Hand-derived per-schedule values (see tests/test_oracle_schedules.py)."""
+    cases = {"recursive_doubling": 1.0, "binomial_tree": 1.0, "rabenseifner": 2.0, "naive": 1.0,
+             "ring": None}
+    vals = [2.0**24, 1.0, -(2.0**24), 1.0]
+    n = 4096 + 3
+    send = [torch.full((n,), v, device="cuda") for v in vals]
+    for s, want in cases.items():
+        recv = [torch.empty(n, device="cuda") for _ in range(4)]
+        lib.ccl_allreduce_schedule(send, recv, s)
+        if want is not None:
+            assert (to_host(recv[0]) == want).all(), s
+
+
+def test_schedule_argument_errors(lib):
+    x = [torch.ones(8, device="cuda") for _ in range(6)]
+    with pytest.raises(lib.CclError):
+        lib.ccl_allreduce_schedule(x, [torch.empty_like(t) for t in x], "recursive_doubling")
+    with pytest.raises(lib.CclError):
+        lib.ccl_allreduce_schedule(x, [torch.empty_like(t) for t in x], "naive", op="max")
