@@ -51,6 +51,10 @@ def _load() -> ctypes.CDLL:
         "ccl_allreduce_schedule": (st, [pp, pp, i32, sz, i32, i32, i32, vp]),
         "ccl_reduce_scatter": (st, [pp, pp, i32, sz, i32, i32, vp]),
         "ccl_all_gather": (st, [pp, pp, i32, sz, i32, vp]),
+        "ccl_broadcast": (st, [vp, pp, i32, sz, i32, i32, vp]),
+        "ccl_reduce": (st, [pp, vp, i32, sz, i32, i32, i32, vp]),
+        "ccl_scatter": (st, [vp, pp, i32, sz, i32, i32, vp]),
+        "ccl_gather": (st, [pp, vp, i32, sz, i32, i32, vp]),
         "ccl_bucket_allreduce_scale_cast": (st, [pp, pp, i32, sz, ctypes.c_float, vp]),
         "ccl_all_to_allv": (st, [pp, ctypes.POINTER(sz), pp, i32, sz, i32, vp]),
         "ccl_ring_literal_workspace_bytes": (sz, [i32, i32, sz, i32]),
@@ -241,6 +245,56 @@ def ccl_all_gather(send, recv, stream=None) -> None:
                               _ptr_array([t.data_ptr() for t in recv]), p, n,
                               _dtype_code(send[0]), _stream(stream, send[0].device)),
            "ccl_all_gather")
+
+
+def _one(t: torch.Tensor, name: str) -> torch.Tensor:
+    return _tensors([t], name)[0]
+
+
+def ccl_broadcast(send, recv, root: int = 0, stream=None) -> None:
+    """Every recv[r] gets a copy of the root's buffer `send`."""
+    send, recv = _one(send, "send"), _tensors(recv, "recv")
+    p, n = len(recv), send.numel()
+    if recv[0].dtype != send.dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    _numel_check(recv, [n] * p, "recv")
+    _check(LIB.ccl_broadcast(send.data_ptr(), _ptr_array([t.data_ptr() for t in recv]), p, n,
+                             _dtype_code(send), root, _stream(stream, send.device)), "ccl_broadcast")
+
+
+def ccl_reduce(send, recv, op: str = "sum", root: int = 0, stream=None) -> None:
+    """The root's buffer `recv` gets the ring-ordered reduction of send[0..p-1]."""
+    send, recv = _tensors(send, "send"), _one(recv, "recv")
+    p, n = len(send), send[0].numel()
+    if recv.dtype != send[0].dtype:
+        raise ValueError("recv must have the send dtype")
+    _numel_check(send, [n] * p, "send")
+    _numel_check([recv], [n], "recv")
+    _check(LIB.ccl_reduce(_ptr_array([t.data_ptr() for t in send]), recv.data_ptr(), p, n,
+                          _dtype_code(recv), _op_code(op), root, _stream(stream, recv.device)),
+           "ccl_reduce")
+
+
+def ccl_scatter(send, recv, root: int = 0, stream=None) -> None:
+    """recv[k] gets chunk k of the root's buffer `send`."""
+    send, recv = _one(send, "send"), _tensors(recv, "recv")
+    p, n = len(recv), send.numel()
+    if recv[0].dtype != send.dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    _numel_check(recv, [_chunk(p, n, k)[1] for k in range(p)], "recv")
+    _check(LIB.ccl_scatter(send.data_ptr(), _ptr_array([t.data_ptr() for t in recv]), p, n,
+                           _dtype_code(send), root, _stream(stream, send.device)), "ccl_scatter")
+
+
+def ccl_gather(send, recv, root: int = 0, stream=None) -> None:
+    """The root's buffer `recv` gets the concatenation of send[0..p-1] (chunk rule)."""
+    send, recv = _tensors(send, "send"), _one(recv, "recv")
+    p, n = len(send), recv.numel()
+    if recv.dtype != send[0].dtype:
+        raise ValueError("recv must have the send dtype")
+    _numel_check(send, [_chunk(p, n, k)[1] for k in range(p)], "send")
+    _check(LIB.ccl_gather(_ptr_array([t.data_ptr() for t in send]), recv.data_ptr(), p, n,
+                          _dtype_code(recv), root, _stream(stream, recv.device)), "ccl_gather")
 
 
 def ccl_bucket_allreduce_scale_cast(grads, out_bf16, scale: float | None = None, stream=None) -> None:

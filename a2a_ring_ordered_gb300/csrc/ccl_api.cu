@@ -350,6 +350,182 @@ extern "C" ccl_status_t ccl_bucket_allreduce_scale_cast(const float* const* grad
   return CCL_OK;
 }
 
+// ========================================= broadcast / reduce / scatter / gather
+namespace {
+
+ccl_status_t check_root(int p, int root) {
+  if (root < 0 || root >= p) return fail(CCL_ERR_INVALID_ARG, "root %d outside 0..%d", root, p - 1);
+  return CCL_OK;
+}
+
+ccl_status_t copy_transfers(int dt, const char* const* src, char* const* dst, const uint64_t* len,
+                            int p, void* stream) {
+  XferArgs x;
+  memset(&x, 0, sizeof(x));
+  x.p = p;
+  for (int r = 0; r < p; ++r) {
+    x.src[r] = src[r];
+    x.dst[r] = dst[r];
+    x.len[r] = len[r];
+  }
+  cudaError_t err = launch_xfer(kXferCopy, dt, CCL_SUM, x, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "copy kernel launch");
+  return CCL_OK;
+}
+
+}  // namespace
+
+extern "C" ccl_status_t ccl_broadcast(const void* send, void* const* recv, int p, size_t n,
+                                      ccl_dtype_t dt, int root, void* stream) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK || (st = check_root(p, root)) != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  if (recv == nullptr) return fail(CCL_ERR_INVALID_ARG, "recv array is NULL");
+  if (n == 0) return CCL_OK;
+  const void* sends[1] = {send};
+  uint64_t in_b[1] = {n * e}, out_b[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  bool in_place[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    out_b[r] = n * e;
+    out[r] = span(recv[r], out_b[r]);
+    in[r] = (r == root) ? span(send, n * e) : Span{0, 0};
+    in_place[r] = (r == root) && recv[r] == send;
+  }
+  if ((st = check_buffers("send", sends, 1, in_b, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", const_cast<const void* const*>(recv), p, out_b, e)) != CCL_OK) return st;
+  for (int r = 0; r < p; ++r)  // the root's data must not overlap any other output
+    if (r != root && overlaps(out[r], span(send, n * e)))
+      return fail(CCL_ERR_INVALID_ARG, "output buffer %d overlaps the root's input", r);
+  if ((st = check_aliasing(in, out, in_place, p)) != CCL_OK) return st;
+  GatherArgs a;
+  memset(&a, 0, sizeof(a));
+  a.send[0] = send;
+  for (int r = 0; r < p; ++r) a.recv[r] = recv[r];
+  a.p = p;
+  bool vec = (reinterpret_cast<uintptr_t>(send) & 15) == 0;
+  for (int r = 0; r < p; ++r) vec = vec && (reinterpret_cast<uintptr_t>(recv[r]) & 15) == 0;
+  cudaError_t err = launch_broadcast(dt, vec, a, n, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "broadcast kernel launch");
+  return CCL_OK;
+}
+
+extern "C" ccl_status_t ccl_reduce(const void* const* send, void* recv, int p, size_t n,
+                                   ccl_dtype_t dt, ccl_op_t op, int root, void* stream) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK || (st = check_root(p, root)) != CCL_OK) return st;
+  // validate as an all-reduce whose only output is the root's
+  void* outs[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) outs[r] = nullptr;
+  if (recv == nullptr && n != 0) return fail(CCL_ERR_INVALID_ARG, "recv is NULL");
+  outs[root] = recv;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (!valid_op(op)) return fail(CCL_ERR_INVALID_ARG, "unknown op %d", op);
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  if (send == nullptr) return fail(CCL_ERR_INVALID_ARG, "send array is NULL");
+  if (n == 0) return CCL_OK;
+  uint64_t in_b[CCL_MAX_RANKS], out_b[1] = {n * e};
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  bool in_place[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    in_b[r] = n * e;
+    in[r] = span(send[r], in_b[r]);
+    out[r] = (r == root) ? span(recv, n * e) : Span{0, 0};
+    in_place[r] = (r == root) && send[r] == recv;
+  }
+  const void* const recvs[1] = {recv};
+  if ((st = check_buffers("send", send, p, in_b, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", recvs, 1, out_b, e)) != CCL_OK) return st;
+  if ((st = check_aliasing(in, out, in_place, p)) != CCL_OK) return st;
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) a.send[r] = send[r];
+  a.recv[0] = recv;
+  a.p = p;
+  a.q = n / static_cast<uint64_t>(p);
+  a.rem = n % static_cast<uint64_t>(p);
+  a.scale = 1.0f;
+  bool vec = (reinterpret_cast<uintptr_t>(recv) & 15) == 0;
+  for (int r = 0; r < p; ++r) vec = vec && (reinterpret_cast<uintptr_t>(send[r]) & 15) == 0;
+  cudaError_t err = launch_fold(kModeReduce, dt, op, vec, a, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "reduce kernel launch");
+  return CCL_OK;
+}
+
+extern "C" ccl_status_t ccl_scatter(const void* send, void* const* recv, int p, size_t n,
+                                    ccl_dtype_t dt, int root, void* stream) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK || (st = check_root(p, root)) != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  if (recv == nullptr) return fail(CCL_ERR_INVALID_ARG, "recv array is NULL");
+  if (n == 0) return CCL_OK;
+  const void* sends[1] = {send};
+  uint64_t in_b[1] = {n * e}, out_b[CCL_MAX_RANKS], len[CCL_MAX_RANKS];
+  const char* src[CCL_MAX_RANKS];
+  char* dst[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  bool in_place[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    uint64_t off, ln;
+    chunk(p, n, r, &off, &ln);
+    out_b[r] = ln * e;
+    len[r] = ln;
+    out[r] = span(recv[r], out_b[r]);
+    in[r] = (r == root) ? span(send, n * e) : Span{0, 0};
+    in_place[r] = (r == root) && static_cast<const char*>(send) + off * e == recv[r];
+    src[r] = static_cast<const char*>(send) + off * e;
+    dst[r] = static_cast<char*>(recv[r]);
+  }
+  if ((st = check_buffers("send", sends, 1, in_b, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", const_cast<const void* const*>(recv), p, out_b, e)) != CCL_OK) return st;
+  for (int r = 0; r < p; ++r)
+    if (r != root && overlaps(out[r], span(send, n * e)))
+      return fail(CCL_ERR_INVALID_ARG, "output buffer %d overlaps the root's input", r);
+  if ((st = check_aliasing(in, out, in_place, p)) != CCL_OK) return st;
+  return copy_transfers(dt, src, dst, len, p, stream);
+}
+
+extern "C" ccl_status_t ccl_gather(const void* const* send, void* recv, int p, size_t n,
+                                   ccl_dtype_t dt, int root, void* stream) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK || (st = check_root(p, root)) != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  if (send == nullptr) return fail(CCL_ERR_INVALID_ARG, "send array is NULL");
+  if (n == 0) return CCL_OK;
+  const void* const recvs[1] = {recv};
+  uint64_t in_b[CCL_MAX_RANKS], out_b[1] = {n * e}, len[CCL_MAX_RANKS];
+  const char* src[CCL_MAX_RANKS];
+  char* dst[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    uint64_t off, ln;
+    chunk(p, n, r, &off, &ln);
+    in_b[r] = ln * e;
+    len[r] = ln;
+    src[r] = static_cast<const char*>(send[r]);
+    dst[r] = static_cast<char*>(recv) + off * e;
+  }
+  if ((st = check_buffers("send", send, p, in_b, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", recvs, 1, out_b, e)) != CCL_OK) return st;
+  const Span whole = span(recv, n * e);
+  for (int r = 0; r < p; ++r) {  // only the root's own block may sit in place
+    if (!overlaps(whole, span(send[r], in_b[r]))) continue;
+    if (r == root && src[r] == dst[r]) continue;
+    return fail(CCL_ERR_INVALID_ARG, "input buffer %d overlaps the root's output", r);
+  }
+  return copy_transfers(dt, src, dst, len, p, stream);
+}
+
 // ============================================================== all-to-allv
 extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts,
                                         void* const* recv, int p, size_t row_elems,

@@ -16,7 +16,8 @@ namespace ccl {
 enum FoldMode : int {
   kModeAllReduce = 0,      // fold, write the result to every rank's buffer
   kModeReduceScatter = 1,  // fold, write chunk c only to rank c's shard
-  kModeBucket = 2          // fold fp32, scale, round to bf16, write to every rank
+  kModeBucket = 2,         // fold fp32, scale, round to bf16, write to every rank
+  kModeReduce = 3          // fold, write the result only to recv[0] (the root's buffer)
 };
 
 struct FoldArgs {
@@ -45,6 +46,8 @@ struct GatherArgs {
   int p;
 };
 cudaError_t launch_gather(int dt, bool vec, const GatherArgs& a, cudaStream_t s);
+// Broadcast: send[0] (n elements) copied to recv[0..p-1]; `vec`: all 16-byte aligned.
+cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, cudaStream_t s);
 
 // ------------------------------------------------------------- all-to-allv
 // One contiguous byte block src -> dst.  Blocks are cut into tiles of

@@ -74,7 +74,9 @@ __device__ __forceinline__ void emit(const FoldArgs& a, int p, int c, const Chun
   }
   uint32_t w[words_for(VEC, Elem<DT_OUT>::kBytes)];
   pack_out<DT_OUT, VEC>(acc, w);
-  if constexpr (MODE == kModeReduceScatter) {
+  if constexpr (MODE == kModeReduce) {
+    store_raw<DT_OUT, VEC>(a.recv[0], i, w);
+  } else if constexpr (MODE == kModeReduceScatter) {
     const uint64_t j = i - ch.off;  // position in rank c's shard
     if (VEC == 1 || (ch.off % VEC) == 0) {
       store_raw<DT_OUT, VEC>(a.recv[c], j, w);
@@ -291,6 +293,8 @@ cudaError_t launch_fold(int mode, int dt, int op, bool vec, const FoldArgs& a, c
     err = launch_mode<kModeReduceScatter>(dt, op, vec, a, s);
   } else if (mode == kModeBucket) {
     err = launch_typed<kF32, kBF16, CCL_SUM, kModeBucket>(vec, a, s);
+  } else if (mode == kModeReduce) {
+    err = launch_mode<kModeReduce>(dt, op, vec, a, s);
   }
   if (err == cudaSuccess) note_launch();
   return err;

@@ -100,7 +100,73 @@ cudaError_t launch_typed(bool vec, const GatherArgs& a, cudaStream_t s) {
   return launch_one<DT, 1, 1>(a, s);
 }
 
+// Broadcast: one 1-D pass over the root's buffer (send[0]); each of a
+// thread's U vectors is loaded once and stored to all p outputs.
+template <int DT, int VEC, int U>
+__global__ void __launch_bounds__(kThreads) broadcast_kernel(const __grid_constant__ GatherArgs a,
+                                                             uint64_t n) {
+  constexpr int W = (VEC * Elem<DT>::kBytes + 3) / 4;
+  pdl_enter();
+  const int p = a.p;
+  const void* src = a.send[0];
+  const uint64_t nv = n / VEC;
+  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  for (uint64_t base = static_cast<uint64_t>(blockIdx.x) * kSpan; base < nv;
+       base += static_cast<uint64_t>(gridDim.x) * kSpan) {
+    uint32_t w[U][W];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+      if (v < nv) load_raw<DT, VEC>(src, v * VEC, w[u]);
+    }
+    for (int r = 0; r < p; ++r) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+        if (v < nv) store_raw<DT, VEC>(a.recv[r], v * VEC, w[u]);
+      }
+    }
+  }
+  if (blockIdx.x == 0) {  // tail elements
+    for (uint64_t i = nv * VEC + threadIdx.x; i < n; i += kThreads) {
+      uint32_t w[1];
+      load_raw<DT, 1>(src, i, w);
+      for (int r = 0; r < p; ++r) store_raw<DT, 1>(a.recv[r], i, w);
+    }
+  }
+}
+
+template <int DT, int VEC, int U>
+cudaError_t launch_bcast(const GatherArgs& a, uint64_t n, cudaStream_t s) {
+  const uint64_t nv = (VEC > 1) ? n / VEC : n;
+  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  uint64_t gx = (nv + kSpan - 1) / kSpan;
+  if (gx < 1) gx = 1;
+  if (gx > (1u << 30)) gx = 1u << 30;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(gx));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = CCL_PDL ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, broadcast_kernel<DT, VEC, U>, a, n);
+}
+
 }  // namespace
+
+cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, cudaStream_t s) {
+  cudaError_t err = cudaErrorInvalidValue;
+  if (dt == kF32 || dt == kI32) {
+    err = vec ? launch_bcast<kF32, 4, 4>(a, n, s) : launch_bcast<kF32, 1, 1>(a, n, s);
+  } else if (dt == kBF16) {
+    err = vec ? launch_bcast<kBF16, 8, 4>(a, n, s) : launch_bcast<kBF16, 1, 1>(a, n, s);
+  }
+  if (err == cudaSuccess) note_launch();
+  return err;
+}
 
 cudaError_t launch_gather(int dt, bool vec, const GatherArgs& a, cudaStream_t s) {
   cudaError_t err = cudaErrorInvalidValue;

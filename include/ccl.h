@@ -142,6 +142,33 @@ ccl_status_t ccl_reduce_scatter(const void* const* send, void* const* recv, int 
 ccl_status_t ccl_all_gather(const void* const* send, void* const* recv, int p, size_t n,
                             ccl_dtype_t dt, void* stream);
 
+/* Broadcast ("Networks and Collective Communication" 4.1: the root's data is
+ * copied to everyone).  send: the root's n elements; recv[r]: p outputs of n
+ * elements; recv[root] == send is allowed (in place).  One read of the root's
+ * data, p writes. */
+ccl_status_t ccl_broadcast(const void* send, void* const* recv, int p, size_t n, ccl_dtype_t dt,
+                           int root, void* stream);
+
+/* Reduce (4.1: element-wise reduction, result only on the root).  The pages
+ * fix no order for it; it is the ring's reduce-scatter followed by a gather
+ * of the shards to the root, so recv holds exactly the bits every rank gets
+ * from ccl_allreduce.  send[r]: p inputs of n elements; recv: the root's n
+ * outputs; recv == send[root] is allowed (in place). */
+ccl_status_t ccl_reduce(const void* const* send, void* recv, int p, size_t n, ccl_dtype_t dt,
+                        ccl_op_t op, int root, void* stream);
+
+/* Scatter ("dist_train", Scatter: the root holds [x_1, ..., x_p] and rank k
+ * receives x_k).  send: the root's n elements; recv[k]: len(k) elements, chunk
+ * k by the CHUNKS rule; recv[root] == send + off(root) is allowed. */
+ccl_status_t ccl_scatter(const void* send, void* const* recv, int p, size_t n, ccl_dtype_t dt,
+                         int root, void* stream);
+
+/* Gather ("dist_train", Gather: rank k holds x_k; the root receives
+ * [x_1, ..., x_p]).  send[k]: len(k) elements; recv: the root's n elements,
+ * block k at off(k); send[root] == recv + off(root) is allowed. */
+ccl_status_t ccl_gather(const void* const* send, void* recv, int p, size_t n, ccl_dtype_t dt,
+                        int root, void* stream);
+
 /* DDP gradient-bucket all-reduce with the average and the cast fused in
  * ("dist_train", Communication-Computation Overlap: DDP cuts gradients into
  * buckets of bucket_cap_mb = 25 and all-reduces each finished bucket).

@@ -40,6 +40,18 @@ def reduce(x: list[np.ndarray], root: int = 0) -> list[np.ndarray | None]:
     return [acc if r == root else None for r in range(len(x))]
 
 
+def reduce_ring(x: list[np.ndarray], root: int = 0, dtype: str = "f32", op: str = "sum"):
+    """Reduce built as the ring's reduce-scatter followed by a gather of the
+    shards to the root (the pages fix no order for reduce; this reading gives
+    the root exactly the ring all-reduce's bits).  Returns (root result, list
+    with None for the other ranks)."""
+    from .ring import ring_reduce_scatter
+
+    shards, _ = ring_reduce_scatter(x, dtype, op)
+    whole = np.concatenate(shards) if shards else np.zeros(0)
+    return [whole if r == root else None for r in range(len(x))]
+
+
 def scatter(data: np.ndarray, p: int) -> list[np.ndarray]:
     """Root's buffer cut into p chunks; rank k receives chunk k."""
     return [data[off:off + ln].copy() for off, ln in chunk_bounds(p, len(data))]

@@ -468,3 +468,77 @@ def test_schedule_argument_errors(lib):
         lib.ccl_allreduce_schedule(x, [torch.empty_like(t) for t in x], "recursive_doubling")
     with pytest.raises(lib.CclError):
         lib.ccl_allreduce_schedule(x, [torch.empty_like(t) for t in x], "naive", op="max")
+
+
+# ---------------------------------------- broadcast / reduce / scatter / gather
+ROOTED = [(1, 10), (3, 1001), (4, 4), (8, 70001), (16, 65543), (72, 1000)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,n", ROOTED)
+def test_rooted_primitives_match_oracle(lib, dtype, p, n):
+    x = make_inputs(dtype, p, n, seed=3 * p + n)
+    root = p // 2
+    send = [to_dev(v, dtype) for v in x]
+    # broadcast
+    outs = guarded_outputs(p, [n] * p, dtype)
+    lib.ccl_broadcast(send[root], [o.view for o in outs], root=root)
+    for r, o in enumerate(outs):
+        assert_equal(to_host(o.view), collectives.broadcast(x, root)[r], dtype, f"bcast {r}")
+        assert o.guards_intact()
+    # reduce: the root gets the ring all-reduce's bits
+    red = Guarded(n, dtype)
+    lib.ccl_reduce(send, red.view, root=root)
+    assert_equal(to_host(red.view), collectives.reduce_ring(x, root, dtype)[root], dtype, "reduce")
+    assert red.guards_intact()
+    # scatter of the root's buffer, then gather back to the root
+    parts = guarded_outputs(p, [ln for _, ln in ring.chunk_bounds(p, n)], dtype, offset=GUARD + 1)
+    lib.ccl_scatter(send[root], [q.view for q in parts], root=root)
+    want_parts = collectives.scatter(x[root], p)
+    for k, q in enumerate(parts):
+        assert_equal(to_host(q.view), want_parts[k], dtype, f"scatter {k}")
+        assert q.guards_intact()
+    back = Guarded(n, dtype)
+    lib.ccl_gather([q.view for q in parts], back.view, root=root)
+    assert_equal(to_host(back.view), x[root], dtype, "gather(scatter)")
+    assert back.guards_intact()
+
+
+@pytest.mark.parametrize("p,n", [(4, 1 << 20), (8, 6_553_600), (16, 1000)])
+def test_identities_on_gpu(lib, p, n):
+    """Section 4.2 on the device: broadcast = scatter + all-gather, and
+    all-reduce = reduce + broadcast, bit for bit."""
+    x = make_inputs("f32", p, n, seed=p)
+    send = [to_dev(v, "f32") for v in x]
+    root = 1
+    parts = [torch.empty(ln, device="cuda") for _, ln in ring.chunk_bounds(p, n)]
+    lib.ccl_scatter(send[root], parts, root=root)
+    via_ag = [torch.empty(n, device="cuda") for _ in range(p)]
+    lib.ccl_all_gather(parts, via_ag)
+    direct = [torch.empty(n, device="cuda") for _ in range(p)]
+    lib.ccl_broadcast(send[root], direct, root=root)
+    for a_, b_ in zip(via_ag, direct):
+        assert torch.equal(a_.view(torch.int32), b_.view(torch.int32))
+    red = torch.empty(n, device="cuda")
+    lib.ccl_reduce(send, red, root=root)
+    bc = [torch.empty(n, device="cuda") for _ in range(p)]
+    lib.ccl_broadcast(red, bc, root=root)
+    ar = [torch.empty(n, device="cuda") for _ in range(p)]
+    lib.ccl_allreduce(send, ar)
+    for a_, b_ in zip(ar, bc):
+        assert torch.equal(a_.view(torch.int32), b_.view(torch.int32))
+
+
+def test_rooted_in_place_forms(lib):
+    p, n = 5, 12345
+    x = make_inputs("f32", p, n, seed=9)
+    send = [to_dev(v, "f32") for v in x]
+    root = 2
+    outs = [torch.empty(n, device="cuda") for _ in range(p)]
+    outs[root] = send[root]
+    lib.ccl_broadcast(send[root], outs, root=root)
+    for o in outs:
+        assert_equal(to_host(o), x[root], "f32", "in-place bcast")
+    want = collectives.reduce_ring(x, root)[root]
+    lib.ccl_reduce(send, send[root], root=root)
+    assert_equal(to_host(send[root]), want, "f32", "in-place reduce")

@@ -144,3 +144,23 @@ def test_scatter_gather_are_inverse():
     data = np.arange(23, dtype=np.float32)
     parts = collectives.scatter(data, 5)
     np.testing.assert_array_equal(collectives.gather(parts, root=3)[3], data)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,n", [(1, 5), (3, 10), (4, 4), (8, 1001)])
+def test_ring_reduce_equals_allreduce_on_the_root(dtype, p, n):
+    """all-reduce = reduce + broadcast (section 4.2 family): the root's reduce
+    result is bit-identical to every rank's all-reduce result."""
+    x = (workloads.integer_valued(p, n, 5, dtype="i32") if dtype == "i32"
+         else workloads.normal(p, n, 1.0, 5, dtype=dtype))
+    ar, _, _ = ring.ring_allreduce(x, dtype)
+    for root in {0, p - 1}:
+        red = collectives.reduce_ring(x, root, dtype)
+        np.testing.assert_array_equal(red[root], ar[0])
+        assert all(red[r] is None for r in range(p) if r != root)
+
+
+def test_ring_reduce_integer_values_exact():
+    x = workloads.integer_valued(6, 37, 2)
+    red = collectives.reduce_ring(x, 2)[2]
+    np.testing.assert_array_equal(red, np.stack(x).sum(axis=0))
