@@ -25,12 +25,12 @@
 namespace ccl {
 namespace {
 
-constexpr int kMaxLevels = 8;  // p <= 128 = 2^7 leaves; one spare level
-
-template <int DT, int VEC>
+// Binary counter of pairwise subtrees, LEVELS slots (enough for 2^(LEVELS-1)
+// leaves plus the carry level), VEC lanes each.
+template <int DT, int VEC, int LEVELS>
 struct Counter {
   using Acc = typename Elem<DT>::Acc;
-  Acc slot[kMaxLevels][VEC];
+  Acc slot[LEVELS][VEC];
 
   // Add leaf number j (0-based) with values x.
   __device__ __forceinline__ void push(int j, const Acc* x) {
@@ -39,7 +39,7 @@ struct Counter {
     for (int e = 0; e < VEC; ++e) carry[e] = x[e];
     bool chain = true;
 #pragma unroll
-    for (int k = 0; k < kMaxLevels; ++k) {
+    for (int k = 0; k < LEVELS; ++k) {
       if (chain) {
         if (j & (1 << k)) {
 #pragma unroll
@@ -57,7 +57,7 @@ struct Counter {
   __device__ __forceinline__ void flush(int p, Acc* out) const {
     bool have = false;
 #pragma unroll
-    for (int k = 0; k < kMaxLevels; ++k) {
+    for (int k = 0; k < LEVELS; ++k) {
       if (p & (1 << k)) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) out[e] = have ? combine<CCL_SUM>(slot[k][e], out[e]) : slot[k][e];
@@ -72,65 +72,93 @@ __device__ __forceinline__ int rank_at(int j, int levels, bool reversed) {
   return reversed ? static_cast<int>(__brev(static_cast<unsigned>(j)) >> (32 - levels)) : j;
 }
 
-template <int DT, int VEC, int MODE>  // MODE 0: pairwise tree, 1: linear (naive)
-__device__ __forceinline__ void fold_one(const FoldArgs& a, int p, int levels, bool reversed,
-                                         uint64_t i, typename Elem<DT>::Acc* acc) {
+// Fold U vectors (t, t + kThreads, ...) of VEC elements; the loads of BATCH
+// ranks x U vectors are issued before any is folded.  MODE 0: pairwise tree,
+// 1: linear (naive).
+template <int DT, int VEC, int MODE, int LEVELS, int BATCH, int U>
+__device__ __forceinline__ void fold_vectors(const FoldArgs& a, int p, int levels, bool reversed,
+                                             uint64_t v0, uint64_t v_hi,
+                                             typename Elem<DT>::Acc (&acc)[U][VEC]) {
   using Acc = typename Elem<DT>::Acc;
   constexpr int W = (VEC * Elem<DT>::kBytes + 3) / 4;
-  constexpr int BATCH = 8;
-  Counter<DT, VEC> ctr;
+  Counter<DT, VEC, LEVELS> ctr[U];
   for (int j0 = 0; j0 < p; j0 += BATCH) {
-    uint32_t raw[BATCH][W];
-#pragma unroll
-    for (int b = 0; b < BATCH; ++b)
-      if (j0 + b < p) load_raw<DT, VEC>(a.send[rank_at(j0 + b, levels, reversed)], i, raw[b]);
+    uint32_t raw[BATCH][U][W];
 #pragma unroll
     for (int b = 0; b < BATCH; ++b) {
       if (j0 + b < p) {
-        Acc x[VEC];
+        const void* src = a.send[rank_at(j0 + b, levels, reversed)];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) x[e] = widen<DT>(raw[b], e);
-        if constexpr (MODE == 0) {
-          ctr.push(j0 + b, x);
-        } else {
+        for (int u = 0; u < U; ++u) {
+          const uint64_t v = v0 + static_cast<uint64_t>(u) * kThreads;
+          if (v < v_hi) load_raw<DT, VEC>(src, v * VEC, raw[b][u]);
+        }
+      }
+    }
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) acc[e] = (j0 + b == 0) ? x[e] : combine<CCL_SUM>(x[e], acc[e]);
+    for (int b = 0; b < BATCH; ++b) {
+      if (j0 + b < p) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          Acc x[VEC];
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) x[e] = widen<DT>(raw[b][u], e);
+          if constexpr (MODE == 0) {
+            ctr[u].push(j0 + b, x);
+          } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+              acc[u][e] = (j0 + b == 0) ? x[e] : combine<CCL_SUM>(x[e], acc[u][e]);
+          }
         }
       }
     }
   }
-  if constexpr (MODE == 0) ctr.flush(p, acc);
+  if constexpr (MODE == 0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) ctr[u].flush(p, acc[u]);
+  }
 }
 
-template <int DT, int VEC, int MODE>
+template <int DT, int VEC, int MODE, int LEVELS, int BATCH, int U>
 __global__ void __launch_bounds__(kThreads) schedule_kernel(const __grid_constant__ FoldArgs a,
                                                             uint64_t n, int levels, int reversed) {
   using Acc = typename Elem<DT>::Acc;
   pdl_enter();
   const int p = a.p;
   const uint64_t nv = n / VEC;
-  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
-  const uint64_t t0 = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  for (uint64_t v = t0; v < nv; v += stride) {
-    Acc acc[VEC];
-    fold_one<DT, VEC, MODE>(a, p, levels, reversed != 0, v * VEC, acc);
-    uint32_t w[(VEC * Elem<DT>::kBytes + 3) / 4];
-    pack_out<DT, VEC>(acc, w);
-    for (int r = 0; r < p; ++r) store_raw<DT, VEC>(a.recv[r], v * VEC, w);
+  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  for (uint64_t base = static_cast<uint64_t>(blockIdx.x) * kSpan; base < nv;
+       base += static_cast<uint64_t>(gridDim.x) * kSpan) {
+    Acc acc[U][VEC];
+    fold_vectors<DT, VEC, MODE, LEVELS, BATCH, U>(a, p, levels, reversed != 0, base + threadIdx.x,
+                                                   nv, acc);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+      if (v < nv) {
+        uint32_t w[(VEC * Elem<DT>::kBytes + 3) / 4];
+        pack_out<DT, VEC>(acc[u], w);
+        for (int r = 0; r < p; ++r) store_raw<DT, VEC>(a.recv[r], v * VEC, w);
+      }
+    }
   }
-  for (uint64_t i = nv * VEC + t0; i < n; i += stride) {  // tail (or everything when VEC == 1)
-    Acc acc[1];
-    fold_one<DT, 1, MODE>(a, p, levels, reversed != 0, i, acc);
-    uint32_t w[1];
-    pack_out<DT, 1>(acc, w);
-    for (int r = 0; r < p; ++r) store_raw<DT, 1>(a.recv[r], i, w);
+  if (VEC > 1 && blockIdx.x == 0) {  // tail elements
+    for (uint64_t i = nv * VEC + threadIdx.x; i < n; i += kThreads) {
+      Acc acc[1][1];
+      fold_vectors<DT, 1, MODE, LEVELS, BATCH, 1>(a, p, levels, reversed != 0, i, i + 1, acc);
+      uint32_t w[1];
+      pack_out<DT, 1>(acc[0], w);
+      for (int r = 0; r < p; ++r) store_raw<DT, 1>(a.recv[r], i, w);
+    }
   }
 }
 
-template <int DT, int VEC, int MODE>
+template <int DT, int VEC, int MODE, int LEVELS, int BATCH, int U>
 cudaError_t launch_one(const FoldArgs& a, uint64_t n, int levels, bool reversed, cudaStream_t s) {
-  const uint64_t work = (VEC > 1) ? n / VEC : n;
-  uint64_t gx = (work + 2 * kThreads - 1) / (2 * kThreads);
+  const uint64_t nv = (VEC > 1) ? n / VEC : n;
+  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  uint64_t gx = (nv + kSpan - 1) / kSpan;
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
   cudaLaunchConfig_t cfg = {};
@@ -142,15 +170,24 @@ cudaError_t launch_one(const FoldArgs& a, uint64_t n, int levels, bool reversed,
   attr[0].val.programmaticStreamSerializationAllowed = CCL_PDL ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, schedule_kernel<DT, VEC, MODE>, a, n, levels,
+  return cudaLaunchKernelEx(&cfg, schedule_kernel<DT, VEC, MODE, LEVELS, BATCH, U>, a, n, levels,
                             reversed ? 1 : 0);
 }
 
+// Shapes by p, as in the small-p ring kernel: few ranks -> several vectors per
+// thread so that about 256 bytes (fp32) / 128 bytes (bf16) of loads are in
+// flight; counter slots sized to the ranks.
 template <int DT, int MODE>
 cudaError_t launch_typed(bool vec, const FoldArgs& a, uint64_t n, int levels, bool reversed,
                          cudaStream_t s) {
-  if (vec) return launch_one<DT, 16 / Elem<DT>::kBytes, MODE>(a, n, levels, reversed, s);
-  return launch_one<DT, 1, MODE>(a, n, levels, reversed, s);
+  if (!vec) return launch_one<DT, 1, MODE, 8, 8, 1>(a, n, levels, reversed, s);
+  constexpr int VEC = 16 / Elem<DT>::kBytes;
+  constexpr int H = (VEC > 4) ? 2 : 1;  // bf16: 8 accumulators per vector
+  if (a.p <= 2) return launch_one<DT, VEC, MODE, 2, 2, 8 / H>(a, n, levels, reversed, s);
+  if (a.p <= 4) return launch_one<DT, VEC, MODE, 3, 4, 4 / H>(a, n, levels, reversed, s);
+  if (a.p <= 8) return launch_one<DT, VEC, MODE, 4, 8, 2 / H>(a, n, levels, reversed, s);
+  if (a.p <= 16) return launch_one<DT, VEC, MODE, 5, 8, 1>(a, n, levels, reversed, s);
+  return launch_one<DT, VEC, MODE, 8, 8, 1>(a, n, levels, reversed, s);
 }
 
 }  // namespace

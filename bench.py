@@ -566,6 +566,45 @@ class Ddp(Workload):
         return dt, self.p * m * 6, f"oracle bucket all-reduce on the first {m} elements of bucket 0"
 
 
+class Rooted(Workload):
+    """broadcast / reduce / scatter / gather of p ranks x `mib` MiB, root 0."""
+    def __init__(self, kind, p=16, mib=64, dtype="f32"):
+        self.kind, self.p, self.mib, self.dtype = kind, p, mib, dtype
+        self.e = 4 if dtype == "f32" else 2
+        self.n = mib * (1 << 20) // self.e
+        self.name = kind
+        self.kernel = {"broadcast": "gather", "reduce": "fold", "scatter": "ring_step",
+                       "gather": "ring_step"}[kind]
+        self.kernel_key = f"{kind}_{dtype}_p{p}_n{self.n}"
+
+    def config(self):
+        return {"workload": f"{self.kind}: p={self.p} ranks, {self.mib} MiB {self.dtype} per rank, root 0",
+                "p": self.p, "n_per_rank": self.n, "inputs": "U(-1,1) drawn on the device (seed 4)"}
+
+    def bytes_per_step(self):
+        n, p, e = self.n, self.p, self.e
+        return {"broadcast": n + p * n, "reduce": p * n + n, "scatter": 2 * n, "gather": 2 * n}[self.kind] * e
+
+    def setup(self, lib, torch, device):
+        self.lib = lib
+        gen = torch.Generator(device=device)
+        gen.manual_seed(4)
+        tdt = torch.float32 if self.dtype == "f32" else torch.bfloat16
+        mk = lambda m: (torch.rand(m, generator=gen, device=device) * 2 - 1).to(tdt)
+        sizes = [lib.ccl_chunk_bounds(self.p, self.n, k)[1] for k in range(self.p)]
+        if self.kind == "broadcast":
+            self.a, self.b = mk(self.n), [torch.empty(self.n, dtype=tdt, device=device) for _ in range(self.p)]
+        elif self.kind == "reduce":
+            self.a, self.b = [mk(self.n) for _ in range(self.p)], torch.empty(self.n, dtype=tdt, device=device)
+        elif self.kind == "scatter":
+            self.a, self.b = mk(self.n), [torch.empty(m, dtype=tdt, device=device) for m in sizes]
+        else:
+            self.a, self.b = [mk(m) for m in sizes], torch.empty(self.n, dtype=tdt, device=device)
+
+    def step(self, stream):
+        getattr(self.lib, f"ccl_{self.kind}")(self.a, self.b, stream=stream)
+
+
 def make_workload(a) -> Workload:
     if a.workload == "bucket":
         return Bucket()
@@ -583,6 +622,8 @@ def make_workload(a) -> Workload:
         return Moe()
     if a.workload == "ddp":
         return Ddp()
+    if a.workload in ("broadcast", "reduce", "scatter", "gather"):
+        return Rooted(a.workload, p=a.p or 16, mib=a.mib or 64, dtype=a.dtype)
     raise SystemExit(f"unknown workload {a.workload}")
 
 
@@ -873,7 +914,7 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bucket",
                     choices=["bucket", "allreduce", "reduce_scatter", "all_gather", "zero", "moe",
-                             "literal", "ddp"])
+                             "literal", "ddp", "broadcast", "reduce", "scatter", "gather"])
     ap.add_argument("--p", type=int, default=0)
     ap.add_argument("--mib", type=int, default=0)
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
