@@ -58,6 +58,10 @@ def _load() -> ctypes.CDLL:
         "ccl_bucket_allreduce_scale_cast": (st, [pp, pp, i32, sz, ctypes.c_float, vp]),
         "ccl_all_to_allv": (st, [pp, ctypes.POINTER(sz), pp, i32, sz, i32, vp]),
         "ccl_ring_literal_workspace_bytes": (sz, [i32, i32, sz, i32]),
+        "ccl_moe_route": (st, [pp, i32, sz, i32, i32, vp, pp, vp]),
+        "ccl_moe_dispatch": (st, [pp, pp, vp, pp, i32, sz, i32, i32, sz, i32, pp, ctypes.POINTER(sz),
+                                  pp, pp, vp]),
+        "ccl_moe_combine": (st, [pp, ctypes.POINTER(sz), pp, pp, vp, pp, i32, sz, i32, i32, sz, pp, vp]),
         "ccl_plan_buckets": (st, [ctypes.POINTER(sz), sz, sz, sz, ctypes.POINTER(ctypes.c_uint32),
                                   ctypes.POINTER(sz), ctypes.POINTER(sz), ctypes.POINTER(sz)]),
         "ccl_ring_allreduce_literal": (st, [pp, pp, i32, sz, i32, i32, ctypes.POINTER(u64), vp, sz, vp]),
@@ -415,3 +419,59 @@ def ccl_ring_reduce_scatter_literal_noalloc(send, recv, op: str = "sum", stream=
               p, n, _dtype_code(send[0]), _op_code(op), sent, _stream(stream, send[0].device)),
            "ccl_ring_reduce_scatter_literal_noalloc")
     return list(sent)
+
+
+# ------------------------------------------------------------ MoE routing
+def _ptrs_or_null(ts):
+    return None if ts is None else _ptr_array([t.data_ptr() for t in ts])
+
+
+def ccl_moe_route(expert_ids, num_experts: int, counts, slots, stream=None) -> None:
+    """expert_ids[s]: (tokens, k) int32 CUDA tensors -> counts (p*p int64) and
+    slots[s] ((tokens, k) int32; -1 where the id is out of range)."""
+    ids = _tensors(expert_ids, "expert_ids")
+    p = len(ids)
+    tokens, k = (ids[0].shape[0], ids[0].shape[1]) if ids[0].dim() == 2 else (ids[0].numel(), 1)
+    if ids[0].dtype != torch.int32 or counts.dtype != torch.int64 or counts.numel() != p * p:
+        raise ValueError("expert_ids must be int32 and counts p*p int64")
+    slots = _tensors(slots, "slots")
+    _numel_check(ids, [tokens * k] * p, "expert_ids")
+    _numel_check(slots, [tokens * k] * p, "slots")
+    _check(LIB.ccl_moe_route(_ptr_array([t.data_ptr() for t in ids]), p, tokens, k, num_experts,
+                             counts.data_ptr(), _ptr_array([t.data_ptr() for t in slots]),
+                             _stream(stream, ids[0].device)), "ccl_moe_route")
+
+
+def ccl_moe_dispatch(x, expert_ids, counts, slots, num_experts: int, recv, recv_scales=None,
+                     recv_expert=None, fp8: bool = False, stream=None) -> None:
+    """Scatter each token row to the ranks of its k experts (bf16, or FP8 with
+    per-128 block scales when fp8=True).  recv[d] sized from counts."""
+    x, ids, slots, recv = (_tensors(x, "x"), _tensors(expert_ids, "expert_ids"),
+                           _tensors(slots, "slots"), list(recv))
+    p = len(x)
+    tokens, hidden = x[0].shape
+    k = ids[0].numel() // tokens
+    rows = (ctypes.c_size_t * p)(*[int(t.shape[0]) if t.numel() else 0 for t in recv])
+    _check(LIB.ccl_moe_dispatch(_ptr_array([t.data_ptr() for t in x]),
+                                _ptr_array([t.data_ptr() for t in ids]), counts.data_ptr(),
+                                _ptr_array([t.data_ptr() for t in slots]), p, tokens, k, num_experts,
+                                hidden, 1 if fp8 else 0, _ptr_array([t.data_ptr() for t in recv]), rows,
+                                _ptrs_or_null(recv_scales), _ptrs_or_null(recv_expert),
+                                _stream(stream, x[0].device)), "ccl_moe_dispatch")
+
+
+def ccl_moe_combine(y, expert_ids, weights, counts, slots, num_experts: int, out, stream=None) -> None:
+    """out[s][t] = bf16(sum_j weights[s][t, j] * y[row of (s, t, j)])."""
+    ids, w, slots, out = (_tensors(expert_ids, "expert_ids"), _tensors(weights, "weights"),
+                          _tensors(slots, "slots"), _tensors(out, "out"))
+    y = list(y)
+    p = len(out)
+    tokens, hidden = out[0].shape
+    k = ids[0].numel() // tokens
+    rows = (ctypes.c_size_t * p)(*[int(t.shape[0]) if t.numel() else 0 for t in y])
+    _check(LIB.ccl_moe_combine(_ptr_array([t.data_ptr() for t in y]), rows,
+                               _ptr_array([t.data_ptr() for t in ids]),
+                               _ptr_array([t.data_ptr() for t in w]), counts.data_ptr(),
+                               _ptr_array([t.data_ptr() for t in slots]), p, tokens, k, num_experts,
+                               hidden, _ptr_array([t.data_ptr() for t in out]),
+                               _stream(stream, out[0].device)), "ccl_moe_combine")

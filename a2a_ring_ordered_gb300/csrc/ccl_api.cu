@@ -526,6 +526,149 @@ extern "C" ccl_status_t ccl_gather(const void* const* send, void* recv, int p, s
   return copy_transfers(dt, src, dst, len, p, stream);
 }
 
+// ==================================================== MoE route / dispatch / combine
+namespace {
+
+ccl_status_t check_moe(int p, size_t tokens, int k, int num_experts, size_t hidden) {
+  if (p < 1 || p > kMoeMaxRanks) return fail(CCL_ERR_INVALID_ARG, "p=%d outside 1..%d", p, kMoeMaxRanks);
+  if (k < 1 || k > kMoeMaxK) return fail(CCL_ERR_INVALID_ARG, "k=%d outside 1..%d", k, kMoeMaxK);
+  if (num_experts < p || num_experts % p != 0)
+    return fail(CCL_ERR_INVALID_ARG, "num_experts=%d must be a positive multiple of p=%d", num_experts, p);
+  if (tokens * static_cast<uint64_t>(k) > 0x7FFFFFFFull || tokens > (1ull << 40))
+    return fail(CCL_ERR_INVALID_ARG, "tokens * k must stay below 2^31");
+  if (hidden == 0 || hidden % 128 != 0 || hidden > (1ull << 30))
+    return fail(CCL_ERR_INVALID_ARG, "hidden=%zu must be a positive multiple of 128", hidden);
+  return CCL_OK;
+}
+
+ccl_status_t check_ptrs(const char* name, const void* const* a, int p, size_t align, bool need) {
+  if (!need) return CCL_OK;
+  if (a == nullptr) return fail(CCL_ERR_INVALID_ARG, "%s array is NULL", name);
+  for (int r = 0; r < p; ++r) {
+    if (a[r] == nullptr) return fail(CCL_ERR_INVALID_ARG, "%s[%d] is NULL", name, r);
+    if (reinterpret_cast<uintptr_t>(a[r]) % align)
+      return fail(CCL_ERR_INVALID_ARG, "%s[%d] is not %zu-byte aligned", name, r, align);
+  }
+  return CCL_OK;
+}
+
+}  // namespace
+
+extern "C" ccl_status_t ccl_moe_route(const int32_t* const* expert_ids, int p, size_t tokens, int k,
+                                      int num_experts, int64_t* counts, int32_t* const* slots,
+                                      void* stream) {
+  clear_error();
+  ccl_status_t st = check_moe(p, tokens, k, num_experts, 128);
+  if (st != CCL_OK) return st;
+  if (counts == nullptr || (reinterpret_cast<uintptr_t>(counts) & 7))
+    return fail(CCL_ERR_INVALID_ARG, "counts is NULL or not 8-byte aligned");
+  const bool any = tokens > 0;
+  if ((st = check_ptrs("expert_ids", reinterpret_cast<const void* const*>(expert_ids), p, 4, any)) != CCL_OK ||
+      (st = check_ptrs("slots", reinterpret_cast<const void* const*>(slots), p, 4, any)) != CCL_OK)
+    return st;
+  MoeRouteArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.ids[r] = any ? expert_ids[r] : nullptr;
+    a.slots[r] = any ? slots[r] : nullptr;
+  }
+  a.counts = counts;
+  a.items = tokens * static_cast<uint64_t>(k);
+  a.p = p;
+  a.epr = num_experts / p;
+  a.num_experts = num_experts;
+  cudaError_t err = launch_moe_route(a, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "MoE route kernel launch");
+  return CCL_OK;
+}
+
+extern "C" ccl_status_t ccl_moe_dispatch(const void* const* x, const int32_t* const* expert_ids,
+                                         const int64_t* counts, const int32_t* const* slots, int p,
+                                         size_t tokens, int k, int num_experts, size_t hidden,
+                                         int fp8, void* const* recv, const size_t* recv_rows,
+                                         float* const* recv_scales, int32_t* const* recv_expert,
+                                         void* stream) {
+  clear_error();
+  ccl_status_t st = check_moe(p, tokens, k, num_experts, hidden);
+  if (st != CCL_OK) return st;
+  if (counts == nullptr || recv_rows == nullptr) return fail(CCL_ERR_INVALID_ARG, "counts or recv_rows is NULL");
+  if (tokens == 0) return CCL_OK;
+  if ((st = check_ptrs("x", x, p, 16, true)) != CCL_OK ||
+      (st = check_ptrs("expert_ids", reinterpret_cast<const void* const*>(expert_ids), p, 4, true)) != CCL_OK ||
+      (st = check_ptrs("slots", reinterpret_cast<const void* const*>(slots), p, 4, true)) != CCL_OK)
+    return st;
+  MoeDispatchArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.cap[r] = recv_rows[r];
+    if (recv_rows[r] != 0) {
+      if (recv == nullptr || recv[r] == nullptr || (reinterpret_cast<uintptr_t>(recv[r]) & 15))
+        return fail(CCL_ERR_INVALID_ARG, "recv[%d] is NULL or not 16-byte aligned", r);
+      if (fp8 && (recv_scales == nullptr || recv_scales[r] == nullptr ||
+                  (reinterpret_cast<uintptr_t>(recv_scales[r]) & 3)))
+        return fail(CCL_ERR_INVALID_ARG, "recv_scales[%d] is NULL or misaligned", r);
+      a.recv[r] = recv[r];
+      a.scales[r] = fp8 ? recv_scales[r] : nullptr;
+      a.rexp[r] = recv_expert != nullptr ? recv_expert[r] : nullptr;
+    }
+    a.x[r] = x[r];
+    a.ids[r] = expert_ids[r];
+    a.slots[r] = slots[r];
+  }
+  a.counts = counts;
+  a.tokens = tokens;
+  a.hidden = hidden;
+  a.p = p;
+  a.k = k;
+  a.epr = num_experts / p;
+  a.num_experts = num_experts;
+  a.rexp_given = recv_expert != nullptr ? 1 : 0;
+  cudaError_t err = launch_moe_dispatch(a, fp8 != 0, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "MoE dispatch kernel launch");
+  return CCL_OK;
+}
+
+extern "C" ccl_status_t ccl_moe_combine(const void* const* y, const size_t* y_rows,
+                                        const int32_t* const* expert_ids, const float* const* weights,
+                                        const int64_t* counts, const int32_t* const* slots, int p,
+                                        size_t tokens, int k, int num_experts, size_t hidden,
+                                        void* const* out, void* stream) {
+  clear_error();
+  ccl_status_t st = check_moe(p, tokens, k, num_experts, hidden);
+  if (st != CCL_OK) return st;
+  if (counts == nullptr || y_rows == nullptr) return fail(CCL_ERR_INVALID_ARG, "counts or y_rows is NULL");
+  if (tokens == 0) return CCL_OK;
+  if ((st = check_ptrs("expert_ids", reinterpret_cast<const void* const*>(expert_ids), p, 4, true)) != CCL_OK ||
+      (st = check_ptrs("weights", reinterpret_cast<const void* const*>(weights), p, 4, true)) != CCL_OK ||
+      (st = check_ptrs("slots", reinterpret_cast<const void* const*>(slots), p, 4, true)) != CCL_OK ||
+      (st = check_ptrs("out", const_cast<const void* const*>(out), p, 16, true)) != CCL_OK)
+    return st;
+  MoeCombineArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.cap[r] = y_rows[r];
+    if (y_rows[r] != 0) {
+      if (y == nullptr || y[r] == nullptr || (reinterpret_cast<uintptr_t>(y[r]) & 15))
+        return fail(CCL_ERR_INVALID_ARG, "y[%d] is NULL or not 16-byte aligned", r);
+      a.y[r] = y[r];
+    }
+    a.ids[r] = expert_ids[r];
+    a.slots[r] = slots[r];
+    a.weights[r] = weights[r];
+    a.out[r] = out[r];
+  }
+  a.counts = counts;
+  a.tokens = tokens;
+  a.hidden = hidden;
+  a.p = p;
+  a.k = k;
+  a.epr = num_experts / p;
+  a.num_experts = num_experts;
+  cudaError_t err = launch_moe_combine(a, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "MoE combine kernel launch");
+  return CCL_OK;
+}
+
 // ============================================================== all-to-allv
 extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts,
                                         void* const* recv, int p, size_t row_elems,

@@ -91,6 +91,45 @@ cudaError_t launch_xfer(int kind, int dt, int op, const XferArgs& a, cudaStream_
 void clear_last_error();
 ccl_status_t report_error(ccl_status_t st, const char* fmt, ...);
 
+// ------------------------------------------------------------------- MoE
+constexpr int kMoeMaxRanks = 64;  // keeps every MoE parameter block under 4 KB
+constexpr int kMoeMaxK = 16;
+struct MoeRouteArgs {
+  const int32_t* ids[kMoeMaxRanks];  // tokens * k expert ids per source
+  int32_t* slots[kMoeMaxRanks];      // out: slot of each (token, choice), -1 if unrouted
+  int64_t* counts;                   // out: p x p rows source -> destination (device)
+  uint64_t items;                    // tokens * k
+  int p, epr, num_experts;
+};
+struct MoeDispatchArgs {
+  const void* x[kMoeMaxRanks];        // tokens x hidden bf16 per source
+  const int32_t* ids[kMoeMaxRanks];
+  const int32_t* slots[kMoeMaxRanks];
+  void* recv[kMoeMaxRanks];           // rows x hidden, bf16 or e4m3
+  float* scales[kMoeMaxRanks];        // FP8: rows x hidden/128 block scales
+  int32_t* rexp[kMoeMaxRanks];        // optional: expert id of each received row
+  const int64_t* counts;              // device p x p
+  uint64_t cap[kMoeMaxRanks];         // rows each recv[d] holds
+  uint64_t tokens, hidden;
+  int p, k, epr, num_experts, rexp_given;
+};
+struct MoeCombineArgs {
+  const void* y[kMoeMaxRanks];        // rows x hidden bf16, dispatch layout
+  const int32_t* ids[kMoeMaxRanks];
+  const int32_t* slots[kMoeMaxRanks];
+  const float* weights[kMoeMaxRanks]; // tokens * k gate weights per source
+  void* out[kMoeMaxRanks];            // tokens x hidden bf16 per source
+  const int64_t* counts;
+  uint64_t cap[kMoeMaxRanks];         // rows each y[d] holds
+  uint64_t tokens, hidden;
+  int p, k, epr, num_experts;
+};
+static_assert(sizeof(MoeDispatchArgs) <= 4096, "MoE dispatch parameters exceed 4 KB");
+static_assert(sizeof(MoeCombineArgs) <= 4096, "MoE combine parameters exceed 4 KB");
+cudaError_t launch_moe_route(const MoeRouteArgs& a, cudaStream_t s);
+cudaError_t launch_moe_dispatch(const MoeDispatchArgs& a, bool fp8, cudaStream_t s);
+cudaError_t launch_moe_combine(const MoeCombineArgs& a, cudaStream_t s);
+
 // Records one successful kernel launch (ccl_kernel_launch_count).
 void note_launch();
 

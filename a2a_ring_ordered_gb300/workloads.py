@@ -122,3 +122,26 @@ def moe_tokens(counts: np.ndarray, hidden: int, rng: np.random.Generator,
         x = rng.standard_normal(rows * hidden, dtype=np.float32)
         out.append(_finish(x, dtype))
     return out
+
+
+def moe_topk_routing(p: int, tokens: int, k: int, num_experts: int, s: float = 1.2,
+                     seed: int = 3) -> list[np.ndarray]:
+    """Per source: (tokens, k) int32 distinct expert ids, drawn without
+    replacement with Zipf(s) popularity over the experts (Gumbel top-k)."""
+    rng = np.random.default_rng(seed)
+    logw = np.log((np.arange(num_experts, dtype=np.float64) + 1.0) ** (-s))
+    out = []
+    for _ in range(p):
+        g = rng.gumbel(size=(tokens, num_experts)) + logw
+        out.append(np.argsort(-g, axis=1)[:, :k].astype(np.int32))
+    return out
+
+
+def moe_gate_weights(p: int, tokens: int, k: int, seed: int = 4) -> list[np.ndarray]:
+    """Per source: (tokens, k) positive float32 gate weights summing to ~1 per token."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(p):
+        w = rng.random((tokens, k)) + 0.05
+        out.append((w / w.sum(axis=1, keepdims=True)).astype(np.float32))
+    return out

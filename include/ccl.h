@@ -216,6 +216,44 @@ ccl_status_t ccl_plan_buckets(const size_t* numel, size_t count, size_t elem_byt
                               size_t cap_bytes, uint32_t* bucket_of, size_t* offset,
                               size_t* bucket_numel, size_t* num_buckets);
 
+/* ------------------------------------------------- MoE expert parallelism
+ * "Networks and Collective Communication" section 7.4: every MoE layer does an
+ * all-to-all dispatch (each token to the ranks holding the k experts it chose)
+ * and an all-to-all combine; DeepSeek-V3 dispatches in FP8 and combines in
+ * BF16.  p <= 64 virtual ranks, 1 <= k <= 16, expert e on rank e / (E/p),
+ * hidden a multiple of 128, tokens * k < 2^31.  Token t of source s sends one
+ * row per choice j; destination d holds its rows grouped by source, then
+ * token, then choice, at row sum_{s' < s} counts[s'][d] + slot.
+ *
+ * ccl_moe_route: expert_ids[s] (device, tokens*k int32, token-major) ->
+ *   counts (device p*p int64, rows source -> destination) and slots[s]
+ *   (device, tokens*k int32; -1 for an id outside [0, E)).  One launch.
+ * ccl_moe_dispatch: x[s] (device, tokens x hidden bf16) -> recv[d] (rows x
+ *   hidden bf16, or e4m3 bytes when fp8 != 0, with recv_scales[d] = rows x
+ *   hidden/128 fp32: scale = amax/448 per 128-element block, code =
+ *   e4m3(x/scale) round-to-nearest-even, saturating).  recv_rows (host, p) is
+ *   the row capacity of each recv[d]; rows beyond it are not written (read
+ *   counts back to size the buffers).  recv_expert (may be NULL) receives each
+ *   row's expert id.
+ * ccl_moe_combine: y[d] (rows x hidden bf16 in dispatch layout, y_rows rows)
+ *   -> out[s] (tokens x hidden bf16) = bf16(sum_j weights[s][t*k+j] * y_j),
+ *   fp32 products and sums in choice order.  With weights 1/k (k a power of
+ *   two) combine(dispatch(x)) == x. */
+ccl_status_t ccl_moe_route(const int32_t* const* expert_ids, int p, size_t tokens, int k,
+                           int num_experts, int64_t* counts, int32_t* const* slots, void* stream);
+
+ccl_status_t ccl_moe_dispatch(const void* const* x, const int32_t* const* expert_ids,
+                              const int64_t* counts, const int32_t* const* slots, int p,
+                              size_t tokens, int k, int num_experts, size_t hidden, int fp8,
+                              void* const* recv, const size_t* recv_rows, float* const* recv_scales,
+                              int32_t* const* recv_expert, void* stream);
+
+ccl_status_t ccl_moe_combine(const void* const* y, const size_t* y_rows,
+                             const int32_t* const* expert_ids, const float* const* weights,
+                             const int64_t* counts, const int32_t* const* slots, int p,
+                             size_t tokens, int k, int num_experts, size_t hidden, void* const* out,
+                             void* stream);
+
 /* ------------------------------------------------------- literal ring engine
  * Executes the ring schedule as written: the reduce-scatter phase's p-1 steps
  * (rank r sends its partial of chunk (r-s-1) mod p to rank r+1, which adds its
