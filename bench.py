@@ -141,7 +141,10 @@ KERNEL_SOURCES = {
     "a2av": ["a2a_ring_ordered_gb300/csrc/a2av.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "ring_step": ["a2a_ring_ordered_gb300/csrc/ring_step.cu",
                   "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
+    "moe": ["a2a_ring_ordered_gb300/csrc/moe.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
 }
+for _part in ("moe_route", "moe_dispatch", "moe_combine"):
+    KERNEL_SOURCES[_part] = KERNEL_SOURCES["moe"]
 
 
 def host_prefix(tensors, m: int) -> list[np.ndarray]:
@@ -605,6 +608,78 @@ class Rooted(Workload):
         getattr(self.lib, f"ccl_{self.kind}")(self.a, self.b, stream=stream)
 
 
+class MoeEp(Workload):
+    """MoE expert parallelism with routing: p=8 ranks x 4096 tokens, hidden 7168,
+    top-8 of 256 experts (Zipf(1.2) popularity).  One step = route + FP8 (or
+    bf16) dispatch + weighted bf16 combine."""
+    name = "moe_ep_route_dispatch_combine"
+    kernel = "moe"
+    launches_per_step = 3
+
+    def __init__(self, p=8, tokens=4096, k=8, experts=256, hidden=7168, fp8=True):
+        self.p, self.T, self.k, self.E, self.h, self.fp8 = p, tokens, k, experts, hidden, fp8
+        self.kernel_key = f"moe_ep_p{p}_t{tokens}_k{k}_e{experts}_h{hidden}_{'fp8' if fp8 else 'bf16'}"
+
+    def config(self):
+        return {"workload": f"MoE EP: p={self.p} ranks x {self.T} tokens, hidden {self.h}, top-{self.k} of "
+                            f"{self.E} experts, {'FP8' if self.fp8 else 'bf16'} dispatch, bf16 combine",
+                "p": self.p, "tokens_per_rank": self.T, "k": self.k, "experts": self.E, "hidden": self.h,
+                "inputs": "tokens N(0,1) drawn on the device; routing Gumbel top-k, Zipf(1.2), seed 3"}
+
+    def setup(self, lib, torch, device):
+        from a2a_ring_ordered_gb300 import workloads
+        self.lib, self.torch = lib, torch
+        p, T, k, E, h = self.p, self.T, self.k, self.E, self.h
+        gen = torch.Generator(device=device)
+        gen.manual_seed(3)
+        self.x = [torch.randn(T, h, generator=gen, device=device).to(torch.bfloat16) for _ in range(p)]
+        self.ids = [torch.from_numpy(i).to(device) for i in workloads.moe_topk_routing(p, T, k, E, seed=3)]
+        self.w = [torch.from_numpy(w).to(device) for w in workloads.moe_gate_weights(p, T, k, seed=4)]
+        self.counts = torch.empty(p * p, dtype=torch.int64, device=device)
+        self.slots = [torch.empty(T, k, dtype=torch.int32, device=device) for _ in range(p)]
+        lib.ccl_moe_route(self.ids, E, self.counts, self.slots)
+        rows = self.counts.cpu().numpy().reshape(p, p).sum(axis=0)
+        self.rows = [int(r) for r in rows]
+        dt = torch.uint8 if self.fp8 else torch.bfloat16
+        self.recv = [torch.empty(r, h, dtype=dt, device=device) for r in self.rows]
+        self.scales = [torch.empty(r, h // 128, device=device) for r in self.rows] if self.fp8 else None
+        # expert outputs (bf16, dispatch layout) for the combine
+        self.y = [torch.randn(r, h, generator=gen, device=device).to(torch.bfloat16) for r in self.rows]
+        self.out = [torch.empty(T, h, dtype=torch.bfloat16, device=device) for _ in range(p)]
+
+    def _bytes(self):
+        p, T, k, h = self.p, self.T, self.k, self.h
+        rows = p * T * k
+        route = 2 * rows * 4
+        disp = p * T * h * 2 + rows * (h + h // 32 if self.fp8 else 2 * h)
+        comb = rows * h * 2 + p * T * h * 2 + rows * 4
+        return route, disp, comb
+
+    def bytes_per_step(self):
+        return sum(self._bytes())
+
+    def _route(self, s):
+        self.lib.ccl_moe_route(self.ids, self.E, self.counts, self.slots, stream=s)
+
+    def _dispatch(self, s):
+        self.lib.ccl_moe_dispatch(self.x, self.ids, self.counts, self.slots, self.E, self.recv,
+                                  self.scales, None, fp8=self.fp8, stream=s)
+
+    def _combine(self, s):
+        self.lib.ccl_moe_combine(self.y, self.ids, self.w, self.counts, self.slots, self.E, self.out,
+                                 stream=s)
+
+    def step(self, stream):
+        self._route(stream)
+        self._dispatch(stream)
+        self._combine(stream)
+
+    def parts(self):
+        r, d, c = self._bytes()
+        return [("moe_route", r, self._route), ("moe_dispatch", d, self._dispatch),
+                ("moe_combine", c, self._combine)]
+
+
 def make_workload(a) -> Workload:
     if a.workload == "bucket":
         return Bucket()
@@ -622,6 +697,8 @@ def make_workload(a) -> Workload:
         return Moe()
     if a.workload == "ddp":
         return Ddp()
+    if a.workload == "moe_ep":
+        return MoeEp(fp8=a.dtype != "bf16")
     if a.workload in ("broadcast", "reduce", "scatter", "gather"):
         return Rooted(a.workload, p=a.p or 16, mib=a.mib or 64, dtype=a.dtype)
     raise SystemExit(f"unknown workload {a.workload}")
@@ -914,7 +991,7 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bucket",
                     choices=["bucket", "allreduce", "reduce_scatter", "all_gather", "zero", "moe",
-                             "literal", "ddp", "broadcast", "reduce", "scatter", "gather"])
+                             "literal", "ddp", "broadcast", "reduce", "scatter", "gather", "moe_ep"])
     ap.add_argument("--p", type=int, default=0)
     ap.add_argument("--mib", type=int, default=0)
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
