@@ -49,10 +49,14 @@ __device__ __forceinline__ void xfer_elems(const char* src, char* dst, uint64_t 
   }
 }
 
-template <int KIND, int DT, int OP>
+// U vectors per thread (t, t + kThreads, ...): all their loads are issued
+// before any store, so a thread keeps several 16-byte loads in flight.
+template <int KIND, int DT, int OP, int U>
 __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ XferArgs a) {
   using T = XferTypes<KIND, DT>;
   constexpr int VEC = T::kVec;
+  constexpr int WS = (VEC * Elem<T::kSrc>::kBytes + 3) / 4;
+  constexpr int WD = (VEC * Elem<T::kDst>::kBytes + 3) / 4;
   pdl_enter();
   const int r = blockIdx.y;
   const char* src = a.src[r];
@@ -60,22 +64,56 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ 
   const uint64_t len = a.len[r];
   const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0;
   const uint64_t nv = vec ? len / VEC : 0;
+  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  for (uint64_t base = static_cast<uint64_t>(blockIdx.x) * kSpan; base < nv;
+       base += static_cast<uint64_t>(gridDim.x) * kSpan) {
+    uint32_t ws[U][WS];
+    uint32_t wd[U][WD];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+      if (v < nv) {
+        load_raw<T::kSrc, VEC>(src, v * VEC, ws[u]);
+        if constexpr (KIND == kXferCombine) load_raw<T::kDst, VEC>(dst, v * VEC, wd[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+      if (v >= nv) continue;
+      if constexpr (KIND == kXferCopy) {
+        store_raw<T::kDst, VEC>(dst, v * VEC, ws[u]);
+      } else {
+        using Acc = typename Elem<T::kSrc>::Acc;
+        Acc acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = widen<T::kSrc>(ws[u], e);
+        if constexpr (KIND == kXferCombine) {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[e] = combine<OP>(acc[e], widen<T::kDst>(wd[u], e));
+        }
+        uint32_t wo[WD];
+        pack_out<T::kDst, VEC>(acc, wo);
+        store_raw<T::kDst, VEC>(dst, v * VEC, wo);
+      }
+    }
+  }
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   const uint64_t t0 = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  for (uint64_t v = t0; v < nv; v += stride) xfer_elems<KIND, DT, OP, VEC>(src, dst, v * VEC);
   for (uint64_t i = nv * VEC + t0; i < len; i += stride) xfer_elems<KIND, DT, OP, 1>(src, dst, i);
 }
 
 template <int KIND, int DT, int OP>
 cudaError_t launch_one(const XferArgs& a, cudaStream_t s) {
   constexpr int VEC = XferTypes<KIND, DT>::kVec;
+  constexpr int U = 4;
   uint64_t longest = 0;
   for (int r = 0; r < a.p; ++r) longest = a.len[r] > longest ? a.len[r] : longest;
   if (longest == 0) return cudaSuccess;
-  uint64_t gx = (longest / VEC + 2 * kThreads - 1) / (2 * kThreads);
+  uint64_t gx = (longest / VEC + kThreads * U - 1) / (kThreads * U);
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
-  cudaError_t err = launch_kernel(xfer_kernel<KIND, DT, OP>, dim3(static_cast<unsigned>(gx), a.p),
+  cudaError_t err = launch_kernel(xfer_kernel<KIND, DT, OP, U>, dim3(static_cast<unsigned>(gx), a.p),
                                   dim3(kThreads), s, a);
   if (err == cudaSuccess) note_launch();
   return err;

@@ -196,6 +196,9 @@ cudaError_t launch_schedule_fold(int dt, bool linear, bool reversed, bool vec, c
                                  uint64_t n, cudaStream_t s) {
   int levels = 0;
   while ((1 << levels) < a.p) ++levels;
+  // with p <= 3 the pairwise tree is ((x0 + x1) + x2), the rank-order fold
+  // (Rabenseifner needs p a power of two, and for p = 2 x0 + x1 = x1 + x0)
+  if (a.p <= 3) linear = true;
   cudaError_t err = cudaErrorInvalidValue;
   if (linear) {
     if (dt == kF32) err = launch_typed<kF32, 1>(vec, a, n, levels, false, s);
