@@ -107,9 +107,11 @@ def _tensors(ts: Sequence[torch.Tensor], name: str) -> list[torch.Tensor]:
         raise ValueError(f"{name}: need 1..{CCL_MAX_RANKS} rank buffers, got {len(ts)}")
     dev = ts[0].device
     for i, t in enumerate(ts):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda:
-            raise ValueError(f"{name}[{i}] must be a CUDA tensor")
-        if t.device != dev:
+        # CUDA tensors, or pinned host tensors: the GPU reads and writes pinned
+        # host memory directly (over NVLink-C2C on GB300)
+        if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name}[{i}] must be a CUDA tensor or a pinned host tensor")
+        if t.is_cuda and dev.type == "cuda" and t.device != dev:
             raise ValueError(f"{name}[{i}] is on {t.device}, expected {dev}")
         if not t.is_contiguous():
             raise ValueError(f"{name}[{i}] must be contiguous")
@@ -134,7 +136,7 @@ def _op_code(op: str) -> int:
 
 def _stream(stream, device) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream(device)
+        stream = torch.cuda.current_stream(device if device.type == "cuda" else None)
     return int(stream.cuda_stream)
 
 

@@ -542,3 +542,17 @@ def test_rooted_in_place_forms(lib):
     want = collectives.reduce_ring(x, root)[root]
     lib.ccl_reduce(send, send[root], root=root)
     assert_equal(to_host(send[root]), want, "f32", "in-place reduce")
+
+
+def test_bucket_reads_and_writes_pinned_host_memory(lib):
+    """Inputs and outputs in pinned host memory: the kernel moves the data over
+    the host link itself; the bits equal the oracle's."""
+    p, n = 8, 1_000_003
+    g = workloads.normal(p, n, 1e-3, seed=21)
+    want = ring.bucket_allreduce_scale_cast(g, 0.125)
+    h_in = [torch.from_numpy(v).pin_memory() for v in g]
+    h_out = [torch.empty(n, dtype=torch.bfloat16).pin_memory() for _ in range(p)]
+    lib.ccl_bucket_allreduce_scale_cast(h_in, h_out, scale=0.125)
+    torch.cuda.synchronize()
+    for r in range(p):
+        np.testing.assert_array_equal(h_out[r].view(torch.int16).numpy().view(np.uint16), want[r])
