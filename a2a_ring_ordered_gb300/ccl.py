@@ -140,8 +140,10 @@ def _stream(stream, device) -> int:
     return int(stream.cuda_stream)
 
 
-def _chunk(p: int, n: int, c: int) -> tuple[int, int]:
-    return ccl_chunk_bounds(p, n, c)
+def _chunk_lengths(p: int, n: int) -> list[int]:
+    """Expected per-rank shard sizes (the library's chunk rule), for size checks."""
+    q, r = divmod(n, p)
+    return [q + (1 if k < r else 0) for k in range(p)]
 
 
 def _numel_check(ts, want, name):
@@ -231,7 +233,7 @@ def ccl_reduce_scatter(send, recv, op: str = "sum", stream=None) -> None:
     if len(recv) != p or recv[0].dtype != send[0].dtype:
         raise ValueError("recv must hold p buffers of the send dtype")
     _numel_check(send, [n] * p, "send")
-    _numel_check(recv, [_chunk(p, n, k)[1] for k in range(p)], "recv")
+    _numel_check(recv, _chunk_lengths(p, n), "recv")
     _check(LIB.ccl_reduce_scatter(_ptr_array([t.data_ptr() for t in send]),
                                   _ptr_array([t.data_ptr() for t in recv]), p, n,
                                   _dtype_code(send[0]), _op_code(op), _stream(stream, send[0].device)),
@@ -245,7 +247,7 @@ def ccl_all_gather(send, recv, stream=None) -> None:
     n = sum(t.numel() for t in send)
     if len(recv) != p or recv[0].dtype != send[0].dtype:
         raise ValueError("recv must hold p buffers of the send dtype")
-    _numel_check(send, [_chunk(p, n, k)[1] for k in range(p)], "send")
+    _numel_check(send, _chunk_lengths(p, n), "send")
     _numel_check(recv, [n] * p, "recv")
     _check(LIB.ccl_all_gather(_ptr_array([t.data_ptr() for t in send]),
                               _ptr_array([t.data_ptr() for t in recv]), p, n,
@@ -287,7 +289,7 @@ def ccl_scatter(send, recv, root: int = 0, stream=None) -> None:
     p, n = len(recv), send.numel()
     if recv[0].dtype != send.dtype:
         raise ValueError("recv must hold p buffers of the send dtype")
-    _numel_check(recv, [_chunk(p, n, k)[1] for k in range(p)], "recv")
+    _numel_check(recv, _chunk_lengths(p, n), "recv")
     _check(LIB.ccl_scatter(send.data_ptr(), _ptr_array([t.data_ptr() for t in recv]), p, n,
                            _dtype_code(send), root, _stream(stream, send.device)), "ccl_scatter")
 
@@ -298,7 +300,7 @@ def ccl_gather(send, recv, root: int = 0, stream=None) -> None:
     p, n = len(send), recv.numel()
     if recv.dtype != send[0].dtype:
         raise ValueError("recv must have the send dtype")
-    _numel_check(send, [_chunk(p, n, k)[1] for k in range(p)], "send")
+    _numel_check(send, _chunk_lengths(p, n), "send")
     _check(LIB.ccl_gather(_ptr_array([t.data_ptr() for t in send]), recv.data_ptr(), p, n,
                           _dtype_code(recv), root, _stream(stream, recv.device)), "ccl_gather")
 
@@ -369,7 +371,7 @@ def ccl_ring_reduce_scatter_literal(send, recv, op: str = "sum", workspace=None,
     send, recv = _tensors(send, "send"), _tensors(recv, "recv")
     p, n = len(send), send[0].numel()
     _numel_check(send, [n] * p, "send")
-    _numel_check(recv, [_chunk(p, n, k)[1] for k in range(p)], "recv")
+    _numel_check(recv, _chunk_lengths(p, n), "recv")
     ws, ws_bytes = _workspace(CCL_KIND_REDUCE_SCATTER, p, n, send[0], workspace)
     sent = (ctypes.c_uint64 * p)()
     _check(LIB.ccl_ring_reduce_scatter_literal(_ptr_array([t.data_ptr() for t in send]),
@@ -385,7 +387,7 @@ def ccl_ring_all_gather_literal(send, recv, stream=None) -> list[int]:
     send, recv = _tensors(send, "send"), _tensors(recv, "recv")
     p = len(send)
     n = sum(t.numel() for t in send)
-    _numel_check(send, [_chunk(p, n, k)[1] for k in range(p)], "send")
+    _numel_check(send, _chunk_lengths(p, n), "send")
     _numel_check(recv, [n] * p, "recv")
     sent = (ctypes.c_uint64 * p)()
     _check(LIB.ccl_ring_all_gather_literal(_ptr_array([t.data_ptr() for t in send]),
@@ -415,7 +417,7 @@ def ccl_ring_reduce_scatter_literal_noalloc(send, recv, op: str = "sum", stream=
     send, recv = _tensors(send, "send"), _tensors(recv, "recv")
     p, n = len(send), send[0].numel()
     _numel_check(send, [n] * p, "send")
-    _numel_check(recv, [_chunk(p, n, k)[1] for k in range(p)], "recv")
+    _numel_check(recv, _chunk_lengths(p, n), "recv")
     sent = (ctypes.c_uint64 * p)()
     _check(fn(_ptr_array([t.data_ptr() for t in send]), _ptr_array([t.data_ptr() for t in recv]),
               p, n, _dtype_code(send[0]), _op_code(op), sent, _stream(stream, send[0].device)),

@@ -75,10 +75,12 @@ __device__ __forceinline__ void row_bases(const int64_t* counts, int p, int s, i
 }
 
 // One CTA per (tile of tokens, source).  Each 16-byte vector of a token row
-// (8 bf16) is loaded once and stored to the k destinations.  FP8: the 16
-// threads holding a 128-element block (vectors are handed out so that 16
-// consecutive threads hold one block) reduce its amax with shuffles; scale =
-// amax / 448, code = e4m3(x / scale), round to nearest even, saturating.
+// (8 bf16) is loaded once and stored to the k destinations.  FP8: 16
+// elements per thread, and the 8 threads holding a 128-element block (vectors
+// are handed out so that 8 consecutive threads hold one block) reduce its amax
+// with shuffles;
+// inv = 448 / amax, code = e4m3(x * inv), round to nearest even, saturating;
+// the block scale amax / 448 is stored for dequantisation.
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_constant__ MoeDispatchArgs a) {
   __shared__ int64_t base[kMoeMaxRanks];
@@ -117,41 +119,51 @@ __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_con
     const uint64_t t = t0 + tt;
     if (t >= a.tokens) break;
     const char* src = static_cast<const char*>(a.x[s]) + t * h * 2;
-    for (uint64_t v = threadIdx.x; v < nvec; v += kThreads) {
-      uint32_t w[4];
-      load_raw<kBF16, 8>(src, v * 8, w);
-      if constexpr (!FP8) {
+    if constexpr (!FP8) {
+      for (uint64_t v = threadIdx.x; v < nvec; v += kThreads) {
+        uint32_t w[4];
+        load_raw<kBF16, 8>(src, v * 8, w);
         for (int j = 0; j < k; ++j) {
           const int d = dest[tt][j];
           if (d >= 0) store_raw<kBF16, 8>(a.recv[d], static_cast<uint64_t>(pos[tt][j]) * h + v * 8, w);
         }
-      } else {
-        float x[8];
+      }
+    } else {
+      // 16 elements (two 16-byte loads) per thread; the 8 consecutive threads
+      // holding a 128-element block reduce its amax with shuffles; one
+      // reciprocal per block, one multiply per element, one 16-byte store of
+      // codes per destination row
+      const uint64_t nv16 = h / 16;
+      for (uint64_t v = threadIdx.x; v < nv16; v += kThreads) {
+        uint32_t w[8];
+        load_raw<kBF16, 8>(src, v * 16, w);
+        load_raw<kBF16, 8>(src, v * 16 + 8, w + 4);
+        float x[16];
         float amax = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 16; ++e) {
           x[e] = widen<kBF16>(w, e);
           amax = fmaxf(amax, fabsf(x[e]));
         }
-        // the 16 lanes of this block are all active (hidden is a multiple of 128)
-        const unsigned group = 0xFFFFu << (threadIdx.x & 16);
+        // the 8 lanes of this block are all active (hidden is a multiple of 128)
+        const unsigned group = 0xFFu << (threadIdx.x & 24);
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(group, amax, off));
+        for (int off = 4; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(group, amax, off));
+        const float inv = (amax > 0.0f) ? __fdiv_rn(448.0f, amax) : 1.0f;
         const float scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        uint32_t q[2] = {0, 0};
+        uint32_t q[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t c = __nv_cvt_float_to_fp8(__fdiv_rn(x[e], scale), __NV_SATFINITE, __NV_E4M3);
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t c = __nv_cvt_float_to_fp8(__fmul_rn(x[e], inv), __NV_SATFINITE, __NV_E4M3);
           q[e >> 2] |= (c & 0xFFu) << (8 * (e & 3));
         }
-        const uint64_t blk = v / 16;  // 16 vectors of 8 = one 128-element block
+        const uint64_t blk = v / 8;  // 8 vectors of 16 = one 128-element block
         for (int j = 0; j < k; ++j) {
           const int d = dest[tt][j];
           if (d < 0) continue;
           const uint64_t row = static_cast<uint64_t>(pos[tt][j]);
-          char* dst = static_cast<char*>(a.recv[d]) + row * h + v * 8;
-          asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(dst), "r"(q[0]), "r"(q[1]) : "memory");
-          if ((threadIdx.x & 15) == 0) a.scales[d][row * (h / 128) + blk] = scale;
+          st_stream16(static_cast<char*>(a.recv[d]) + row * h + v * 16, make_uint4(q[0], q[1], q[2], q[3]));
+          if ((threadIdx.x & 7) == 0) a.scales[d][row * (h / 128) + blk] = scale;
         }
       }
     }

@@ -132,7 +132,7 @@ def test_fp8_rows_within_half_ulp():
             deq = moe.e4m3_to_f32(recv[d][pos]).reshape(-1, 128) * scales[d][pos][:, None]
             err = np.abs(deq - x[i // k].reshape(-1, 128))
             bound = np.maximum(np.abs(x[i // k].reshape(-1, 128)) * 2.0**-4,
-                               scales[d][pos][:, None] * 2.0**-10) * (1 + 1e-6)
+                               scales[d][pos][:, None] * 2.0**-10) * (1 + 1e-5)
             assert (err <= bound).all()
             amax = np.abs(x[i // k].reshape(-1, 128)).max(axis=1)
             np.testing.assert_array_equal(scales[d][pos], (amax / np.float32(448)).astype(np.float32))
