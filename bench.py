@@ -817,9 +817,26 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
     torch.cuda.synchronize(device)
     if a.steps <= 0:  # auto: about one second of timed device work
         ms_warm = w0.elapsed_time(w1) / a.warmup
-        a.steps = int(max(50, min(200000, round(1000.0 / max(ms_warm, 1e-3)))))
+        a.steps = int(max(64, min(200000, round(1000.0 / max(ms_warm, 1e-3)))))
+        a.steps = -(-a.steps // 64) * 64  # a multiple of the graph's 64 steps
         a.steps = int(max_over_ranks(float(a.steps), world, device))
 
+    # The timed steps replay a CUDA graph of G steps (G divides K), so that the
+    # host cost of issuing a call never leaves the GPU idle between steps;
+    # --eager issues every step from Python instead.
+    graph, group = None, 1
+    if not a.eager:
+        group = max(d for d in range(1, min(a.steps, 64) + 1) if a.steps % d == 0)
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(group):
+                wl.step(cap)
+        stream.wait_stream(cap)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize(device)
     sampler = ClockSampler(local)
     time.sleep(0.05)
     launches0 = lib.ccl_kernel_launch_count()
@@ -828,13 +845,26 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
     torch.cuda.synchronize(device)
     t0 = time.time()
     start.record(stream)
-    for _ in range(a.steps):
-        wl.step(stream)
+    if graph is None:
+        for _ in range(a.steps):
+            wl.step(stream)
+    else:
+        with torch.cuda.stream(stream):
+            for _ in range(a.steps // group):
+                graph.replay()
     stop.record(stream)
     torch.cuda.synchronize(device)
     t1 = time.time()
     barrier(world, device)
-    launches = lib.ccl_kernel_launch_count() - launches0
+    # kernels launched by the timed steps (a replayed graph launches its
+    # captured kernels without calling the library again)
+    per_step = (lib.ccl_kernel_launch_count() - launches0) if graph is None else None
+    if graph is not None:
+        c0 = lib.ccl_kernel_launch_count()
+        wl.step(stream)
+        torch.cuda.synchronize(device)
+        per_step = (lib.ccl_kernel_launch_count() - c0) * a.steps
+    launches = per_step
     sampler.stop()
     ms_total = start.elapsed_time(stop)
     ms_total = max_over_ranks(ms_total, world, device)
@@ -883,14 +913,30 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
         k = max(3, min(a.steps, 200))
         for _ in range(3):
             fn(stream)
+        pg = None
+        if not a.eager:
+            cap = torch.cuda.Stream(device)
+            cap.wait_stream(stream)
+            pg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(pg, stream=cap):
+                for _ in range(k):
+                    fn(cap)
+            stream.wait_stream(cap)
+            with torch.cuda.stream(stream):
+                pg.replay()
         p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         p0.record(stream)
-        for _ in range(k):
-            fn(stream)
+        if pg is None:
+            for _ in range(k):
+                fn(stream)
+        else:
+            with torch.cuda.stream(stream):
+                pg.replay()
         p1.record(stream)
         torch.cuda.synchronize(device)
         ms = max_over_ranks(p0.elapsed_time(p1) / k, world, device)
         part_stats.append((name, pbytes, ms))
+        del pg
     if rank != 0:
         return None
     name, pbytes, pms = max(part_stats, key=lambda t: t[2])
@@ -911,6 +957,8 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
     cfg["l2"] = (f"no flush: each step touches {footprint / 1e6:.0f} MB "
                  f"({footprint / L2_BYTES:.1f}x the 129 MB L2), steps back to back")
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU, p virtual ranks in HBM"
+    cfg["timing"] = ("eager Python calls" if a.eager else
+                     f"CUDA graph of {group} steps replayed {a.steps // group} times")
     out = {
         "metric": "effective GB/s (primitive minimum bytes / step time) and fraction of HBM roofline",
         "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": a.steps,
@@ -1019,6 +1067,8 @@ def main(argv=None) -> int:
                     choices=["ring", "recursive_doubling", "rabenseifner", "binomial_tree", "naive"],
                     help="fold order of --workload allreduce")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="issue every timed step from Python instead of replaying a CUDA graph")
     ap.add_argument("--sweep", action="store_true",
                     help="all-reduce message-size sweep (1 KiB..1 GiB per rank), one line per point")
     ap.add_argument("--sweep-stride", type=int, default=1, help="log2 step between sweep sizes")
