@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
         "ccl_all_to_allv": (st, [pp, ctypes.POINTER(sz), pp, i32, sz, i32, vp]),
         "ccl_ring_literal_workspace_bytes": (sz, [i32, i32, sz, i32]),
         "ccl_moe_route": (st, [pp, i32, sz, i32, i32, vp, pp, vp]),
+        "ccl_all_to_all_heads": (st, [pp, pp, i32, sz, sz, sz, i32, i32, vp]),
         "ccl_moe_dispatch": (st, [pp, pp, vp, pp, i32, sz, i32, i32, sz, i32, pp, ctypes.POINTER(sz),
                                   pp, pp, vp]),
         "ccl_moe_combine": (st, [pp, ctypes.POINTER(sz), pp, pp, vp, pp, i32, sz, i32, i32, sz, pp, vp]),
@@ -479,3 +480,21 @@ def ccl_moe_combine(y, expert_ids, weights, counts, slots, num_experts: int, out
                                _ptr_array([t.data_ptr() for t in slots]), p, tokens, k, num_experts,
                                hidden, _ptr_array([t.data_ptr() for t in out]),
                                _stream(stream, out[0].device)), "ccl_moe_combine")
+
+
+# ------------------------------------------------ Ulysses head <-> sequence
+def ccl_all_to_all_heads(send, recv, seq_per_rank: int, heads: int, head_dim: int,
+                         inverse: bool = False, stream=None) -> None:
+    """Forward: send[r] = [seq_per_rank, heads, head_dim] sequence shard ->
+    recv[r] = [p*seq_per_rank, heads/p, head_dim] head group; inverse: back."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p = len(send)
+    n = seq_per_rank * heads * head_dim
+    if len(recv) != p or recv[0].dtype != send[0].dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [n] * p, "recv")
+    _check(LIB.ccl_all_to_all_heads(_ptr_array([t.data_ptr() for t in send]),
+                                    _ptr_array([t.data_ptr() for t in recv]), p, seq_per_rank, heads,
+                                    head_dim, _dtype_code(send[0]), 1 if inverse else 0,
+                                    _stream(stream, send[0].device)), "ccl_all_to_all_heads")

@@ -669,6 +669,52 @@ extern "C" ccl_status_t ccl_moe_combine(const void* const* y, const size_t* y_ro
   return CCL_OK;
 }
 
+// ============================================= Ulysses head <-> sequence all-to-all
+extern "C" ccl_status_t ccl_all_to_all_heads(const void* const* send, void* const* recv, int p,
+                                             size_t seq_per_rank, size_t heads, size_t head_dim,
+                                             ccl_dtype_t dt, int inverse, void* stream) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (heads == 0 || heads % static_cast<size_t>(p) != 0)
+    return fail(CCL_ERR_INVALID_ARG, "heads=%zu must be a positive multiple of p=%d", heads, p);
+  if (seq_per_rank > (1ull << 32) || heads > (1ull << 20) || head_dim > (1ull << 20))
+    return fail(CCL_ERR_INVALID_ARG, "sizes too large");
+  if (send == nullptr || recv == nullptr) return fail(CCL_ERR_INVALID_ARG, "send or recv array is NULL");
+  const uint64_t n = seq_per_rank * heads * head_dim;  // elements per rank, both layouts
+  if (n == 0) return CCL_OK;
+  uint64_t b[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    b[r] = n * e;
+    in[r] = span(send[r], b[r]);
+    out[r] = span(recv[r], b[r]);
+  }
+  if ((st = check_buffers("send", send, p, b, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", const_cast<const void* const*>(recv), p, b, e)) != CCL_OK) return st;
+  if ((st = check_aliasing(in, out, nullptr, p)) != CCL_OK) return st;
+  UlyssesArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.x[r] = send[r];
+    a.y[r] = recv[r];
+  }
+  a.seq_per_rank = seq_per_rank;
+  a.heads = heads;
+  a.head_dim = head_dim;
+  a.segments = static_cast<uint64_t>(p) * p * seq_per_rank;
+  a.p = p;
+  a.inverse = inverse ? 1 : 0;
+  const uint64_t seg_bytes = heads / p * head_dim * e;
+  const bool vec = all_aligned16(send, p, const_cast<const void* const*>(recv)) &&
+                   seg_bytes % 16 == 0 && (heads * head_dim * e) % 16 == 0;
+  cudaError_t err = launch_ulysses(dt, vec, a, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "Ulysses all-to-all kernel launch");
+  return CCL_OK;
+}
+
 // ============================================================== all-to-allv
 extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts,
                                         void* const* recv, int p, size_t row_elems,

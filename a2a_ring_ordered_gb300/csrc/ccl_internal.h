@@ -91,6 +91,15 @@ cudaError_t launch_xfer(int kind, int dt, int op, const XferArgs& a, cudaStream_
 void clear_last_error();
 ccl_status_t report_error(ccl_status_t st, const char* fmt, ...);
 
+// ------------------------------------------------- Ulysses head <-> sequence
+struct UlyssesArgs {
+  const void* x[CCL_MAX_RANKS];  // inputs (sequence shards, or head groups when inverse)
+  void* y[CCL_MAX_RANKS];        // outputs
+  uint64_t seq_per_rank, heads, head_dim, segments;  // segments = p * p * seq_per_rank
+  int p, inverse;
+};
+cudaError_t launch_ulysses(int dt, bool vec, const UlyssesArgs& a, cudaStream_t s);
+
 // ------------------------------------------------------------------- MoE
 constexpr int kMoeMaxRanks = 64;  // keeps every MoE parameter block under 4 KB
 constexpr int kMoeMaxK = 16;

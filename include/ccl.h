@@ -216,6 +216,19 @@ ccl_status_t ccl_plan_buckets(const size_t* numel, size_t count, size_t elem_byt
                               size_t cap_bytes, uint32_t* bucket_of, size_t* offset,
                               size_t* bucket_numel, size_t* num_buckets);
 
+/* Head <-> sequence all-to-all of sequence-parallel attention ("LLM
+ * Distributed Training Collectives", Sequence Parallelism / Ulysses).
+ * Forward (inverse == 0): send[r] is sequence shard r with every head,
+ * [seq_per_rank, heads, head_dim]; recv[r] gets the whole sequence of head
+ * group r, [p * seq_per_rank, heads / p, head_dim]:
+ *   recv[r][s*seq_per_rank + t][h][:] = send[s][t][r*heads/p + h][:].
+ * Inverse (inverse != 0): the same arguments describe the way back (send[r]
+ * is head group r, recv[s] gets sequence shard s).  heads must be a multiple
+ * of p.  Buffers must not overlap.  Pure copy, bit-exact. */
+ccl_status_t ccl_all_to_all_heads(const void* const* send, void* const* recv, int p,
+                                  size_t seq_per_rank, size_t heads, size_t head_dim,
+                                  ccl_dtype_t dt, int inverse, void* stream);
+
 /* ------------------------------------------------- MoE expert parallelism
  * "Networks and Collective Communication" section 7.4: every MoE layer does an
  * all-to-all dispatch (each token to the ranks holding the k experts it chose)

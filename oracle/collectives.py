@@ -99,3 +99,29 @@ def all_to_allv(send: list[np.ndarray], counts: np.ndarray, row_elems: int) -> l
         blocks.append(row)
     return [np.concatenate([blocks[s][d] for s in range(p)]) if p else np.zeros(0)
             for d in range(p)]
+
+
+def ulysses_seq_to_heads(x: list[np.ndarray], heads: int, head_dim: int) -> list[np.ndarray]:
+    """Sequence-parallel attention's all-to-all ("LLM Distributed Training
+    Collectives", Sequence Parallelism / Ulysses): rank r holds sequence shard r
+    with every head, shape [S/p, H, D]; afterwards rank r holds the whole
+    sequence for head group r, [S, H/p, D]:
+        y_r[s * S/p + t, h, :] = x_s[t, r * H/p + h, :]."""
+    p = len(x)
+    if heads % p:
+        raise ValueError("heads must be a multiple of p")
+    hp = heads // p
+    xs = [xi.reshape(-1, heads, head_dim) for xi in x]
+    return [np.concatenate([xs[s][:, r * hp:(r + 1) * hp, :] for s in range(p)], axis=0).reshape(-1)
+            for r in range(p)]
+
+
+def ulysses_heads_to_seq(y: list[np.ndarray], heads: int, head_dim: int) -> list[np.ndarray]:
+    """The inverse exchange: [S, H/p, D] per head group back to [S/p, H, D] per
+    sequence shard: x_s[t, r * H/p + h, :] = y_r[s * S/p + t, h, :]."""
+    p = len(y)
+    hp = heads // p
+    ys = [yi.reshape(-1, hp, head_dim) for yi in y]
+    sp = ys[0].shape[0] // p
+    return [np.concatenate([ys[r][s * sp:(s + 1) * sp] for r in range(p)], axis=1).reshape(-1)
+            for s in range(p)]

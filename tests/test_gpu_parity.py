@@ -556,3 +556,22 @@ def test_bucket_reads_and_writes_pinned_host_memory(lib):
     torch.cuda.synchronize()
     for r in range(p):
         np.testing.assert_array_equal(h_out[r].view(torch.int16).numpy().view(np.uint16), want[r])
+
+
+# ------------------------------------------------ Ulysses head <-> sequence
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("p,sp,H,D", [(1, 5, 4, 8), (2, 64, 8, 64), (4, 33, 16, 128), (8, 128, 32, 128),
+                                      (4, 7, 4, 3)])
+def test_ulysses_all_to_all_matches_oracle(lib, dtype, p, sp, H, D):
+    n = sp * H * D
+    x = make_inputs(dtype, p, n, seed=p * 7 + sp)
+    want = collectives.ulysses_seq_to_heads(x, H, D)
+    outs = guarded_outputs(p, [n] * p, dtype)
+    lib.ccl_all_to_all_heads([to_dev(v, dtype) for v in x], [o.view for o in outs], sp, H, D)
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"heads rank {r}")
+        assert outs[r].guards_intact()
+    back = [torch.empty(n, dtype=outs[0].view.dtype, device="cuda") for _ in range(p)]
+    lib.ccl_all_to_all_heads([o.view for o in outs], back, sp, H, D, inverse=True)
+    for r in range(p):
+        assert_equal(to_host(back[r]), x[r], dtype, f"inverse rank {r}")

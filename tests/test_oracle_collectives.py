@@ -164,3 +164,32 @@ def test_ring_reduce_integer_values_exact():
     x = workloads.integer_valued(6, 37, 2)
     red = collectives.reduce_ring(x, 2)[2]
     np.testing.assert_array_equal(red, np.stack(x).sum(axis=0))
+
+
+@pytest.mark.parametrize("p,sp,H,D", [(1, 3, 2, 4), (2, 5, 4, 8), (4, 3, 8, 16), (8, 2, 16, 4)])
+def test_ulysses_exchange_by_brute_force_and_inverse(p, sp, H, D):
+    """Element (s, t, h, d) of the sequence shards lands at (r = h // (H/p),
+    row s*sp + t, head h % (H/p), d) -- checked element by element -- and the
+    inverse exchange restores every shard."""
+    x = [np.arange(sp * H * D, dtype=np.float32) + 10_000 * s for s in range(p)]
+    y = collectives.ulysses_seq_to_heads(x, H, D)
+    hp = H // p
+    for s in range(p):
+        for t in range(sp):
+            for h in range(H):
+                r = h // hp
+                got = y[r].reshape(p * sp, hp, D)[s * sp + t, h % hp]
+                want = x[s].reshape(sp, H, D)[t, h]
+                np.testing.assert_array_equal(got, want)
+    back = collectives.ulysses_heads_to_seq(y, H, D)
+    for a, b in zip(x, back):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_ulysses_is_an_all_to_all_of_contiguous_segments():
+    """With one token per shard and D = 1 the exchange is the plain block
+    transpose of section 4.1."""
+    p = 4
+    x = workloads.normal(p, p, 1.0, 0)  # shard s: [1 token, H = p heads, D = 1]
+    np.testing.assert_array_equal(np.concatenate(collectives.ulysses_seq_to_heads(x, p, 1)),
+                                  np.concatenate(collectives.all_to_all(x)))
