@@ -142,6 +142,7 @@ KERNEL_SOURCES = {
     "ring_step": ["a2a_ring_ordered_gb300/csrc/ring_step.cu",
                   "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "moe": ["a2a_ring_ordered_gb300/csrc/moe.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
+    "ulysses": ["a2a_ring_ordered_gb300/csrc/ulysses.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
 }
 for _part in ("moe_route", "moe_dispatch", "moe_combine"):
     KERNEL_SOURCES[_part] = KERNEL_SOURCES["moe"]
@@ -688,6 +689,48 @@ class MoeEp(Workload):
                 ("moe_combine", c, self._combine)]
 
 
+class Ulysses(Workload):
+    """Ulysses head <-> sequence all-to-all: p ranks x (S/p tokens, H heads,
+    D = 128) bf16, forward then inverse (2 launches)."""
+    kernel = "ulysses"
+    launches_per_step = 2
+
+    def __init__(self, p=8, seq_per_rank=8192, heads=32, head_dim=128):
+        self.p, self.sp, self.H, self.D = p, seq_per_rank, heads, head_dim
+        self.n = seq_per_rank * heads * head_dim
+        self.name = "ulysses_all_to_all"
+        self.kernel_key = f"ulysses_p{p}_s{seq_per_rank}_h{heads}_d{head_dim}"
+
+    def config(self):
+        return {"workload": f"Ulysses head<->sequence all-to-all: p={self.p} ranks x {self.sp} tokens x "
+                            f"{self.H} heads x {self.D} bf16, forward + inverse",
+                "p": self.p, "tokens_per_rank": self.sp, "heads": self.H, "head_dim": self.D,
+                "inputs": "N(0,1) drawn on the device"}
+
+    def setup(self, lib, torch, device):
+        self.lib = lib
+        self.x = [torch.randn(self.n, device=device).to(torch.bfloat16) for _ in range(self.p)]
+        self.y = [torch.empty_like(t) for t in self.x]
+        self.z = [torch.empty_like(t) for t in self.x]
+
+    def bytes_per_step(self):
+        return 2 * 2 * self.p * self.n * 2
+
+    def _fwd(self, s):
+        self.lib.ccl_all_to_all_heads(self.x, self.y, self.sp, self.H, self.D, stream=s)
+
+    def _inv(self, s):
+        self.lib.ccl_all_to_all_heads(self.y, self.z, self.sp, self.H, self.D, inverse=True, stream=s)
+
+    def step(self, stream):
+        self._fwd(stream)
+        self._inv(stream)
+
+    def parts(self):
+        half = self.bytes_per_step() // 2
+        return [("ulysses", half, self._fwd), ("ulysses", half, self._inv)]
+
+
 def make_workload(a) -> Workload:
     if a.workload == "bucket":
         return Bucket()
@@ -705,6 +748,8 @@ def make_workload(a) -> Workload:
         return Moe()
     if a.workload == "ddp":
         return Ddp()
+    if a.workload == "ulysses":
+        return Ulysses(p=a.p or 8)
     if a.workload == "moe_ep":
         return MoeEp(fp8=a.dtype != "bf16")
     if a.workload in ("broadcast", "reduce", "scatter", "gather"):
@@ -1060,7 +1105,8 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bucket",
                     choices=["bucket", "allreduce", "reduce_scatter", "all_gather", "zero", "moe",
-                             "literal", "ddp", "broadcast", "reduce", "scatter", "gather", "moe_ep"])
+                             "literal", "ddp", "broadcast", "reduce", "scatter", "gather", "moe_ep",
+                             "ulysses"])
     ap.add_argument("--p", type=int, default=0)
     ap.add_argument("--mib", type=int, default=0)
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
