@@ -229,22 +229,54 @@ class Bucket(Workload):
         self.x = self.host_inputs()
         self.send = [torch.from_numpy(v).to(device) for v in self.x]
         self.recv = [torch.empty(self.n, dtype=torch.bfloat16, device=device) for _ in range(self.p)]
-        # pinned host copies for the end-to-end path
+        # pinned host copies for the end-to-end path, and a second device buffer
+        # set so that consecutive steps can overlap copy-out with copy-in
         self.h_in = [torch.from_numpy(v).pin_memory() for v in self.x]
         self.h_out = [torch.empty(self.n, dtype=torch.bfloat16).pin_memory() for _ in range(self.p)]
+        self.sets = [(self.send, self.recv),
+                     ([torch.empty_like(t) for t in self.send], [torch.empty_like(t) for t in self.recv])]
+        self.s_h2d, self.s_d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        self.i_e2e = 0
+        self.freed = [None, None]  # per set: event after its last kernel and copy-out
 
     def step(self, stream):
         self.lib.ccl_bucket_allreduce_scale_cast(self.send, self.recv, scale=self.scale, stream=stream)
 
     def e2e_step(self, stream):
         """Pinned host inputs to pinned host outputs through the public API:
-        H2D copies of the p fp32 gradient buffers, the kernel, D2H copies of the
-        p bf16 results (one cudaMemcpyAsync per buffer)."""
-        for d, h in zip(self.send, self.h_in):
-            d.copy_(h, non_blocking=True)
-        self.step(stream)
-        for h, d in zip(self.h_out, self.recv):
-            h.copy_(d, non_blocking=True)
+        H2D copies of the p fp32 gradient buffers (copy-in stream), the kernel
+        (the caller's stream), D2H copies of the p bf16 results (copy-out
+        stream), one cudaMemcpyAsync per buffer.  Consecutive steps alternate
+        between two device buffer sets, so step i's copy-out overlaps step
+        i+1's copy-in, as successive DDP buckets do."""
+        torch = self.torch
+        k = self.i_e2e % 2
+        self.i_e2e += 1
+        send, recv = self.sets[k]
+        if self.freed[k] is not None:
+            self.s_h2d.wait_event(self.freed[k])
+        with torch.cuda.stream(self.s_h2d):
+            for d, h in zip(send, self.h_in):
+                d.copy_(h, non_blocking=True)
+        stream.wait_stream(self.s_h2d)
+        self.lib.ccl_bucket_allreduce_scale_cast(send, recv, scale=self.scale, stream=stream)
+        self.s_d2h.wait_stream(stream)
+        with torch.cuda.stream(self.s_d2h):
+            for h, d in zip(self.h_out, recv):
+                h.copy_(d, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(self.s_d2h)
+        self.freed[k] = ev
+
+    def e2e_begin(self, stream):
+        """Order the copy streams after `stream` (after the timed region's start event)."""
+        self.s_h2d.wait_stream(stream)
+        self.s_d2h.wait_stream(stream)
+
+    def e2e_finish(self, stream):
+        """Make `stream` wait for every outstanding copy of the end-to-end path."""
+        stream.wait_stream(self.s_h2d)
+        stream.wait_stream(self.s_d2h)
 
     def e2e_zero_copy_step(self, stream):
         """Same data movement with no staging: the kernel reads the gradients
@@ -928,8 +960,12 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
         barrier(world, device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        if hasattr(wl, "e2e_begin"):
+            wl.e2e_begin(stream)
         for _ in range(k):
             wl.e2e_step(stream)
+        if hasattr(wl, "e2e_finish"):
+            wl.e2e_finish(stream)
         e1.record(stream)
         torch.cuda.synchronize(device)
         barrier(world, device)
@@ -937,7 +973,8 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
         hb, db = wl.e2e_bytes()
         e2e = {"value": round(world * nbytes / (ms_e2e * 1e-3) / 1e9, 3), "unit": "GB/s",
                "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db,
-               "steps": k, "path": "cudaMemcpyAsync H2D, kernel, cudaMemcpyAsync D2H"}
+               "steps": k, "path": "cudaMemcpyAsync H2D (copy-in stream), kernel, cudaMemcpyAsync D2H "
+                                   "(copy-out stream); step i's copy-out overlaps step i+1's copy-in"}
         if hasattr(wl, "e2e_zero_copy_step"):
             for _ in range(2):
                 wl.e2e_zero_copy_step(stream)
