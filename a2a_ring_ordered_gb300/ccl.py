@@ -21,7 +21,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 # CCL_LIBRARY overrides the in-tree library (e.g. a build kept elsewhere)
 LIB_PATH = os.environ.get("CCL_LIBRARY") or os.path.join(_PKG, "lib", "libccl.so")
 
-CCL_OK, CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED, CCL_ERR_CUDA = 0, 1, 2, 3
+CCL_OK, CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED, CCL_ERR_CUDA, CCL_ERR_TIMEOUT = 0, 1, 2, 3, 4
 CCL_F32, CCL_BF16, CCL_I32 = 0, 1, 2
 CCL_SUM, CCL_MAX, CCL_MIN = 0, 1, 2
 CCL_KIND_ALLREDUCE, CCL_KIND_REDUCE_SCATTER, CCL_KIND_ALL_GATHER = 0, 1, 2

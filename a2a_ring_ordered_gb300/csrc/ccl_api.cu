@@ -198,6 +198,7 @@ extern "C" const char* ccl_status_string(ccl_status_t status) {
     case CCL_ERR_INVALID_ARG: return "CCL_ERR_INVALID_ARG: invalid argument";
     case CCL_ERR_UNSUPPORTED: return "CCL_ERR_UNSUPPORTED: not implemented for these arguments";
     case CCL_ERR_CUDA: return "CCL_ERR_CUDA: a CUDA call failed";
+    case CCL_ERR_TIMEOUT: return "CCL_ERR_TIMEOUT: a bounded wait gave up";
     default: return "unknown ccl_status_t";
   }
 }
