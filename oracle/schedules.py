@@ -14,6 +14,12 @@ TEST INFRASTRUCTURE ONLY -- see ``oracle/__init__.py``.
   broadcast back along it, 2 ceil(log2 p) steps;
 * naive: everyone sends to the root, the root sends the sum to everyone.
 
+Section 6.3 (hierarchical all-reduce) and section 6.1 (two-dimensional
+all-reduce) add a two-level ring: p = a * b devices in b groups of a (the a
+GPUs of a node, or one row of an a x b torus); a ring reduce-scatter inside
+every group, a ring all-reduce across the groups among the devices with the
+same index inside their group, then a ring all-gather inside every group.
+
 Readings (listed in the design doc): a receiver computes (received partial) +
 (own value) -- IEEE addition is commutative, so only the pairing matters;
 the halving step pairs devices at distance p/2 first and a device keeps the
@@ -32,7 +38,8 @@ import math
 import numpy as np
 
 from .bf16 import bf16_to_f32, f32_to_bf16_rne
-from .ring import _check, chunk_bounds, combine
+from .ring import (_check, _finish_chunk, chunk_bounds, combine, ring_all_gather_phase,
+                   ring_reduce_scatter_phase)
 
 SCHEDULES = ("recursive_doubling", "rabenseifner", "binomial_tree", "naive")
 
@@ -162,6 +169,55 @@ def naive(x, dtype="f32", op="sum"):
     result = _finish(acc, dtype)
     out = [result.copy() for _ in range(p)]
     sent[0] += (p - 1) * n * _e(dtype)
+    return out, sent
+
+
+def hierarchical(x, group, dtype="f32", op="sum"):
+    """Two-level ring all-reduce over b = p / group groups of `group`
+    consecutive ranks (group g = ranks g*a .. g*a + a - 1, a = group).
+
+    Readings (listed in the design doc): every ring is the ring of ``oracle.ring``
+    (rank order inside its ring, chunk rule, chunk c starts after its owner);
+    device (g, l) owns chunk l of the a chunks after step 1; in step 2 the
+    ring over the groups for chunk l has group g at position g and cuts that
+    chunk into b sub-chunks by the same chunk rule, sub-chunk m owned by group
+    m; partial sums travel in fp32 (int32) through both reduce-scatters and
+    the owner of a sub-chunk rounds bf16 once, before the all-gathers.
+    Returns (outputs, bytes_sent).
+    """
+    p, n = _check(x, dtype)
+    a = int(group)
+    if a < 1 or p % a:
+        raise ValueError("group must divide p")
+    b = p // a
+    want = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32}[dtype]
+    part = "i32" if dtype == "i32" else "f32"  # what partials travel as
+    sent = [0] * p
+    # 1. reduce-scatter inside every group
+    work = [None] * p
+    for g in range(b):
+        w, s = ring_reduce_scatter_phase([x[g * a + l] for l in range(a)], dtype, op)
+        for l in range(a):
+            work[g * a + l] = w[l]
+            sent[g * a + l] += s[l]
+    out = [np.zeros(n, dtype=want) for _ in range(p)]
+    # 2. all-reduce of chunk l across the groups (a rings, one per local index)
+    for l, (off, ln) in enumerate(chunk_bounds(a, n)):
+        w2, s2 = ring_reduce_scatter_phase([work[g * a + l][off:off + ln] for g in range(b)], part, op)
+        bufs = []
+        for g, (o2, l2) in enumerate(chunk_bounds(b, ln)):
+            buf = np.zeros(ln, dtype=want)
+            buf[o2:o2 + l2] = _finish_chunk(w2[g][o2:o2 + l2], dtype)
+            bufs.append(buf)
+        s3 = ring_all_gather_phase(bufs, dtype)
+        for g in range(b):
+            sent[g * a + l] += s2[g] + s3[g]
+            out[g * a + l][off:off + ln] = bufs[g]
+    # 3. all-gather inside every group
+    for g in range(b):
+        s4 = ring_all_gather_phase([out[g * a + l] for l in range(a)], dtype)
+        for l in range(a):
+            sent[g * a + l] += s4[l]
     return out, sent
 
 

@@ -113,3 +113,79 @@ def test_power_of_two_required():
         schedules.recursive_doubling(workloads.normal(6, 10, 1.0, 0))
     with pytest.raises(ValueError):
         schedules.rabenseifner(workloads.normal(3, 10, 1.0, 0))
+
+
+# ------------------------------------------------- hierarchical / 2-D ring
+# Hand-derived (fp32, nearest even; 2^24 + 1 rounds to 2^24).
+#   p = 6, groups of 3: group 0 = (-2^24, 2^24, 1), group 1 = zeros.  Chunk l
+#   of the group ring starts at local rank l + 1:
+#     l = 0: (2^24 + 1) - 2^24 = 0;  l = 1: (1 - 2^24) + 2^24 = 1;
+#     l = 2: (-2^24 + 2^24) + 1 = 1; the 2-group ring adds zeros.
+#   p = 6, groups of 2: group partials (-2^24, 2^24, 1); sub-chunk m of the
+#   ring over the groups starts at group m + 1:
+#     m = 0: (2^24 + 1) - 2^24 = 0;  m = 1: (1 - 2^24) + 2^24 = 1;
+#     m = 2: (-2^24 + 2^24) + 1 = 1.
+HIER_CASES = [
+    (3, [-(2.0**24), 2.0**24, 1.0, 0.0, 0.0, 0.0], [0, 0, 1, 1, 1, 1]),
+    (2, [-(2.0**24), 0.0, 2.0**24, 0.0, 1.0, 0.0], [0, 1, 1, 0, 1, 1]),
+]
+
+
+@pytest.mark.parametrize("group,vals,want", HIER_CASES)
+def test_hierarchical_fold_order_by_hand(group, vals, want):
+    x = [np.full(6, v, dtype=np.float32) for v in vals]
+    out, _ = schedules.hierarchical(x, group)
+    for o in out:
+        np.testing.assert_array_equal(o, np.array(want, dtype=np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,n", [(1, 5), (4, 1), (6, 23), (8, 1000), (12, 37)])
+def test_hierarchical_with_one_level_is_the_ring(dtype, p, n):
+    """One group of p, or p groups of one: the two-level ring is the flat ring."""
+    x = (workloads.integer_valued(p, n, 5, lo=-2**30, hi=2**30, dtype="i32") if dtype == "i32"
+         else workloads.normal(p, n, 1.0, 5, dtype=dtype))
+    want, _, _ = ring.ring_allreduce(x, dtype)
+    for group in (1, p):
+        out, _ = schedules.hierarchical(x, group, dtype)
+        for o, w in zip(out, want):
+            np.testing.assert_array_equal(o, w)
+
+
+@pytest.mark.parametrize("p,group", [(4, 2), (6, 3), (6, 2), (8, 4), (16, 8), (12, 4)])
+def test_hierarchical_exact_integer_sums_and_identical_outputs(p, group):
+    for n in (p, 3 * p + 1, 100, 1):
+        x = workloads.integer_valued(p, n, seed=p + n)
+        out, _ = schedules.hierarchical(x, group)
+        exact = np.stack(x).astype(np.int64).sum(axis=0)
+        for o in out:
+            np.testing.assert_array_equal(o.astype(np.int64), exact)
+    y = workloads.normal(p, 501, 1.0, 9, dtype="bf16")
+    out, _ = schedules.hierarchical(y, group, "bf16")
+    for o in out[1:]:
+        np.testing.assert_array_equal(o, out[0])
+
+
+def test_hierarchical_differs_from_the_flat_ring():
+    """Same data as the first hand case: the flat 6-ring starts chunk 0 at rank 1."""
+    x = [np.full(6, v, dtype=np.float32) for v in HIER_CASES[0][1]]
+    flat, _, _ = ring.ring_allreduce(x)
+    hier, _ = schedules.hierarchical(x, 3)
+    assert not np.array_equal(flat[0], hier[0])
+
+
+def test_hierarchical_bytes_section_6_3():
+    """p = 16 as 2 nodes x 8 GPUs, n divisible by everything: each GPU sends
+    2 (a-1)/a n inside its node and 2 (N-1)/N n/8 across nodes (fp32)."""
+    p, a, n = 16, 8, 16 * 64
+    x = workloads.normal(p, n, 1.0, 3)
+    _, sent = schedules.hierarchical(x, a)
+    b = p // a
+    intra = 2 * (a - 1) * n // a
+    inter = 2 * (b - 1) * (n // a) // b
+    assert all(s == 4 * (intra + inter) for s in sent)
+
+
+def test_hierarchical_group_must_divide_p():
+    with pytest.raises(ValueError):
+        schedules.hierarchical(workloads.normal(6, 10, 1.0, 0), 4)
