@@ -10,6 +10,7 @@
 // by source, then token, then choice.  route() gives each (t, j) its slot --
 // its rank among the rows the source sends to the same destination -- so the
 // row lands at sum_{s' < s} counts[s'][d] + slot of d's buffer.
+#include <cooperative_groups.h>
 #include <cuda_fp8.h>
 
 #include "device_common.cuh"
@@ -17,50 +18,122 @@
 namespace ccl {
 namespace {
 
-constexpr int kRouteThreads = 1024;  // 32 warps
+constexpr int kRouteThreads = 1024;                  // 32 warps
+constexpr int kRouteSub = 4;                         // items per thread per tile
+constexpr int kRouteTile = kRouteThreads * kRouteSub;  // 4096 items
+constexpr int kRouteRows = kRouteSub * 32;           // one count row per (sub-tile, warp)
+constexpr int kRouteMaxCluster = 8;                  // portable cluster size
 
-// One CTA per source.  Items (t, j) are taken in order, 1024 per tile; inside
-// a warp __match_any_sync groups the lanes with the same destination, which
-// gives each item its rank among earlier same-destination items of the warp;
-// an exclusive scan over the 32 warps on top of the running per-destination
-// count turns that into the slot.
-__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const __grid_constant__ MoeRouteArgs a) {
-  __shared__ int warp_cnt[32][kMoeMaxRanks];
+__device__ __forceinline__ int route_dest(const MoeRouteArgs& a, const int32_t* ids, uint64_t item,
+                                          uint64_t hi) {
+  if (item >= hi) return -1;
+  const int e = ids[item];
+  return (e >= 0 && e < a.num_experts) ? e / a.epr : -1;
+}
+
+// Routing of one source is split over a cluster of up to 8 CTAs (grid x =
+// cluster rank, grid y = source); CTA c owns a contiguous segment of the
+// (token, choice) items.
+//
+// 1. Each CTA counts its segment's items per destination (__match_any_sync
+//    groups a warp's lanes by destination; one shared atomic per group).
+// 2. After a cluster barrier, CTA c adds up the counts of CTAs 0..c-1 from
+//    their shared memory (distributed shared memory), which is the number of
+//    earlier same-destination items of the source: its base.  The last CTA
+//    also writes the source's row of the p x p counts.
+// 3. The segment is walked in tiles of 4096 items, thread t holding items
+//    t, t + 1024, t + 2048, t + 3072 of the tile; in a warp, __match_any_sync
+//    gives every item its rank among the earlier same-destination lanes, the
+//    group leader stores the group's size in the (sub-tile, warp) row of a
+//    count table, and a warp-shuffle scan down each destination's column (in
+//    item order: sub-tile, then warp) on top of the running count turns the
+//    table into the number of earlier same-destination items: item's slot =
+//    table entry + its rank in the warp.
+// A second cluster barrier keeps every CTA's counts alive until the others
+// have read them.
+__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const __grid_constant__ MoeRouteArgs a,
+                                                                 uint64_t seg) {
+  namespace cg = cooperative_groups;
+  __shared__ int table[kRouteRows][kMoeMaxRanks + 1];  // +1: conflict-free column scan
+  __shared__ int hist[kMoeMaxRanks];
   __shared__ int run[kMoeMaxRanks];
   pdl_enter();
-  const int s = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int c = static_cast<int>(cluster.block_rank());
+  const int s = blockIdx.y;
   const int p = a.p;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int d = tid; d < p; d += kRouteThreads) run[d] = 0;
   const int32_t* ids = a.ids[s];
   int32_t* slots = a.slots[s];
-  for (uint64_t base = 0; base < a.items; base += kRouteThreads) {
-    for (int i = tid; i < 32 * p; i += kRouteThreads) warp_cnt[i / p][i % p] = 0;
-    __syncthreads();
-    const uint64_t item = base + tid;
-    int d = -1;
-    if (item < a.items) {
-      const int e = ids[item];
-      if (e >= 0 && e < a.num_experts) d = e / a.epr;
+  const uint64_t lo = min(static_cast<uint64_t>(c) * seg, a.items);
+  const uint64_t hi = min(lo + seg, a.items);
+  for (int d = tid; d < p; d += kRouteThreads) hist[d] = 0;
+  __syncthreads();
+
+  // 1. per-destination counts of the segment
+  for (uint64_t b = lo; b < hi; b += kRouteTile) {
+    int d[kRouteSub];
+#pragma unroll
+    for (int j = 0; j < kRouteSub; ++j) d[j] = route_dest(a, ids, b + j * kRouteThreads + tid, hi);
+#pragma unroll
+    for (int j = 0; j < kRouteSub; ++j) {
+      const unsigned same = __match_any_sync(0xFFFFFFFFu, d[j]);
+      if (d[j] >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[d[j]], __popc(same));
     }
-    const unsigned same = __match_any_sync(0xFFFFFFFFu, d);
-    const int rank = __popc(same & ((1u << lane) - 1u));
-    if (d >= 0 && rank == 0) warp_cnt[warp][d] = __popc(same);
-    __syncthreads();
-    if (tid < p) {
-      int acc = run[tid];
-      for (int w = 0; w < 32; ++w) {
-        const int c = warp_cnt[w][tid];
-        warp_cnt[w][tid] = acc;
-        acc += c;
-      }
-      run[tid] = acc;
-    }
-    __syncthreads();
-    if (item < a.items) slots[item] = (d >= 0) ? warp_cnt[warp][d] + rank : -1;
-    __syncthreads();
   }
-  if (tid < p) a.counts[static_cast<uint64_t>(s) * p + tid] = run[tid];
+  cluster.sync();
+
+  // 2. base = items of the same source and destination in earlier segments
+  if (tid < p) {
+    int base = 0;
+    for (int q = 0; q < c; ++q) base += cluster.map_shared_rank(hist, q)[tid];
+    run[tid] = base;
+    if (c == static_cast<int>(cluster.num_blocks()) - 1)
+      a.counts[static_cast<uint64_t>(s) * p + tid] = base + hist[tid];
+  }
+  cluster.barrier_arrive();
+  __syncthreads();
+
+  // 3. slots, tile by tile
+  for (uint64_t b = lo; b < hi; b += kRouteTile) {
+    int d[kRouteSub], rank[kRouteSub];
+#pragma unroll
+    for (int j = 0; j < kRouteSub; ++j) d[j] = route_dest(a, ids, b + j * kRouteThreads + tid, hi);
+    // this warp's rows are read only by this warp (slots of the previous
+    // tile) and by the scan, which a __syncthreads has closed
+    for (int i = lane; i < kRouteSub * p; i += 32) table[(i / p) * 32 + warp][i % p] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kRouteSub; ++j) {
+      const unsigned same = __match_any_sync(0xFFFFFFFFu, d[j]);
+      rank[j] = __popc(same & ((1u << lane) - 1u));
+      if (d[j] >= 0 && rank[j] == 0) table[j * 32 + warp][d[j]] = __popc(same);
+    }
+    __syncthreads();
+    for (int dd = warp; dd < p; dd += 32) {  // warp w scans columns w and w + 32
+      int acc = run[dd];
+#pragma unroll
+      for (int j = 0; j < kRouteSub; ++j) {
+        const int v = table[j * 32 + lane][dd];
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        table[j * 32 + lane][dd] = acc + incl - v;
+        acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      if (lane == 0) run[dd] = acc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRouteSub; ++j) {
+      const uint64_t item = b + j * kRouteThreads + tid;
+      if (item < hi) slots[item] = (d[j] >= 0) ? table[j * 32 + warp][d[j]] + rank[j] : -1;
+    }
+  }
+  cluster.barrier_wait();
 }
 
 constexpr int kTokensPerCta = 8;
@@ -254,7 +327,24 @@ __global__ void __launch_bounds__(kThreads) moe_combine_kernel(const __grid_cons
 }  // namespace
 
 cudaError_t launch_moe_route(const MoeRouteArgs& a, cudaStream_t s) {
-  cudaError_t err = launch_kernel(moe_route_kernel, dim3(a.p), dim3(kRouteThreads), s, a);
+  // cluster size: one CTA per 4096-item tile, up to 8; segments whole tiles
+  const uint64_t tiles = (a.items + kRouteTile - 1) / kRouteTile;
+  const unsigned cl = static_cast<unsigned>(tiles < 1 ? 1 : (tiles > kRouteMaxCluster ? kRouteMaxCluster : tiles));
+  const uint64_t seg = ((tiles + cl - 1) / cl) * kRouteTile;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cl, static_cast<unsigned>(a.p));
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = CCL_PDL ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cl;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, moe_route_kernel, a, seg);
   if (err == cudaSuccess) note_launch();
   return err;
 }

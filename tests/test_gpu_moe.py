@@ -41,11 +41,16 @@ def _run(lib, p, T, k, E, h, fp8, seed=0, bad_id=False):
     return ids, toks, d_ids, counts, c, slots, recv, scales, rexp
 
 
+# items = T * k: one 4096-item tile and under; 8 tiles (a cluster of 8 CTAs per
+# source, one tile each); 35,000 (9 tiles: two-tile segments, the last CTAs
+# empty, a ragged last tile); 200,000 (seven-tile segments); none at all
 @pytest.mark.parametrize("p,T,k,E", [(1, 10, 1, 4), (2, 300, 2, 8), (4, 1000, 4, 16), (8, 777, 8, 64),
-                                     (16, 200, 3, 32), (64, 50, 2, 128)])
+                                     (16, 200, 3, 32), (64, 50, 2, 128), (8, 4096, 8, 256),
+                                     (5, 7000, 5, 10), (2, 100000, 2, 8), (4, 0, 2, 8)])
 def test_route_matches_oracle(lib, p, T, k, E):
     ids = workloads.moe_topk_routing(p, T, k, E, seed=p)
-    ids[0][0, 0] = -1  # routes nowhere
+    if T:
+        ids[0][0, 0] = -1  # routes nowhere
     want_c, want_s, _ = moe.route([i.reshape(-1) for i in ids], p, E)
     counts = torch.empty(p * p, dtype=torch.int64, device="cuda")
     slots = [torch.empty(T, k, dtype=torch.int32, device="cuda") for _ in range(p)]
