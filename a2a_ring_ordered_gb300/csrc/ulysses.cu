@@ -6,77 +6,62 @@
 // Rank r holds sequence shard r with every head, [S/p, H, D]; after the
 // forward exchange it holds the whole sequence of head group r, [S, H/p, D]:
 //   y_r[s * S/p + t, h, :] = x_s[t, r * H/p + h, :].
-// The inverse exchange maps back.  Both are p * p * (S/p) contiguous segments
-// of (H/p) * D elements; one 1-D grid strides over the 16-byte vectors of all
-// segments (4 per thread in flight) -- a pure copy, bit-exact.
+// The inverse exchange maps back.  A token row of a shard (H * D elements) is
+// p contiguous segments of (H/p) * D elements, segment d going to rank d.  A
+// CTA takes a block of token rows of one shard: thread x walks the row's
+// 16-byte vectors o = x, x + blockDim.x, ...; the vector's segment d and
+// offset e in it are worked out once per o and serve every row, and the
+// rows (threadIdx.y + u * blockDim.y) are loaded together, kRows at a time,
+// before they are stored -- a pure copy, bit-exact, with both sides read or
+// written in runs of whole segments.
 #include "device_common.cuh"
 
 namespace ccl {
 namespace {
 
-constexpr int kUnroll = 4;
-
-// Source and destination byte addresses of element offset `i` (in vectors of
-// VEC elements) of segment `g`.
-template <int DT>
-__device__ __forceinline__ void segment_ends(const UlyssesArgs& a, uint64_t g, const char** src,
-                                             char** dst) {
-  constexpr int B = Elem<DT>::kBytes;
-  const uint64_t sp = a.seq_per_rank, hp = a.heads / a.p, D = a.head_dim;
-  const uint64_t t = g % sp;            // token within the shard
-  const uint64_t pair = g / sp;
-  const uint64_t d = pair % a.p;        // head group / destination rank
-  const uint64_t s = pair / a.p;        // sequence shard / source rank
-  const uint64_t shard_off = (t * a.heads + d * hp) * D;  // in the [S/p, H, D] shard
-  const uint64_t group_off = ((s * sp + t) * hp) * D;     // in the [S, H/p, D] head group
-  if (!a.inverse) {
-    *src = static_cast<const char*>(a.x[s]) + shard_off * B;
-    *dst = static_cast<char*>(a.y[d]) + group_off * B;
-  } else {
-    *src = static_cast<const char*>(a.x[d]) + group_off * B;
-    *dst = static_cast<char*>(a.y[s]) + shard_off * B;
-  }
-}
+constexpr int kRows = 8;  // rows per thread, loads in flight
 
 template <int DT, int VEC>
 __global__ void __launch_bounds__(kThreads) ulysses_kernel(const __grid_constant__ UlyssesArgs a) {
   constexpr int W = (VEC * Elem<DT>::kBytes + 3) / 4;
   pdl_enter();
-  const uint64_t L = (a.heads / a.p) * a.head_dim;  // elements per segment
-  const uint64_t vps = L / VEC;                      // vectors per segment
-  const uint64_t total = a.segments * vps;
-  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * kUnroll;
-  for (uint64_t base = static_cast<uint64_t>(blockIdx.x) * kSpan; base < total;
-       base += static_cast<uint64_t>(gridDim.x) * kSpan) {
-    uint32_t w[kUnroll][W];
-    char* dst[kUnroll];
-    uint64_t off[kUnroll];
+  const uint64_t sp = a.seq_per_rank;
+  const uint64_t R = a.heads * a.head_dim / VEC;             // vectors per shard row
+  const uint64_t G = (a.heads / a.p) * a.head_dim / VEC;     // vectors per segment
+  const uint64_t s = blockIdx.y;                              // sequence shard
+  const uint64_t rows_per_cta = static_cast<uint64_t>(blockDim.y) * kRows;
+  const uint64_t t0 = blockIdx.x * rows_per_cta + threadIdx.y;
+  for (uint64_t o = threadIdx.x; o < R; o += blockDim.x) {
+    const uint64_t d = o / G, e = o - d * G;
+    // element offsets of row t0: in the [S/p, H, D] shard and in rank d's [S, H/p, D] group
+    const uint64_t shard0 = (t0 * R + o) * VEC;
+    const uint64_t group0 = ((s * sp + t0) * G + e) * VEC;
+    const void* src = a.inverse ? a.x[d] : a.x[s];
+    void* dst = a.inverse ? a.y[s] : a.y[d];
+    const uint64_t src0 = a.inverse ? group0 : shard0, dst0 = a.inverse ? shard0 : group0;
+    const uint64_t src_step = (a.inverse ? G : R) * VEC * blockDim.y;
+    const uint64_t dst_step = (a.inverse ? R : G) * VEC * blockDim.y;
+    uint32_t w[kRows][W];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
-      dst[u] = nullptr;
-      if (v < total) {
-        const char* src;
-        segment_ends<DT>(a, v / vps, &src, &dst[u]);
-        off[u] = (v % vps) * VEC;
-        load_raw<DT, VEC>(src, off[u], w[u]);
-      }
-    }
+    for (int u = 0; u < kRows; ++u)
+      if (t0 + static_cast<uint64_t>(u) * blockDim.y < sp) load_raw<DT, VEC>(src, src0 + u * src_step, w[u]);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (dst[u] != nullptr) store_raw<DT, VEC>(dst[u], off[u], w[u]);
+    for (int u = 0; u < kRows; ++u)
+      if (t0 + static_cast<uint64_t>(u) * blockDim.y < sp) store_raw<DT, VEC>(dst, dst0 + u * dst_step, w[u]);
   }
 }
 
 template <int DT, int VEC>
 cudaError_t launch_one(const UlyssesArgs& a, cudaStream_t s) {
-  const uint64_t L = (a.heads / a.p) * a.head_dim;
-  const uint64_t total = a.segments * (L / VEC);
-  constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * kUnroll;
-  uint64_t gx = (total + kSpan - 1) / kSpan;
-  if (gx < 1) gx = 1;
-  if (gx > (1u << 30)) gx = 1u << 30;
-  return launch_kernel(ulysses_kernel<DT, VEC>, dim3(static_cast<unsigned>(gx)), dim3(kThreads), s, a);
+  const uint64_t R = a.heads * a.head_dim / VEC;
+  // x covers the row's vectors (whole warps), y the rows that fit beside them
+  unsigned bx = kThreads;
+  if (R < kThreads) bx = static_cast<unsigned>((R + 31) / 32 * 32);
+  const unsigned by = kThreads / bx;
+  const uint64_t rows_per_cta = static_cast<uint64_t>(by) * kRows;
+  const uint64_t gx = (a.seq_per_rank + rows_per_cta - 1) / rows_per_cta;
+  if (gx > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+  return launch_kernel(ulysses_kernel<DT, VEC>, dim3(static_cast<unsigned>(gx), a.p), dim3(bx, by), s, a);
 }
 
 }  // namespace

@@ -470,6 +470,69 @@ def test_schedule_argument_errors(lib):
         lib.ccl_allreduce_schedule(x, [torch.empty_like(t) for t in x], "naive", op="max")
 
 
+# ------------------------------------------- hierarchical / 2-D two-level ring
+# (p, group, n): 2 nodes x 8, 4 x 2, 3 x 3 with sub-chunks that start off the
+# 16-byte grid, one group (the flat ring), groups of one, tiny n (empty
+# sub-chunks), 9 x 8 = 72 ranks
+HIER_CASES = [(16, 8, 65536 + 7), (8, 2, 70001), (9, 3, 1001), (6, 6, 4099), (6, 1, 4099),
+              (4, 2, 3), (72, 8, 1000), (2, 1, 4096 * 4 + 5)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,group,n", HIER_CASES)
+def test_hierarchical_allreduce_matches_oracle(lib, dtype, p, group, n):
+    from oracle import schedules
+
+    x = make_inputs(dtype, p, n, seed=p + 7 * n + group)
+    want, _ = schedules.hierarchical(x, group, dtype)
+    outs = guarded_outputs(p, [n] * p, dtype)
+    lib.ccl_allreduce_hierarchical([to_dev(v, dtype) for v in x], [o.view for o in outs], group)
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"hierarchical p={p} a={group} rank {r}")
+        assert outs[r].guards_intact()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_hierarchical_unaligned_and_in_place(lib, dtype):
+    from oracle import schedules
+
+    p, group, n = 8, 4, 10007
+    x = make_inputs(dtype, p, n, seed=11)
+    want, _ = schedules.hierarchical(x, group, dtype)
+    ins = [Guarded(n, dtype, offset=GUARD + 1) for _ in range(p)]  # off the 16-byte grid
+    for g, v in zip(ins, x):
+        g.view.copy_(to_dev(v, dtype))
+    lib.ccl_allreduce_hierarchical([g.view for g in ins], [g.view for g in ins], group)  # in place
+    for r in range(p):
+        assert_equal(to_host(ins[r].view), want[r], dtype, f"in place rank {r}")
+        assert ins[r].guards_intact()
+
+
+def test_hierarchical_hand_cases_on_gpu(lib):
+    """The hand-derived fold orders of tests/test_oracle_schedules.py, on
+    vectors long enough for the 16-byte path."""
+    cases = [(3, [-(2.0**24), 2.0**24, 1.0, 0.0, 0.0, 0.0]), (2, [-(2.0**24), 0.0, 2.0**24, 0.0, 1.0, 0.0])]
+    n = 6 * 1024
+    for group, vals in cases:
+        send = [torch.full((n,), v, device="cuda") for v in vals]
+        recv = [torch.empty(n, device="cuda") for _ in range(6)]
+        lib.ccl_allreduce_hierarchical(send, recv, group)
+        from oracle import schedules
+        want, _ = schedules.hierarchical([to_host(t) for t in send], group)
+        for r in range(6):
+            np.testing.assert_array_equal(to_host(recv[r]), want[r])
+        assert set(np.unique(to_host(recv[0])).tolist()) == {0.0, 1.0}
+
+
+def test_hierarchical_argument_errors(lib):
+    x = [torch.ones(8, device="cuda") for _ in range(6)]
+    for bad in (0, 4, 7):
+        with pytest.raises(lib.CclError):
+            lib.ccl_allreduce_hierarchical(x, [torch.empty_like(t) for t in x], bad)
+    with pytest.raises(lib.CclError):
+        lib.ccl_allreduce_hierarchical(x, [torch.empty_like(t) for t in x], 3, op="max")
+
+
 # ---------------------------------------- broadcast / reduce / scatter / gather
 ROOTED = [(1, 10), (3, 1001), (4, 4), (8, 70001), (16, 65543), (72, 1000)]
 
@@ -560,8 +623,11 @@ def test_bucket_reads_and_writes_pinned_host_memory(lib):
 
 # ------------------------------------------------ Ulysses head <-> sequence
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+# rows of 8 KB and over (x covers 256 vectors), rows under 256 vectors (2-D
+# blocks), 30 vectors a row (a part-idle warp), unaligned segments (scalar
+# path), ragged row blocks (sp = 33, 50, 1001)
 @pytest.mark.parametrize("p,sp,H,D", [(1, 5, 4, 8), (2, 64, 8, 64), (4, 33, 16, 128), (8, 128, 32, 128),
-                                      (4, 7, 4, 3)])
+                                      (4, 7, 4, 3), (2, 50, 6, 20), (8, 1001, 32, 128)])
 def test_ulysses_all_to_all_matches_oracle(lib, dtype, p, sp, H, D):
     n = sp * H * D
     x = make_inputs(dtype, p, n, seed=p * 7 + sp)
