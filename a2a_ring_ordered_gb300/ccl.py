@@ -49,6 +49,7 @@ def _load() -> ctypes.CDLL:
         "ccl_chunk_bounds": (st, [i32, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
         "ccl_allreduce": (st, [pp, pp, i32, sz, i32, i32, vp]),
         "ccl_allreduce_schedule": (st, [pp, pp, i32, sz, i32, i32, i32, vp]),
+        "ccl_allreduce_hierarchical": (st, [pp, pp, i32, i32, sz, i32, i32, vp]),
         "ccl_reduce_scatter": (st, [pp, pp, i32, sz, i32, i32, vp]),
         "ccl_all_gather": (st, [pp, pp, i32, sz, i32, vp]),
         "ccl_broadcast": (st, [vp, pp, i32, sz, i32, i32, vp]),
@@ -225,6 +226,22 @@ def ccl_allreduce_schedule(send, recv, schedule: str = "ring", op: str = "sum", 
                                       _dtype_code(send[0]), _op_code(op), SCHEDULES[schedule],
                                       _stream(stream, send[0].device)),
            "ccl_allreduce_schedule")
+
+
+def ccl_allreduce_hierarchical(send, recv, group: int, op: str = "sum", stream=None) -> None:
+    """All-reduce with the bits of the two-level ring: groups of `group`
+    consecutive ranks, a ring inside every group, then a ring over the groups."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    if len(recv) != p or recv[0].dtype != send[0].dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [n] * p, "recv")
+    _check(LIB.ccl_allreduce_hierarchical(_ptr_array([t.data_ptr() for t in send]),
+                                          _ptr_array([t.data_ptr() for t in recv]), p, int(group), n,
+                                          _dtype_code(send[0]), _op_code(op),
+                                          _stream(stream, send[0].device)),
+           "ccl_allreduce_hierarchical")
 
 
 def ccl_reduce_scatter(send, recv, op: str = "sum", stream=None) -> None:

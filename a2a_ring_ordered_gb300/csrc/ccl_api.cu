@@ -284,6 +284,33 @@ extern "C" ccl_status_t ccl_allreduce_schedule(const void* const* send, void* co
   return CCL_OK;
 }
 
+extern "C" ccl_status_t ccl_allreduce_hierarchical(const void* const* send, void* const* recv, int p,
+                                                   int group, size_t n, ccl_dtype_t dt, ccl_op_t op,
+                                                   void* stream) {
+  clear_error();
+  ccl_status_t st = check_reduce(0, send, recv, p, n, dt, op);
+  if (st != CCL_OK) return st;
+  if (group < 1 || p % group != 0)
+    return fail(CCL_ERR_INVALID_ARG, "group=%d must divide p=%d", group, p);
+  if (op != CCL_SUM)
+    return fail(CCL_ERR_UNSUPPORTED, "the hierarchical fold is implemented for SUM only");
+  if (n == 0) return CCL_OK;
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.send[r] = send[r];
+    a.recv[r] = recv[r];
+  }
+  a.p = p;
+  a.q = n / static_cast<uint64_t>(group);
+  a.rem = n % static_cast<uint64_t>(group);
+  a.scale = 1.0f;
+  const bool vec = all_aligned16(send, p, const_cast<const void* const*>(recv));
+  cudaError_t err = launch_hier_fold(dt, vec, a, group, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "hierarchical fold kernel launch");
+  return CCL_OK;
+}
+
 extern "C" ccl_status_t ccl_reduce_scatter(const void* const* send, void* const* recv, int p,
                                            size_t n, ccl_dtype_t dt, ccl_op_t op, void* stream) {
   clear_error();

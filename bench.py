@@ -137,6 +137,9 @@ class ClockSampler:
 # ---------------------------------------------------------------- workloads
 KERNEL_SOURCES = {
     "fold": ["a2a_ring_ordered_gb300/csrc/fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
+    "schedule": ["a2a_ring_ordered_gb300/csrc/schedule_fold.cu",
+                 "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
+    "hier": ["a2a_ring_ordered_gb300/csrc/hier_fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "gather": ["a2a_ring_ordered_gb300/csrc/gather.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "a2av": ["a2a_ring_ordered_gb300/csrc/a2av.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "ring_step": ["a2a_ring_ordered_gb300/csrc/ring_step.cu",
@@ -299,23 +302,34 @@ class Bucket(Workload):
 class AllReduce(Workload):
     kernel = "fold"
 
-    def __init__(self, p=16, mib=256, dtype="f32", seed=4, op="sum", literal=False, schedule="ring"):
+    def __init__(self, p=16, mib=256, dtype="f32", seed=4, op="sum", literal=False, schedule="ring",
+                 group=8):
         self.p, self.dtype, self.seed, self.op, self.literal = p, dtype, seed, op, literal
         self.schedule = schedule
+        self.group = group if schedule == "hierarchical" else None
+        if self.group is not None and (group < 1 or p % group):
+            raise SystemExit(f"--group {group} must divide --p {p}")
         self.e = 4 if dtype == "f32" else 2
         self.n = mib * (1 << 20) // self.e
         self.mib = mib
         self.name = "ring_allreduce_literal" if literal else "allreduce"
-        self.kernel = "ring_step" if literal else "fold"
-        self.kernel_key = f"{'ring_step' if literal else 'fold'}_ar_{dtype}_p{p}_n{self.n}"
+        self.kernel = ("ring_step" if literal else "fold" if schedule == "ring"
+                       else "hier" if schedule == "hierarchical" else "schedule")
+        tag = "" if schedule == "ring" else f"_{schedule}" + (f"_g{group}" if self.group else "")
+        self.kernel_key = f"{self.kernel}_ar{tag}_{dtype}_p{p}_n{self.n}"
         # literal engine: set-up move + (p-1) reduce-scatter steps + (bf16: rounding
         # move) + (p-1) all-gather steps
         self.launches_per_step = (2 * p - 1 + (1 if dtype == "bf16" else 0)) if literal else 1
 
     def config(self):
         kind = "literal ring" if self.literal else f"fused {self.schedule.replace('_', ' ')}"
-        return {"workload": f"{kind} all-reduce: p={self.p} ranks x {self.mib} MiB {self.dtype} per rank",
-                "p": self.p, "n_per_rank": self.n, "inputs": f"U(-1,1) seed {self.seed}"}
+        if self.group is not None:
+            kind += f" ({self.p // self.group} groups of {self.group})"
+        cfg = {"workload": f"{kind} all-reduce: p={self.p} ranks x {self.mib} MiB {self.dtype} per rank",
+               "p": self.p, "n_per_rank": self.n, "inputs": f"U(-1,1) seed {self.seed}"}
+        if self.group is not None:
+            cfg["group"] = self.group
+        return cfg
 
     def bytes_per_step(self):
         return 2 * self.p * self.n * self.e
@@ -335,6 +349,11 @@ class AllReduce(Workload):
 
     def oracle_sample(self, frac):
         from oracle import ring, schedules
+        if self.schedule == "hierarchical":
+            return oracle_prefix_sample(
+                self.send, self.n, frac,
+                lambda xs: schedules.hierarchical(xs, self.group, self.dtype, self.op),
+                2 * self.p * self.e, f"oracle hierarchical all-reduce, groups of {self.group}")
         if self.schedule != "ring":
             return oracle_prefix_sample(
                 self.send, self.n, frac,
@@ -348,6 +367,9 @@ class AllReduce(Workload):
         if self.literal:
             self.lib.ccl_ring_allreduce_literal(self.send, self.recv, op=self.op,
                                                 workspace=self.ws, stream=stream)
+        elif self.schedule == "hierarchical":
+            self.lib.ccl_allreduce_hierarchical(self.send, self.recv, self.group, op=self.op,
+                                                stream=stream)
         elif self.schedule != "ring":
             self.lib.ccl_allreduce_schedule(self.send, self.recv, self.schedule, op=self.op,
                                             stream=stream)
@@ -767,7 +789,8 @@ def make_workload(a) -> Workload:
     if a.workload == "bucket":
         return Bucket()
     if a.workload == "allreduce":
-        return AllReduce(p=a.p or 16, mib=a.mib or 256, dtype=a.dtype, schedule=a.schedule)
+        return AllReduce(p=a.p or 16, mib=a.mib or 256, dtype=a.dtype, schedule=a.schedule,
+                         group=a.group)
     if a.workload == "literal":
         return AllReduce(p=a.p or 8, mib=a.mib or 25, dtype=a.dtype, literal=True)
     if a.workload == "reduce_scatter":
@@ -893,28 +916,49 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
         wl.step(stream)
     w1.record(stream)
     torch.cuda.synchronize(device)
-    if a.steps <= 0:  # auto: about one second of timed device work
-        ms_warm = w0.elapsed_time(w1) / a.warmup
-        a.steps = int(max(64, min(200000, round(1000.0 / max(ms_warm, 1e-3)))))
-        a.steps = -(-a.steps // 64) * 64  # a multiple of the graph's 64 steps
-        a.steps = int(max_over_ranks(float(a.steps), world, device))
+
+    def capture(g):
+        """A CUDA graph of g steps, replayed once (warm)."""
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap):
+            for _ in range(g):
+                wl.step(cap)
+        stream.wait_stream(cap)
+        with torch.cuda.stream(stream):
+            gr.replay()
+        torch.cuda.synchronize(device)
+        return gr
 
     # The timed steps replay a CUDA graph of G steps (G divides K), so that the
     # host cost of issuing a call never leaves the GPU idle between steps;
     # --eager issues every step from Python instead.
     graph, group = None, 1
-    if not a.eager:
-        group = max(d for d in range(1, min(a.steps, 64) + 1) if a.steps % d == 0)
-        cap = torch.cuda.Stream(device)
-        cap.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=cap):
-            for _ in range(group):
-                wl.step(cap)
-        stream.wait_stream(cap)
-        with torch.cuda.stream(stream):
-            graph.replay()
+    if a.steps <= 0:  # auto: about one second of timed device work, from warm steps
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if a.eager:
+            p0.record(stream)
+            for _ in range(20):
+                wl.step(stream)
+            p1.record(stream)
+            probe = 20
+        else:
+            graph, group = capture(64), 64
+            p0.record(stream)
+            with torch.cuda.stream(stream):
+                graph.replay()
+                graph.replay()
+            p1.record(stream)
+            probe = 128
         torch.cuda.synchronize(device)
+        ms_probe = p0.elapsed_time(p1) / probe
+        a.steps = int(max(64, min(200000, round(1000.0 / max(ms_probe, 1e-3)))))
+        a.steps = -(-a.steps // 64) * 64  # a multiple of the graph's 64 steps
+        a.steps = int(max_over_ranks(float(a.steps), world, device))
+    if not a.eager and graph is None:
+        group = max(d for d in range(1, min(a.steps, 64) + 1) if a.steps % d == 0)
+        graph = capture(group)
     sampler = ClockSampler(local)
     time.sleep(0.05)
     launches0 = lib.ccl_kernel_launch_count()
@@ -1148,8 +1192,11 @@ def main(argv=None) -> int:
     ap.add_argument("--mib", type=int, default=0)
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--schedule", default="ring",
-                    choices=["ring", "recursive_doubling", "rabenseifner", "binomial_tree", "naive"],
+                    choices=["ring", "recursive_doubling", "rabenseifner", "binomial_tree", "naive",
+                             "hierarchical"],
                     help="fold order of --workload allreduce")
+    ap.add_argument("--group", type=int, default=8,
+                    help="ranks per group of --schedule hierarchical (groups of consecutive ranks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="issue every timed step from Python instead of replaying a CUDA graph")

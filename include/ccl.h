@@ -128,6 +128,22 @@ ccl_status_t ccl_allreduce_schedule(const void* const* send, void* const* recv, 
                                     ccl_dtype_t dt, ccl_op_t op, ccl_schedule_t schedule,
                                     void* stream);
 
+/* All-reduce with the result of the hierarchical (two-level ring) all-reduce
+ * ("Networks and Collective Communication" 6.3; 6.1's two-dimensional
+ * all-reduce on an a x b grid folds the same way), in one fused pass (same
+ * buffers and aliasing rules as ccl_allreduce).
+ *   group   a, the ranks per group; groups are runs of consecutive ranks
+ *           (group g = ranks g*a .. g*a + a - 1), b = p / a groups.
+ * The buffer is cut into a chunks (chunk rule), chunk l into b sub-chunks; an
+ * element of sub-chunk (l, m) is folded along every group's ring starting at
+ * local rank l + 1, then along the ring over the groups starting at group
+ * m + 1, in fp32 (int32), bf16 rounded once.  group == p or group == 1 gives
+ * ccl_allreduce's bits.  Errors: group < 1 or not dividing p ->
+ * CCL_ERR_INVALID_ARG; MAX / MIN -> CCL_ERR_UNSUPPORTED (order-free: use
+ * ccl_allreduce). */
+ccl_status_t ccl_allreduce_hierarchical(const void* const* send, void* const* recv, int p, int group,
+                                        size_t n, ccl_dtype_t dt, ccl_op_t op, void* stream);
+
 /* Reduce-scatter ("dist_train": process k gets sum_i x_i^(k); ZeRO's key op).
  *   send[r]  p device pointers, each n elements.
  *   recv[k]  p device pointers; recv[k] holds len(k) elements: chunk k of the
