@@ -84,3 +84,49 @@ def bucket_at(grads: list[np.ndarray], idx: np.ndarray, scale: float):
     """DDP bucket output (any rank) at the given indices: bf16(fold * scale)."""
     acc = fold_at(grads, idx, "f32", "sum")
     return f32_to_bf16_rne(acc * np.float32(scale))
+
+
+def hierarchical_at_columns(cols: list[np.ndarray], idx: np.ndarray, n: int, group: int,
+                            dtype: str = "f32"):
+    """The two-level ring fold ("Networks and Collective Communication"
+    sections 6.3 and 6.1; the readings of ``oracle.schedules.hierarchical``)
+    at indices ``idx``, in the output dtype: element i lies in chunk l of the
+    a = group chunks and in sub-chunk m of that chunk's b = p / a pieces; each
+    group's value is its ring fold from local rank l + 1 to l, and the group
+    values are folded from group m + 1 to m.  Checked against the literal
+    simulation in ``tests/test_oracle_schedules.py``."""
+    p = len(cols)
+    a = int(group)
+    if a < 1 or p % a:
+        raise ValueError("group must divide p")
+    b = p // a
+    idx = np.asarray(idx, dtype=np.int64)
+    acc_dtype = np.int32 if dtype == "i32" else np.float32
+    out = np.empty(idx.shape, dtype=acc_dtype)
+    level1 = chunk_bounds(a, n)
+    l_of = chunk_of(a, n, idx)
+
+    def value(rank, mask):
+        v = cols[rank][mask]
+        return bf16_to_f32(v) if dtype == "bf16" else v.astype(acc_dtype, copy=True)
+
+    for l in range(a):
+        in_l = l_of == l
+        if not in_l.any():
+            continue
+        off, ln = level1[l]
+        m_of = np.full(idx.shape, -1, dtype=np.int64)
+        m_of[in_l] = chunk_of(b, ln, idx[in_l] - off)
+        for m in range(b):
+            mask = in_l & (m_of == m)
+            if not mask.any():
+                continue
+            tot = None
+            for gi in range(1, b + 1):
+                g = (m + gi) % b
+                part = value(g * a + (l + 1) % a, mask)
+                for li in range(2, a + 1):
+                    part = combine(part, value(g * a + (l + li) % a, mask), "sum")
+                tot = part if tot is None else combine(tot, part, "sum")
+            out[mask] = tot
+    return f32_to_bf16_rne(out) if dtype == "bf16" else out

@@ -524,6 +524,35 @@ def test_hierarchical_hand_cases_on_gpu(lib):
         assert set(np.unique(to_host(recv[0])).tolist()) == {0.0, 1.0}
 
 
+@pytest.mark.parametrize("p,group,mib", [(16, 8, 256), (72, 8, 128)])
+def test_hierarchical_full_size_sampled(lib, p, group, mib):
+    """The bench's hierarchical configurations (fp32, U(-1, 1) drawn on the
+    device with torch's seeded generator): sampled elements against the
+    pointwise two-level fold; all ranks identical on the device."""
+    from oracle import pointwise
+
+    n = mib * (1 << 20) // 4
+    b = p // group
+    edges = []
+    for off, ln in ring.chunk_bounds(group, n):  # every sub-chunk's first and last element
+        for o2, l2 in ring.chunk_bounds(b, ln):
+            edges += [off + o2, off + o2 + max(l2 - 1, 0)]
+    idx = np.unique(np.concatenate([sample_indices(n, p, 1 << 17, seed=p + group),
+                                    np.array(edges, dtype=np.int64)]))
+    idx_t = torch.from_numpy(idx).cuda()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4)
+    send = [torch.rand(n, generator=gen, device="cuda") * 2.0 - 1.0 for _ in range(p)]
+    cols = [to_host(v[idx_t]) for v in send]
+    recv = [torch.empty_like(v) for v in send]
+    lib.ccl_allreduce_hierarchical(send, recv, group)
+    want = pointwise.hierarchical_at_columns(cols, idx, n, group, "f32")
+    for r in (0, group, p - 1):
+        assert_equal(to_host(recv[r][idx_t]), want, "f32", f"hierarchical {mib} MiB p={p} rank {r}")
+    for r in range(1, p):
+        assert torch.equal(recv[r].view(torch.int32), recv[0].view(torch.int32))
+
+
 def test_hierarchical_argument_errors(lib):
     x = [torch.ones(8, device="cuda") for _ in range(6)]
     for bad in (0, 4, 7):
@@ -622,10 +651,28 @@ def test_bucket_reads_and_writes_pinned_host_memory(lib):
 
 
 # ------------------------------------------------ Ulysses head <-> sequence
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ulysses_full_size(lib):
+    """The bench's Ulysses configuration (p=8, 8192 tokens x 32 heads x 128
+    bf16 per rank), every element, forward and inverse."""
+    p, sp, H, D = 8, 8192, 32, 128
+    n = sp * H * D
+    x = workloads.normal(p, n, 1.0, 17, dtype="bf16")
+    want = collectives.ulysses_seq_to_heads(x, H, D)
+    send = [to_dev(v, "bf16") for v in x]
+    recv = [torch.empty_like(t) for t in send]
+    lib.ccl_all_to_all_heads(send, recv, sp, H, D)
+    for r in range(p):
+        assert_equal(to_host(recv[r]), want[r], "bf16", f"heads rank {r}")
+    back = [torch.empty_like(t) for t in send]
+    lib.ccl_all_to_all_heads(recv, back, sp, H, D, inverse=True)
+    for r in range(p):
+        assert torch.equal(back[r], send[r])
+
+
 # rows of 8 KB and over (x covers 256 vectors), rows under 256 vectors (2-D
 # blocks), 30 vectors a row (a part-idle warp), unaligned segments (scalar
 # path), ragged row blocks (sp = 33, 50, 1001)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("p,sp,H,D", [(1, 5, 4, 8), (2, 64, 8, 64), (4, 33, 16, 128), (8, 128, 32, 128),
                                       (4, 7, 4, 3), (2, 50, 6, 20), (8, 1001, 32, 128)])
 def test_ulysses_all_to_all_matches_oracle(lib, dtype, p, sp, H, D):

@@ -189,3 +189,19 @@ def test_hierarchical_bytes_section_6_3():
 def test_hierarchical_group_must_divide_p():
     with pytest.raises(ValueError):
         schedules.hierarchical(workloads.normal(6, 10, 1.0, 0), 4)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,group,n", [(6, 3, 23), (6, 2, 100), (16, 8, 1001), (8, 4, 5), (12, 1, 37),
+                                       (12, 12, 37), (9, 3, 2)])
+def test_pointwise_hierarchical_matches_the_literal_simulation(dtype, p, group, n):
+    from oracle import pointwise
+    x = (workloads.integer_valued(p, n, 2, lo=-2**30, hi=2**30, dtype="i32") if dtype == "i32"
+         else workloads.normal(p, n, 1.0, 2, dtype=dtype))
+    want, _ = schedules.hierarchical(x, group, dtype)
+    idx = np.arange(n)
+    got = pointwise.hierarchical_at_columns([v[idx] for v in x], idx, n, group, dtype)
+    np.testing.assert_array_equal(got, want[0])
+    sub = np.array([0, n - 1, n // 2], dtype=np.int64)
+    got = pointwise.hierarchical_at_columns([v[sub] for v in x], sub, n, group, dtype)
+    np.testing.assert_array_equal(got, want[0][sub])
