@@ -123,6 +123,7 @@ struct MoeDispatchArgs {
   uint64_t cap[kMoeMaxRanks];         // rows each recv[d] holds
   uint64_t tokens, hidden;
   int p, k, epr, num_experts, rexp_given;
+  int tpc;                            // tokens per CTA (set by the launcher)
 };
 struct MoeCombineArgs {
   const void* y[kMoeMaxRanks];        // rows x hidden bf16, dispatch layout
@@ -134,6 +135,7 @@ struct MoeCombineArgs {
   uint64_t cap[kMoeMaxRanks];         // rows each y[d] holds
   uint64_t tokens, hidden;
   int p, k, epr, num_experts;
+  int tpc;                            // tokens per CTA (set by the launcher)
 };
 static_assert(sizeof(MoeDispatchArgs) <= 4096, "MoE dispatch parameters exceed 4 KB");
 static_assert(sizeof(MoeCombineArgs) <= 4096, "MoE combine parameters exceed 4 KB");

@@ -78,7 +78,7 @@ __device__ __forceinline__ void write_all(const FoldArgs& f, uint64_t i, typenam
 
 // f.q, f.rem: the level-1 split, floor(n / a) and n mod a.
 template <int DT, int VEC>
-__global__ void __launch_bounds__(kThreads) hier_fold_kernel(const __grid_constant__ FoldArgs f, int a, int b) {
+__global__ void __launch_bounds__(kThreads, 2) hier_fold_kernel(const __grid_constant__ FoldArgs f, int a, int b) {
   using Acc = typename Elem<DT>::Acc;
   pdl_enter();
   const int l = static_cast<int>(blockIdx.y) / b;

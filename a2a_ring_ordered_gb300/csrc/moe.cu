@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const __grid_c
   cluster.barrier_wait();
 }
 
-constexpr int kTokensPerCta = 8;
+constexpr int kMaxTokensPerCta = 16;
 
 // base[d] = rows of destination d sent by sources before s.
 __device__ __forceinline__ void row_bases(const int64_t* counts, int p, int s, int64_t* base) {
@@ -147,78 +147,107 @@ __device__ __forceinline__ void row_bases(const int64_t* counts, int p, int s, i
   }
 }
 
-// One CTA per (tile of tokens, source).  Each 16-byte vector of a token row
-// (8 bf16) is loaded once and stored to the k destinations.  FP8: 16
-// elements per thread, and the 8 threads holding a 128-element block (vectors
-// are handed out so that 8 consecutive threads hold one block) reduce its amax
-// with shuffles;
-// inv = 448 / amax, code = e4m3(x * inv), round to nearest even, saturating;
-// the block scale amax / 448 is stored for dequantisation.
-template <bool FP8>
-__global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_constant__ MoeDispatchArgs a) {
-  __shared__ int64_t base[kMoeMaxRanks];
-  __shared__ int64_t pos[kTokensPerCta][kMoeMaxK];
-  __shared__ int dest[kTokensPerCta][kMoeMaxK];
-  __shared__ int expert[kTokensPerCta][kMoeMaxK];
-  pdl_enter();
-  const int s = blockIdx.y;
-  const int p = a.p, k = a.k;
-  const uint64_t t0 = static_cast<uint64_t>(blockIdx.x) * kTokensPerCta;
-  row_bases(a.counts, p, s, base);
-  __syncthreads();
-  for (int i = threadIdx.x; i < kTokensPerCta * k; i += kThreads) {
-    const int tt = i / k, j = i % k;
+// Destination rank and row of each (token, choice) of the CTA's tokens; -1
+// when the id is out of range, the item was not routed, or the row lies past
+// the destination buffer's capacity (a short buffer loses rows, never memory).
+// Combine also gathers each choice's gate weight (`weights` non-NULL).
+template <typename Args>
+__device__ __forceinline__ void token_rows(const Args& a, int s, uint64_t t0, int tpc, const int64_t* base,
+                                           int (*dest)[kMoeMaxK], int64_t (*pos)[kMoeMaxK],
+                                           int (*expert)[kMoeMaxK], const float* const* weights,
+                                           float (*wt)[kMoeMaxK]) {
+  const int k = a.k;
+  for (int i = threadIdx.x; i < tpc * k; i += blockDim.x) {
+    const int tt = i / k, j = i - (i / k) * k;
     const uint64_t t = t0 + tt;
-    int d = -1;
+    int d = -1, e = -1;
     int64_t row = -1;
-    int e = -1;
     if (t < a.tokens) {
       e = a.ids[s][t * k + j];
       const int slot = a.slots[s][t * k + j];
+      if (weights != nullptr) wt[tt][j] = weights[s][t * k + j];
       if (e >= 0 && e < a.num_experts && slot >= 0) {
         d = e / a.epr;
         row = base[d] + slot;
-        if (static_cast<uint64_t>(row) >= a.cap[d]) d = -1;  // never write past a buffer
+        if (static_cast<uint64_t>(row) >= a.cap[d]) d = -1;
       }
     }
     dest[tt][j] = d;
     pos[tt][j] = row;
-    expert[tt][j] = e;
+    if (expert != nullptr) expert[tt][j] = e;
   }
+}
+
+// One CTA per (tpc tokens, source).  The CTA's (token, vector) items are one
+// flat index range, U items per thread with their loads issued together, and
+// tpc is chosen so that the range is a whole number of passes (no idle lanes
+// in the last one).  Each vector of a token row is loaded once and stored to
+// the token's k destination rows.  bf16: 8 elements (16 bytes) per item.
+// FP8: 16 elements per item, and the 8 consecutive lanes holding a
+// 128-element block reduce its amax with shuffles (a row is a multiple of 128
+// elements, so an aligned group of 8 items never straddles two blocks or two
+// tokens); inv = 448 / amax, code = e4m3(x * inv) rounded to nearest even and
+// saturating; the block scale amax / 448 is stored for dequantisation.
+template <bool FP8, int U>
+__global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_constant__ MoeDispatchArgs a) {
+  constexpr int EPI = FP8 ? 16 : 8;  // elements per item
+  constexpr int WI = EPI / 2;        // 32-bit words of bf16 input per item
+  __shared__ int64_t base[kMoeMaxRanks];
+  __shared__ int64_t pos[kMaxTokensPerCta][kMoeMaxK];
+  __shared__ int dest[kMaxTokensPerCta][kMoeMaxK];
+  __shared__ int expert[kMaxTokensPerCta][kMoeMaxK];
+  pdl_enter();
+  const int s = blockIdx.y;
+  const int k = a.k, tpc = a.tpc;
+  const uint64_t t0 = static_cast<uint64_t>(blockIdx.x) * tpc;
+  row_bases(a.counts, a.p, s, base);
   __syncthreads();
+  token_rows(a, s, t0, tpc, base, dest, pos, expert, nullptr, static_cast<float (*)[kMoeMaxK]>(nullptr));
+  __syncthreads();
+  if (a.rexp_given) {
+    for (int i = threadIdx.x; i < tpc * k; i += kThreads) {
+      const int tt = i / k, j = i - (i / k) * k;
+      const int d = dest[tt][j];
+      if (d >= 0 && a.rexp[d] != nullptr) a.rexp[d][pos[tt][j]] = expert[tt][j];
+    }
+  }
   const uint64_t h = a.hidden;
-  const uint64_t nvec = h / 8;
-  for (int tt = 0; tt < kTokensPerCta; ++tt) {
-    const uint64_t t = t0 + tt;
-    if (t >= a.tokens) break;
-    const char* src = static_cast<const char*>(a.x[s]) + t * h * 2;
-    if constexpr (!FP8) {
-      for (uint64_t v = threadIdx.x; v < nvec; v += kThreads) {
-        uint32_t w[4];
-        load_raw<kBF16, 8>(src, v * 8, w);
-        for (int j = 0; j < k; ++j) {
-          const int d = dest[tt][j];
-          if (d >= 0) store_raw<kBF16, 8>(a.recv[d], static_cast<uint64_t>(pos[tt][j]) * h + v * 8, w);
-        }
+  const uint32_t nv = static_cast<uint32_t>(h / EPI);  // items per token row
+  const uint64_t left = a.tokens - t0;
+  const uint32_t ntok = static_cast<uint32_t>(left < static_cast<uint64_t>(tpc) ? left : tpc);
+  const uint32_t total = ntok * nv;
+  const char* xs = static_cast<const char*>(a.x[s]);
+  for (uint32_t f0 = threadIdx.x; f0 < total; f0 += kThreads * U) {
+    uint32_t w[U][WI];
+    uint32_t tt[U], v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t f = f0 + u * kThreads;
+      tt[u] = f / nv;
+      v[u] = f - tt[u] * nv;
+      if (f < total) {
+        const char* row = xs + (t0 + tt[u]) * h * 2;
+#pragma unroll
+        for (int q = 0; q < WI / 4; ++q) load_raw<kBF16, 8>(row, static_cast<uint64_t>(v[u]) * EPI + q * 8, w[u] + 4 * q);
       }
-    } else {
-      // 16 elements (two 16-byte loads) per thread; the 8 consecutive threads
-      // holding a 128-element block reduce its amax with shuffles; one
-      // reciprocal per block, one multiply per element, one 16-byte store of
-      // codes per destination row
-      const uint64_t nv16 = h / 16;
-      for (uint64_t v = threadIdx.x; v < nv16; v += kThreads) {
-        uint32_t w[8];
-        load_raw<kBF16, 8>(src, v * 16, w);
-        load_raw<kBF16, 8>(src, v * 16 + 8, w + 4);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (f0 + u * kThreads >= total) continue;  // whole aligned groups of 8 lanes drop out together
+      if constexpr (!FP8) {
+        for (int j = 0; j < k; ++j) {
+          const int d = dest[tt[u]][j];
+          if (d >= 0)
+            store_raw<kBF16, 8>(a.recv[d], static_cast<uint64_t>(pos[tt[u]][j]) * h + static_cast<uint64_t>(v[u]) * 8, w[u]);
+        }
+      } else {
         float x[16];
         float amax = 0.0f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          x[e] = widen<kBF16>(w, e);
+          x[e] = widen<kBF16>(w[u], e);
           amax = fmaxf(amax, fabsf(x[e]));
         }
-        // the 8 lanes of this block are all active (hidden is a multiple of 128)
         const unsigned group = 0xFFu << (threadIdx.x & 24);
 #pragma unroll
         for (int off = 4; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(group, amax, off));
@@ -230,98 +259,84 @@ __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_con
           const uint32_t c = __nv_cvt_float_to_fp8(__fmul_rn(x[e], inv), __NV_SATFINITE, __NV_E4M3);
           q[e >> 2] |= (c & 0xFFu) << (8 * (e & 3));
         }
-        const uint64_t blk = v / 8;  // 8 vectors of 16 = one 128-element block
+        const uint64_t blk = v[u] / 8;  // 8 items of 16 = one 128-element block
         for (int j = 0; j < k; ++j) {
-          const int d = dest[tt][j];
+          const int d = dest[tt[u]][j];
           if (d < 0) continue;
-          const uint64_t row = static_cast<uint64_t>(pos[tt][j]);
-          st_stream16(static_cast<char*>(a.recv[d]) + row * h + v * 16, make_uint4(q[0], q[1], q[2], q[3]));
+          const uint64_t row = static_cast<uint64_t>(pos[tt[u]][j]);
+          st_stream16(static_cast<char*>(a.recv[d]) + row * h + static_cast<uint64_t>(v[u]) * 16,
+                      make_uint4(q[0], q[1], q[2], q[3]));
           if ((threadIdx.x & 7) == 0) a.scales[d][row * (h / 128) + blk] = scale;
         }
       }
     }
-    if (a.rexp_given && threadIdx.x < k) {
-      const int d = dest[tt][threadIdx.x];
-      if (d >= 0 && a.rexp[d] != nullptr) a.rexp[d][pos[tt][threadIdx.x]] = expert[tt][threadIdx.x];
-    }
   }
 }
 
-// One CTA per (tile of tokens, source): token t's output is the bf16 of the
-// fp32 sum over choices j of w[t][j] * y_j, in choice order (each product and
-// each sum rounded; no fused multiply-add).  The k rows' loads are issued
-// before any is combined.
+// One CTA per (tpc tokens, source), the (token, vector) items a flat range as
+// in dispatch: token t's output is the bf16 of the fp32 sum over choices j of
+// w[t][j] * y_j, in choice order (each product and each sum rounded; no fused
+// multiply-add).  The k rows' loads are issued before any is combined.
 __global__ void __launch_bounds__(kThreads) moe_combine_kernel(const __grid_constant__ MoeCombineArgs a) {
   __shared__ int64_t base[kMoeMaxRanks];
-  __shared__ int64_t pos[kTokensPerCta][kMoeMaxK];
-  __shared__ int dest[kTokensPerCta][kMoeMaxK];
-  __shared__ float wt[kTokensPerCta][kMoeMaxK];
+  __shared__ int64_t pos[kMaxTokensPerCta][kMoeMaxK];
+  __shared__ int dest[kMaxTokensPerCta][kMoeMaxK];
+  __shared__ float wt[kMaxTokensPerCta][kMoeMaxK];
   pdl_enter();
   const int s = blockIdx.y;
-  const int p = a.p, k = a.k;
-  const uint64_t t0 = static_cast<uint64_t>(blockIdx.x) * kTokensPerCta;
-  row_bases(a.counts, p, s, base);
+  const int k = a.k, tpc = a.tpc;
+  const uint64_t t0 = static_cast<uint64_t>(blockIdx.x) * tpc;
+  row_bases(a.counts, a.p, s, base);
   __syncthreads();
-  for (int i = threadIdx.x; i < kTokensPerCta * k; i += kThreads) {
-    const int tt = i / k, j = i % k;
-    const uint64_t t = t0 + tt;
-    int d = -1;
-    int64_t row = -1;
-    float wj = 0.0f;
-    if (t < a.tokens) {
-      const int e = a.ids[s][t * k + j];
-      const int slot = a.slots[s][t * k + j];
-      wj = a.weights[s][t * k + j];
-      if (e >= 0 && e < a.num_experts && slot >= 0) {
-        d = e / a.epr;
-        row = base[d] + slot;
-        if (static_cast<uint64_t>(row) >= a.cap[d]) d = -1;
-      }
-    }
-    dest[tt][j] = d;
-    pos[tt][j] = row;
-    wt[tt][j] = wj;
-  }
+  token_rows(a, s, t0, tpc, base, dest, pos, static_cast<int (*)[kMoeMaxK]>(nullptr), a.weights, wt);
   __syncthreads();
   const uint64_t h = a.hidden;
-  const uint64_t nvec = h / 8;
-  for (int tt = 0; tt < kTokensPerCta; ++tt) {
-    const uint64_t t = t0 + tt;
-    if (t >= a.tokens) break;
-    for (uint64_t v = threadIdx.x; v < nvec; v += kThreads) {
-      float acc[8];
-      bool have = false;
-      for (int j0 = 0; j0 < k; j0 += 8) {
-        uint32_t raw[8][4];
+  const uint32_t nv = static_cast<uint32_t>(h / 8);
+  const uint64_t left = a.tokens - t0;
+  const uint32_t ntok = static_cast<uint32_t>(left < static_cast<uint64_t>(tpc) ? left : tpc);
+  const uint32_t total = ntok * nv;
+  for (uint32_t f = threadIdx.x; f < total; f += kThreads) {
+    const uint32_t tt = f / nv, v = f - (f / nv) * nv;
+    float acc[8];
+    bool have = false;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint32_t raw[8][4];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int j = j0 + b;
-          if (j < k && dest[tt][j] >= 0)
-            load_raw<kBF16, 8>(a.y[dest[tt][j]], static_cast<uint64_t>(pos[tt][j]) * h + v * 8, raw[b]);
-        }
+      for (int b = 0; b < 8; ++b) {
+        const int j = j0 + b;
+        if (j < k && dest[tt][j] >= 0)
+          load_raw<kBF16, 8>(a.y[dest[tt][j]], static_cast<uint64_t>(pos[tt][j]) * h + static_cast<uint64_t>(v) * 8, raw[b]);
+      }
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int j = j0 + b;
-          if (j < k && dest[tt][j] >= 0) {
-            const float wj = wt[tt][j];
+      for (int b = 0; b < 8; ++b) {
+        const int j = j0 + b;
+        if (j < k && dest[tt][j] >= 0) {
+          const float wj = wt[tt][j];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float prod = __fmul_rn(wj, widen<kBF16>(raw[b], e));
-              acc[e] = have ? __fadd_rn(acc[e], prod) : prod;
-            }
-            have = true;
+          for (int e = 0; e < 8; ++e) {
+            const float prod = __fmul_rn(wj, widen<kBF16>(raw[b], e));
+            acc[e] = have ? __fadd_rn(acc[e], prod) : prod;
           }
+          have = true;
         }
       }
-      if (!have) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-      }
-      uint32_t w[4];
-      pack_out<kBF16, 8>(acc, w);
-      store_raw<kBF16, 8>(a.out[s], t * h + v * 8, w);
     }
+    if (!have) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    }
+    uint32_t w[4];
+    pack_out<kBF16, 8>(acc, w);
+    store_raw<kBF16, 8>(a.out[s], (t0 + tt) * h + static_cast<uint64_t>(v) * 8, w);
   }
+}
+
+// Tokens per CTA: the fewest (at most 16) that make the CTA's items a whole
+// number of passes of `per_pass` items.
+__host__ int tokens_per_cta(uint64_t items_per_token, uint64_t per_pass) {
+  for (int t = 1; t <= kMaxTokensPerCta; ++t)
+    if ((items_per_token * static_cast<uint64_t>(t)) % per_pass == 0) return t;
+  return 8;
 }
 
 }  // namespace
@@ -349,16 +364,21 @@ cudaError_t launch_moe_route(const MoeRouteArgs& a, cudaStream_t s) {
   return err;
 }
 
-cudaError_t launch_moe_dispatch(const MoeDispatchArgs& a, bool fp8, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((a.tokens + kTokensPerCta - 1) / kTokensPerCta), a.p);
-  cudaError_t err = fp8 ? launch_kernel(moe_dispatch_kernel<true>, grid, dim3(kThreads), s, a)
-                        : launch_kernel(moe_dispatch_kernel<false>, grid, dim3(kThreads), s, a);
+cudaError_t launch_moe_dispatch(const MoeDispatchArgs& args, bool fp8, cudaStream_t s) {
+  constexpr int kU8 = 2, kU16 = 4;  // items per thread: FP8 (32-byte loads), bf16 (16-byte)
+  MoeDispatchArgs a = args;
+  a.tpc = tokens_per_cta(a.hidden / (fp8 ? 16 : 8), static_cast<uint64_t>(kThreads) * (fp8 ? kU8 : kU16));
+  const dim3 grid(static_cast<unsigned>((a.tokens + a.tpc - 1) / a.tpc), a.p);
+  cudaError_t err = fp8 ? launch_kernel(moe_dispatch_kernel<true, kU8>, grid, dim3(kThreads), s, a)
+                        : launch_kernel(moe_dispatch_kernel<false, kU16>, grid, dim3(kThreads), s, a);
   if (err == cudaSuccess) note_launch();
   return err;
 }
 
-cudaError_t launch_moe_combine(const MoeCombineArgs& a, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((a.tokens + kTokensPerCta - 1) / kTokensPerCta), a.p);
+cudaError_t launch_moe_combine(const MoeCombineArgs& args, cudaStream_t s) {
+  MoeCombineArgs a = args;
+  a.tpc = tokens_per_cta(a.hidden / 8, kThreads);
+  const dim3 grid(static_cast<unsigned>((a.tokens + a.tpc - 1) / a.tpc), a.p);
   cudaError_t err = launch_kernel(moe_combine_kernel, grid, dim3(kThreads), s, a);
   if (err == cudaSuccess) note_launch();
   return err;

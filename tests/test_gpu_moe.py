@@ -60,7 +60,10 @@ def test_route_matches_oracle(lib, p, T, k, E):
         np.testing.assert_array_equal(slots[s].cpu().numpy().reshape(-1), want_s[s])
 
 
-@pytest.mark.parametrize("p,T,k,E,h", [(2, 100, 2, 8, 128), (4, 500, 4, 16, 256), (8, 1024, 8, 64, 4096)])
+# h = 7168 (the DeepSeek-V3 hidden size): 8 tokens per CTA for dispatch, 2 for
+# combine; T = 37 leaves a short last CTA
+@pytest.mark.parametrize("p,T,k,E,h", [(2, 100, 2, 8, 128), (4, 500, 4, 16, 256), (8, 1024, 8, 64, 4096),
+                                       (8, 37, 8, 256, 7168)])
 def test_dispatch_bf16_matches_oracle(lib, p, T, k, E, h):
     ids, toks, *_, recv, _, rexp = _run(lib, p, T, k, E, h, fp8=False, seed=1, bad_id=True)
     want, _, want_e, _, _ = moe.dispatch(toks, [i.reshape(-1) for i in ids], p, k, E, h)
@@ -69,7 +72,7 @@ def test_dispatch_bf16_matches_oracle(lib, p, T, k, E, h):
         np.testing.assert_array_equal(rexp[d].cpu().numpy(), want_e[d])
 
 
-@pytest.mark.parametrize("p,T,k,E,h", [(2, 100, 2, 8, 128), (8, 512, 8, 64, 4096)])
+@pytest.mark.parametrize("p,T,k,E,h", [(2, 100, 2, 8, 128), (8, 512, 8, 64, 4096), (8, 37, 8, 256, 7168)])
 def test_dispatch_fp8_matches_oracle(lib, p, T, k, E, h):
     ids, toks, *_, recv, scales, _ = _run(lib, p, T, k, E, h, fp8=True, seed=2)
     want, want_sc, _, _, _ = moe.dispatch(toks, [i.reshape(-1) for i in ids], p, k, E, h, fp8=True)
@@ -78,7 +81,8 @@ def test_dispatch_fp8_matches_oracle(lib, p, T, k, E, h):
         np.testing.assert_array_equal(scales[d].cpu().numpy(), want_sc[d], err_msg=f"scales rank {d}")
 
 
-@pytest.mark.parametrize("p,T,k,E,h", [(2, 100, 2, 8, 128), (4, 300, 3, 16, 256), (8, 512, 8, 64, 4096)])
+@pytest.mark.parametrize("p,T,k,E,h", [(2, 100, 2, 8, 128), (4, 300, 3, 16, 256), (8, 512, 8, 64, 4096),
+                                       (8, 37, 8, 256, 7168), (3, 5, 16, 48, 384)])
 def test_combine_matches_oracle_and_inverts_dispatch(lib, p, T, k, E, h):
     ids, toks, d_ids, counts, c, slots, recv, _, _ = _run(lib, p, T, k, E, h, fp8=False, seed=3)
     w = workloads.moe_gate_weights(p, T, k, seed=5)
