@@ -102,7 +102,8 @@ __device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
   if (tid < n_edge) copy_byte(tid < n_head ? lo + tid : ub + (tid - n_head), shift);
 }
 
-__global__ void __launch_bounds__(kThreads) a2av_kernel(const __grid_constant__ A2AArgs a) {
+template <int CAP>
+__global__ void __launch_bounds__(kThreads) a2av_kernel(const __grid_constant__ A2AArgsT<CAP> a) {
   pdl_enter();
   for (uint64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
     // the block that owns tile t: the last one whose first tile is <= t
@@ -137,7 +138,17 @@ cudaError_t launch_a2av(const A2AArgs& a, cudaStream_t s) {
   if (a.total_tiles == 0 || a.ndesc == 0) return cudaSuccess;
   uint64_t g = a.total_tiles;
   if (g > (1u << 30)) g = 1u << 30;
-  cudaError_t err = launch_kernel(a2av_kernel, dim3(static_cast<unsigned>(g)), dim3(kThreads), s, a);
+  const dim3 grid(static_cast<unsigned>(g));
+  cudaError_t err;
+  if (a.ndesc <= kA2ASmallDesc) {  // the common case: a 4 KB parameter block
+    A2AArgsT<kA2ASmallDesc> small;
+    small.total_tiles = a.total_tiles;
+    small.ndesc = a.ndesc;
+    for (int i = 0; i < a.ndesc; ++i) small.d[i] = a.d[i];
+    err = launch_kernel(a2av_kernel<kA2ASmallDesc>, grid, dim3(kThreads), s, small);
+  } else {
+    err = launch_kernel(a2av_kernel<kA2AMaxDesc>, grid, dim3(kThreads), s, a);
+  }
   if (err == cudaSuccess) note_launch();
   return err;
 }

@@ -447,10 +447,7 @@ extern "C" ccl_status_t ccl_reduce(const void* const* send, void* recv, int p, s
   ccl_status_t st = check_p(p);
   if (st != CCL_OK || (st = check_root(p, root)) != CCL_OK) return st;
   // validate as an all-reduce whose only output is the root's
-  void* outs[CCL_MAX_RANKS];
-  for (int r = 0; r < p; ++r) outs[r] = nullptr;
   if (recv == nullptr && n != 0) return fail(CCL_ERR_INVALID_ARG, "recv is NULL");
-  outs[root] = recv;
   const size_t e = elem_bytes(dt);
   if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
   if (!valid_op(op)) return fail(CCL_ERR_INVALID_ARG, "unknown op %d", op);
@@ -782,7 +779,7 @@ extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* c
 
   // exclusive prefix sums: source s's block for d, destination d's block from s
   uint64_t recv_row[CCL_MAX_RANKS] = {0};  // next free row of each destination
-  A2AArgs a;
+  static thread_local A2AArgs a;             // 32 KB: kept off the stack
   memset(&a, 0, sizeof(a));
   for (int s = 0; s < p; ++s) {
     uint64_t send_row = 0;

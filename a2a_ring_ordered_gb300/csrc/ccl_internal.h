@@ -61,13 +61,22 @@ struct A2ADesc {
   uint64_t bytes;
   uint64_t tile0;
 };
-constexpr int kA2AMaxDesc = 112;  // 112 * 32 B + header < 4 KB of parameters
+// Descriptors per launch: up to 112 travel in a parameter block under the
+// classic 4 KB limit; a call with more blocks (p > 10) uses the 32 KB
+// parameter space of CUDA 12.1+ drivers (1016 descriptors), so even p = 128
+// (16,384 blocks) takes 17 launches instead of 147.
+constexpr int kA2ASmallDesc = 112;
+constexpr int kA2AMaxDesc = 1016;  // 1016 * 32 B + header < 32,764 bytes
 constexpr uint64_t kA2ATileBytes = 32768;
-struct A2AArgs {
+template <int CAP>
+struct A2AArgsT {
   uint64_t total_tiles;
   int ndesc;
-  A2ADesc d[kA2AMaxDesc];
+  A2ADesc d[CAP];
 };
+using A2AArgs = A2AArgsT<kA2AMaxDesc>;
+static_assert(sizeof(A2AArgsT<kA2ASmallDesc>) <= 4096, "all-to-allv parameters exceed 4 KB");
+static_assert(sizeof(A2AArgs) <= 32764, "all-to-allv parameters exceed 32,764 bytes");
 uint64_t a2a_tiles_for(const char* dst, uint64_t bytes);
 cudaError_t launch_a2av(const A2AArgs& a, cudaStream_t s);
 

@@ -35,6 +35,13 @@ __device__ __forceinline__ uint4 ld_once16(const void* p) {
       : "l"(p));
   return v;
 }
+// 16-byte read-only load that allocates in L1 (for data a thread reads as two
+// halves of one sector).
+__device__ __forceinline__ uint4 ld_l1_16(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ uint32_t ld_once4(const void* p) {
   uint32_t v;
   asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -65,7 +72,21 @@ template <int DT, int VEC>
 __device__ __forceinline__ void load_raw(const void* base, uint64_t i, uint32_t* w) {
   constexpr int B = Elem<DT>::kBytes;
   const char* p = static_cast<const char*>(base) + i * B;
-  if constexpr (VEC * B >= 16) {
+  if constexpr (VEC * B == 32) {
+    // Two 16-byte halves of one 32-byte sector per thread: a warp's first
+    // load touches every other 16 bytes of 32 sectors, so both loads allocate
+    // in L1 and the second is served there.  In HBM the second would hit L2
+    // anyway; from pinned host memory (zero-copy) it saves a second trip over
+    // the host link, which doubles the kernel's host-memory throughput.
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      uint4 v = ld_l1_16(p + 16 * k);
+      w[4 * k + 0] = v.x;
+      w[4 * k + 1] = v.y;
+      w[4 * k + 2] = v.z;
+      w[4 * k + 3] = v.w;
+    }
+  } else if constexpr (VEC * B >= 16) {
 #pragma unroll
     for (int k = 0; k < VEC * B / 16; ++k) {
       uint4 v = ld_once16(p + 16 * k);

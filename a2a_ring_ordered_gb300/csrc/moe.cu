@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const __grid_c
 
 constexpr int kMaxTokensPerCta = 16;
 
+
 // base[d] = rows of destination d sent by sources before s.
 __device__ __forceinline__ void row_bases(const int64_t* counts, int p, int s, int64_t* base) {
   for (int d = threadIdx.x; d < p; d += blockDim.x) {
@@ -228,7 +229,20 @@ __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_con
       if (f < total) {
         const char* row = xs + (t0 + tt[u]) * h * 2;
 #pragma unroll
-        for (int q = 0; q < WI / 4; ++q) load_raw<kBF16, 8>(row, static_cast<uint64_t>(v[u]) * EPI + q * 8, w[u] + 4 * q);
+        if constexpr (FP8) {
+          // the item's 32 bytes are two 16-byte loads; they allocate in L1 so
+          // that the second finds the sector the first brought in
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint4 g = ld_l1_16(row + static_cast<uint64_t>(v[u]) * 32 + 16 * q);
+            w[u][4 * q] = g.x;
+            w[u][4 * q + 1] = g.y;
+            w[u][4 * q + 2] = g.z;
+            w[u][4 * q + 3] = g.w;
+          }
+        } else {
+          load_raw<kBF16, 8>(row, static_cast<uint64_t>(v[u]) * EPI, w[u]);
+        }
       }
     }
 #pragma unroll

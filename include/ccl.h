@@ -209,7 +209,8 @@ ccl_status_t ccl_bucket_allreduce_scale_cast(const float* const* grads, void* co
  *   recv[d]    sum_s counts[s][d] rows; the block from s lands at row
  *              sum_{s' < s} counts[s'][d].
  * Combine is the same call on the received buffers with counts transposed.
- * Buffers must not overlap.  Bit-exact copy for every dtype. */
+ * Buffers must not overlap.  Bit-exact copy for every dtype.  One kernel
+ * launch per 1016 non-empty blocks (one launch up to p = 31). */
 ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts, void* const* recv,
                              int p, size_t row_elems, ccl_dtype_t dt, void* stream);
 

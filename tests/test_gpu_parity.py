@@ -323,16 +323,23 @@ def test_all_to_allv_ragged_rows(lib, row_elems, dtype, p):
         assert outs[d].guards_intact()
 
 
-def test_all_to_allv_many_blocks_spans_launches(lib):
-    """p=16 -> 256 blocks: more than one launch's worth of block descriptors."""
-    p, row = 16, 64
-    rng = np.random.default_rng(5)
-    counts = rng.integers(1, 40, size=(p, p))
-    x = [workloads.normal(1, int(counts[s].sum()) * row, 1.0, seed=s, dtype="bf16")[0] for s in range(p)]
+@pytest.mark.parametrize("p,row,hi", [(16, 64, 40), (48, 3, 6), (128, 8, 2)])
+def test_all_to_allv_many_blocks(lib, p, row, hi):
+    """More blocks than a 4 KB parameter block holds: p=16 (256 blocks, one
+    launch with the large parameter block), p=48 with 3-element rows (about
+    1900 blocks, two launches, shuffle realignment), p=128 (about 8200 blocks
+    of 0-1 rows, nine launches)."""
+    rng = np.random.default_rng(5 + p)
+    counts = rng.integers(0 if p > 16 else 1, hi, size=(p, p))
+    x = [workloads.normal(1, max(int(counts[s].sum()), 1) * row, 1.0, seed=s, dtype="bf16")[0][: int(counts[s].sum()) * row]
+         for s in range(p)]
     want = collectives.all_to_allv(x, counts, row)
     recv = [torch.empty(int(counts[:, d].sum()) * row, dtype=torch.bfloat16, device="cuda")
             for d in range(p)]
+    blocks = int((counts > 0).sum())
+    n0 = lib.ccl_kernel_launch_count()
     lib.ccl_all_to_allv([to_dev(v, "bf16") for v in x], counts, recv, row)
+    assert lib.ccl_kernel_launch_count() - n0 == -(-blocks // 1016)
     for d in range(p):
         assert_equal(to_host(recv[d]), want[d], "bf16", f"rank {d}")
 
