@@ -10,9 +10,22 @@
 #include <atomic>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ccl_internal.h"
 
 namespace ccl {
+
+// An NVTX range named after the entry point, so that a profiler's timeline
+// (ncu --nvtx, Nsight Systems) groups each call's kernels under its name.
+// Without an attached tool a push/pop costs a few nanoseconds.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define CCL_TRACE() ::ccl::NvtxRange ccl_trace_range_(__func__)
 
 static std::atomic<uint64_t> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -245,6 +258,7 @@ ccl_status_t fused_reduce(int mode, const void* const* send, void* const* recv, 
 
 extern "C" ccl_status_t ccl_allreduce(const void* const* send, void* const* recv, int p, size_t n,
                                       ccl_dtype_t dt, ccl_op_t op, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_reduce(0, send, recv, p, n, dt, op);
   if (st != CCL_OK || n == 0) return st;
@@ -254,6 +268,7 @@ extern "C" ccl_status_t ccl_allreduce(const void* const* send, void* const* recv
 extern "C" ccl_status_t ccl_allreduce_schedule(const void* const* send, void* const* recv, int p,
                                                size_t n, ccl_dtype_t dt, ccl_op_t op,
                                                ccl_schedule_t schedule, void* stream) {
+  CCL_TRACE();
   clear_error();
   if (schedule == CCL_SCHEDULE_RING) return ccl_allreduce(send, recv, p, n, dt, op, stream);
   if (schedule < CCL_SCHEDULE_RECURSIVE_DOUBLING || schedule > CCL_SCHEDULE_NAIVE)
@@ -287,6 +302,7 @@ extern "C" ccl_status_t ccl_allreduce_schedule(const void* const* send, void* co
 extern "C" ccl_status_t ccl_allreduce_hierarchical(const void* const* send, void* const* recv, int p,
                                                    int group, size_t n, ccl_dtype_t dt, ccl_op_t op,
                                                    void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_reduce(0, send, recv, p, n, dt, op);
   if (st != CCL_OK) return st;
@@ -313,6 +329,7 @@ extern "C" ccl_status_t ccl_allreduce_hierarchical(const void* const* send, void
 
 extern "C" ccl_status_t ccl_reduce_scatter(const void* const* send, void* const* recv, int p,
                                            size_t n, ccl_dtype_t dt, ccl_op_t op, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_reduce(1, send, recv, p, n, dt, op);
   if (st != CCL_OK || n == 0) return st;
@@ -321,6 +338,7 @@ extern "C" ccl_status_t ccl_reduce_scatter(const void* const* send, void* const*
 
 extern "C" ccl_status_t ccl_all_gather(const void* const* send, void* const* recv, int p, size_t n,
                                        ccl_dtype_t dt, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_gather(send, recv, p, n, dt);
   if (st != CCL_OK || n == 0) return st;
@@ -342,6 +360,7 @@ extern "C" ccl_status_t ccl_all_gather(const void* const* send, void* const* rec
 extern "C" ccl_status_t ccl_bucket_allreduce_scale_cast(const float* const* grads,
                                                         void* const* out_bf16, int p, size_t n,
                                                         float scale, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_p(p);
   if (st != CCL_OK) return st;
@@ -405,6 +424,7 @@ ccl_status_t copy_transfers(int dt, const char* const* src, char* const* dst, co
 
 extern "C" ccl_status_t ccl_broadcast(const void* send, void* const* recv, int p, size_t n,
                                       ccl_dtype_t dt, int root, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_p(p);
   if (st != CCL_OK || (st = check_root(p, root)) != CCL_OK) return st;
@@ -443,6 +463,7 @@ extern "C" ccl_status_t ccl_broadcast(const void* send, void* const* recv, int p
 
 extern "C" ccl_status_t ccl_reduce(const void* const* send, void* recv, int p, size_t n,
                                    ccl_dtype_t dt, ccl_op_t op, int root, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_p(p);
   if (st != CCL_OK || (st = check_root(p, root)) != CCL_OK) return st;
@@ -484,6 +505,7 @@ extern "C" ccl_status_t ccl_reduce(const void* const* send, void* recv, int p, s
 
 extern "C" ccl_status_t ccl_scatter(const void* send, void* const* recv, int p, size_t n,
                                     ccl_dtype_t dt, int root, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_p(p);
   if (st != CCL_OK || (st = check_root(p, root)) != CCL_OK) return st;
@@ -520,6 +542,7 @@ extern "C" ccl_status_t ccl_scatter(const void* send, void* const* recv, int p, 
 
 extern "C" ccl_status_t ccl_gather(const void* const* send, void* recv, int p, size_t n,
                                    ccl_dtype_t dt, int root, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_p(p);
   if (st != CCL_OK || (st = check_root(p, root)) != CCL_OK) return st;
@@ -582,6 +605,7 @@ ccl_status_t check_ptrs(const char* name, const void* const* a, int p, size_t al
 extern "C" ccl_status_t ccl_moe_route(const int32_t* const* expert_ids, int p, size_t tokens, int k,
                                       int num_experts, int64_t* counts, int32_t* const* slots,
                                       void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_moe(p, tokens, k, num_experts, 128);
   if (st != CCL_OK) return st;
@@ -613,6 +637,7 @@ extern "C" ccl_status_t ccl_moe_dispatch(const void* const* x, const int32_t* co
                                          int fp8, void* const* recv, const size_t* recv_rows,
                                          float* const* recv_scales, int32_t* const* recv_expert,
                                          void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_moe(p, tokens, k, num_experts, hidden);
   if (st != CCL_OK) return st;
@@ -658,6 +683,7 @@ extern "C" ccl_status_t ccl_moe_combine(const void* const* y, const size_t* y_ro
                                         const int64_t* counts, const int32_t* const* slots, int p,
                                         size_t tokens, int k, int num_experts, size_t hidden,
                                         void* const* out, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_moe(p, tokens, k, num_experts, hidden);
   if (st != CCL_OK) return st;
@@ -698,6 +724,7 @@ extern "C" ccl_status_t ccl_moe_combine(const void* const* y, const size_t* y_ro
 extern "C" ccl_status_t ccl_all_to_all_heads(const void* const* send, void* const* recv, int p,
                                              size_t seq_per_rank, size_t heads, size_t head_dim,
                                              ccl_dtype_t dt, int inverse, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_p(p);
   if (st != CCL_OK) return st;
@@ -744,6 +771,7 @@ extern "C" ccl_status_t ccl_all_to_all_heads(const void* const* send, void* cons
 extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts,
                                         void* const* recv, int p, size_t row_elems,
                                         ccl_dtype_t dt, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_p(p);
   if (st != CCL_OK) return st;
@@ -926,6 +954,7 @@ extern "C" ccl_status_t ccl_ring_allreduce_literal(const void* const* send, void
                                                    int p, size_t n, ccl_dtype_t dt, ccl_op_t op,
                                                    uint64_t* bytes_sent, void* workspace,
                                                    size_t workspace_bytes, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_reduce(0, send, recv, p, n, dt, op);
   if (st != CCL_OK) return st;
@@ -970,6 +999,7 @@ extern "C" ccl_status_t ccl_ring_reduce_scatter_literal(const void* const* send,
                                                         ccl_op_t op, uint64_t* bytes_sent,
                                                         void* workspace, size_t workspace_bytes,
                                                         void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_reduce(1, send, recv, p, n, dt, op);
   if (st != CCL_OK) return st;
@@ -1011,6 +1041,7 @@ extern "C" ccl_status_t ccl_ring_reduce_scatter_literal(const void* const* send,
 extern "C" ccl_status_t ccl_ring_all_gather_literal(const void* const* send, void* const* recv,
                                                     int p, size_t n, ccl_dtype_t dt,
                                                     uint64_t* bytes_sent, void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_gather(send, recv, p, n, dt);
   if (st != CCL_OK) return st;
@@ -1083,6 +1114,7 @@ extern "C" ccl_status_t ccl_ring_reduce_scatter_literal_noalloc(const void* cons
                                                                 ccl_dtype_t dt, ccl_op_t op,
                                                                 uint64_t* bytes_sent,
                                                                 void* stream) {
+  CCL_TRACE();
   clear_error();
   ccl_status_t st = check_reduce(1, send, recv, p, n, dt, op);
   if (st != CCL_OK) return st;
