@@ -37,9 +37,11 @@ def chunk_of(p: int, n: int, idx: np.ndarray) -> np.ndarray:
 
 
 def fold_columns(cols: list[np.ndarray], idx: np.ndarray, n: int, dtype: str = "f32",
-                 op: str = "sum"):
+                 op: str = "sum", wire: str = "fp32"):
     """The fold at indices ``idx`` of n-element rank buffers, given only the
-    sampled values: ``cols[r][j]`` is rank r's element ``idx[j]``."""
+    sampled values: ``cols[r][j]`` is rank r's element ``idx[j]``.  With
+    ``wire="bf16"`` every hop's new partial is rounded to bf16 (the ring's
+    bf16-wire variant, ``oracle.ring``)."""
     p = len(cols)
     idx = np.asarray(idx, dtype=np.int64)
     chunks = chunk_of(p, n, idx)
@@ -57,6 +59,8 @@ def fold_columns(cols: list[np.ndarray], idx: np.ndarray, n: int, dtype: str = "
         acc = value((c + 1) % p, mask)
         for j in range(2, p + 1):
             acc = combine(acc, value((c + j) % p, mask), op)
+            if wire == "bf16":
+                acc = bf16_to_f32(f32_to_bf16_rne(acc))
         out[mask] = acc
     return out
 
@@ -74,9 +78,9 @@ def allreduce_at(x: list[np.ndarray], idx: np.ndarray, dtype: str = "f32", op: s
 
 
 def allreduce_at_columns(cols: list[np.ndarray], idx: np.ndarray, n: int, dtype: str = "f32",
-                         op: str = "sum"):
+                         op: str = "sum", wire: str = "fp32"):
     """All-reduce output at ``idx`` from sampled columns (see ``fold_columns``)."""
-    acc = fold_columns(cols, idx, n, dtype, op)
+    acc = fold_columns(cols, idx, n, dtype, op, wire)
     return f32_to_bf16_rne(acc) if dtype == "bf16" else acc
 
 

@@ -28,6 +28,9 @@ Readings taken where the pages are silent (each is listed in the design doc):
    rank r sends chunk (r-s) mod p.
 3. bf16 inputs: the partial travels and accumulates in fp32; the owner rounds
    its finished chunk to bf16 once (nearest-even) and the AG phase moves bf16.
+   The variant ``wire="bf16"`` sends the partial as bf16 instead: every hop
+   adds in fp32 and rounds the new partial to bf16 (nearest-even) before it
+   travels on, so the reduce-scatter moves 2 bytes per element.
 4. MAX/MIN (not on the pages; extras of the library): the receiver keeps its
    own value when it is strictly greater (smaller), else the received partial.
 
@@ -93,8 +96,17 @@ def combine(received: np.ndarray, own: np.ndarray, op: str) -> np.ndarray:
     raise ValueError(f"op must be one of {OPS}")
 
 
-def _wire_size_rs(dtype: str) -> int:
+def _wire_size_rs(dtype: str, wire: str = "fp32") -> int:
+    if wire == "bf16":
+        return 2  # bf16 partials
     return 4  # fp32 partials (f32 and bf16) or int32 partials
+
+
+def _check_wire(dtype: str, wire: str) -> None:
+    if wire not in ("fp32", "bf16"):
+        raise ValueError("wire must be 'fp32' or 'bf16'")
+    if wire == "bf16" and dtype != "bf16":
+        raise ValueError("a bf16 wire needs bf16 data")
 
 
 def _elem_size(dtype: str) -> int:
@@ -102,7 +114,8 @@ def _elem_size(dtype: str) -> int:
 
 
 # ------------------------------------------------------------------ RS phase
-def ring_reduce_scatter_phase(x: list[np.ndarray], dtype: str = "f32", op: str = "sum"):
+def ring_reduce_scatter_phase(x: list[np.ndarray], dtype: str = "f32", op: str = "sum",
+                              wire: str = "fp32"):
     """Run the p-1 reduce-scatter steps on copies of the rank buffers.
 
     Returns (work, bytes_sent): ``work[r]`` is rank r's full working buffer
@@ -112,8 +125,9 @@ def ring_reduce_scatter_phase(x: list[np.ndarray], dtype: str = "f32", op: str =
     p, n = _check(x, dtype)
     if op not in OPS:
         raise ValueError(f"op must be one of {OPS}")
+    _check_wire(dtype, wire)
     bounds = chunk_bounds(p, n)
-    wire = _wire_size_rs(dtype)
+    wire_bytes = _wire_size_rs(dtype, wire)
     work = [_widen(xi, dtype) for xi in x]
     sent = [0] * p
     for s in range(p - 1):
@@ -123,12 +137,15 @@ def ring_reduce_scatter_phase(x: list[np.ndarray], dtype: str = "f32", op: str =
             c = (r - s - 1) % p
             off, ln = bounds[c]
             messages.append((c, work[r][off:off + ln].copy()))
-            sent[r] += ln * wire
+            sent[r] += ln * wire_bytes
         for r in range(p):
             c, msg = messages[r]
             dst = (r + 1) % p
             off, ln = bounds[c]
-            work[dst][off:off + ln] = combine(msg, work[dst][off:off + ln], op)
+            part = combine(msg, work[dst][off:off + ln], op)
+            if wire == "bf16":  # the new partial is what travels: round it now
+                part = bf16_to_f32(f32_to_bf16_rne(part))
+            work[dst][off:off + ln] = part
     return work, sent
 
 
@@ -139,13 +156,13 @@ def _finish_chunk(values: np.ndarray, dtype: str) -> np.ndarray:
     return values.astype({"f32": np.float32, "i32": np.int32}[dtype], copy=True)
 
 
-def ring_reduce_scatter(x: list[np.ndarray], dtype: str = "f32", op: str = "sum"):
+def ring_reduce_scatter(x: list[np.ndarray], dtype: str = "f32", op: str = "sum", wire: str = "fp32"):
     """Reduce-scatter: rank k gets chunk k of the ring-ordered reduction.
 
     Returns (shards, bytes_sent); ``shards[k]`` has len(chunk k) elements of
     the input dtype.
     """
-    work, sent = ring_reduce_scatter_phase(x, dtype, op)
+    work, sent = ring_reduce_scatter_phase(x, dtype, op, wire)
     bounds = chunk_bounds(len(x), len(x[0]))
     shards = []
     for k, (off, ln) in enumerate(bounds):
@@ -200,13 +217,13 @@ def ring_all_gather(shards: list[np.ndarray], dtype: str = "f32"):
 
 
 # ------------------------------------------------------------------ all-reduce
-def ring_allreduce(x: list[np.ndarray], dtype: str = "f32", op: str = "sum"):
+def ring_allreduce(x: list[np.ndarray], dtype: str = "f32", op: str = "sum", wire: str = "fp32"):
     """All-reduce = the RS phase then the AG phase on the same working buffers.
 
     Returns (outputs, bytes_sent_rs, bytes_sent_ag).  For bf16 the owner of
     each chunk rounds it to bf16 between the phases (reading 3).
     """
-    work, sent_rs = ring_reduce_scatter_phase(x, dtype, op)
+    work, sent_rs = ring_reduce_scatter_phase(x, dtype, op, wire)
     p, n = len(x), len(x[0])
     bounds = chunk_bounds(p, n)
     want = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32}[dtype]
