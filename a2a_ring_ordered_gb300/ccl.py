@@ -50,6 +50,8 @@ def _load() -> ctypes.CDLL:
         "ccl_allreduce": (st, [pp, pp, i32, sz, i32, i32, vp]),
         "ccl_allreduce_schedule": (st, [pp, pp, i32, sz, i32, i32, i32, vp]),
         "ccl_allreduce_hierarchical": (st, [pp, pp, i32, i32, sz, i32, i32, vp]),
+        "ccl_allreduce_bf16_wire": (st, [pp, pp, i32, sz, vp]),
+        "ccl_reduce_scatter_bf16_wire": (st, [pp, pp, i32, sz, vp]),
         "ccl_reduce_scatter": (st, [pp, pp, i32, sz, i32, i32, vp]),
         "ccl_all_gather": (st, [pp, pp, i32, sz, i32, vp]),
         "ccl_broadcast": (st, [vp, pp, i32, sz, i32, i32, vp]),
@@ -242,6 +244,32 @@ def ccl_allreduce_hierarchical(send, recv, group: int, op: str = "sum", stream=N
                                           _dtype_code(send[0]), _op_code(op),
                                           _stream(stream, send[0].device)),
            "ccl_allreduce_hierarchical")
+
+
+def ccl_allreduce_bf16_wire(send, recv, stream=None) -> None:
+    """bf16 ring all-reduce whose partials are rounded to bf16 at every hop."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    if send[0].dtype != torch.bfloat16 or len(recv) != p or recv[0].dtype != torch.bfloat16:
+        raise ValueError("send and recv must hold p bf16 buffers")
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [n] * p, "recv")
+    _check(LIB.ccl_allreduce_bf16_wire(_ptr_array([t.data_ptr() for t in send]),
+                                       _ptr_array([t.data_ptr() for t in recv]), p, n,
+                                       _stream(stream, send[0].device)), "ccl_allreduce_bf16_wire")
+
+
+def ccl_reduce_scatter_bf16_wire(send, recv, stream=None) -> None:
+    """bf16 ring reduce-scatter whose partials are rounded to bf16 at every hop."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    if send[0].dtype != torch.bfloat16 or len(recv) != p or recv[0].dtype != torch.bfloat16:
+        raise ValueError("send and recv must hold p bf16 buffers")
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, _chunk_lengths(p, n), "recv")
+    _check(LIB.ccl_reduce_scatter_bf16_wire(_ptr_array([t.data_ptr() for t in send]),
+                                            _ptr_array([t.data_ptr() for t in recv]), p, n,
+                                            _stream(stream, send[0].device)), "ccl_reduce_scatter_bf16_wire")
 
 
 def ccl_reduce_scatter(send, recv, op: str = "sum", stream=None) -> None:

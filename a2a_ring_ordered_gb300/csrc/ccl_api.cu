@@ -299,6 +299,44 @@ extern "C" ccl_status_t ccl_allreduce_schedule(const void* const* send, void* co
   return CCL_OK;
 }
 
+namespace {
+ccl_status_t wire_reduce(int mode, const void* const* send, void* const* recv, int p, size_t n,
+                         void* stream) {
+  FoldArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < p; ++r) {
+    a.send[r] = send[r];
+    a.recv[r] = recv[r];
+  }
+  a.p = p;
+  a.q = n / static_cast<uint64_t>(p);
+  a.rem = n % static_cast<uint64_t>(p);
+  a.scale = 1.0f;
+  const bool vec = all_aligned16(send, p, const_cast<const void* const*>(recv));
+  cudaError_t err = launch_wire_fold(mode, vec, a, as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "bf16-wire fold kernel launch");
+  return CCL_OK;
+}
+}  // namespace
+
+extern "C" ccl_status_t ccl_allreduce_bf16_wire(const void* const* send, void* const* recv, int p,
+                                                size_t n, void* stream) {
+  CCL_TRACE();
+  clear_error();
+  ccl_status_t st = check_reduce(0, send, recv, p, n, CCL_BF16, CCL_SUM);
+  if (st != CCL_OK || n == 0) return st;
+  return wire_reduce(kModeAllReduce, send, recv, p, n, stream);
+}
+
+extern "C" ccl_status_t ccl_reduce_scatter_bf16_wire(const void* const* send, void* const* recv, int p,
+                                                     size_t n, void* stream) {
+  CCL_TRACE();
+  clear_error();
+  ccl_status_t st = check_reduce(1, send, recv, p, n, CCL_BF16, CCL_SUM);
+  if (st != CCL_OK || n == 0) return st;
+  return wire_reduce(kModeReduceScatter, send, recv, p, n, stream);
+}
+
 extern "C" ccl_status_t ccl_allreduce_hierarchical(const void* const* send, void* const* recv, int p,
                                                    int group, size_t n, ccl_dtype_t dt, ccl_op_t op,
                                                    void* stream) {

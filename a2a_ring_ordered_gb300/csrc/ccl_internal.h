@@ -35,6 +35,8 @@ cudaError_t launch_fold(int mode, int dt, int op, bool vec, const FoldArgs& a, c
 // Fold in another schedule's order (schedule_fold.cu): `linear` = the naive
 // root's rank-order fold; otherwise the pairwise tree over ranks in identity
 // or (`reversed`) bit-reversed order.
+// bf16 ring with bf16 partials (rounded at every hop); mode AR or RS.
+cudaError_t launch_wire_fold(int mode, bool vec, const FoldArgs& a, cudaStream_t s);
 // Two-level ring fold; f.q / f.rem = floor(n / a), n mod a (the level-1 split).
 cudaError_t launch_hier_fold(int dt, bool vec, const FoldArgs& f, int a, cudaStream_t s);
 cudaError_t launch_schedule_fold(int dt, bool linear, bool reversed, bool vec, const FoldArgs& a,

@@ -140,6 +140,7 @@ KERNEL_SOURCES = {
     "schedule": ["a2a_ring_ordered_gb300/csrc/schedule_fold.cu",
                  "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "hier": ["a2a_ring_ordered_gb300/csrc/hier_fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
+    "wire": ["a2a_ring_ordered_gb300/csrc/wire_fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "gather": ["a2a_ring_ordered_gb300/csrc/gather.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "a2av": ["a2a_ring_ordered_gb300/csrc/a2av.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "ring_step": ["a2a_ring_ordered_gb300/csrc/ring_step.cu",
@@ -303,8 +304,11 @@ class AllReduce(Workload):
     kernel = "fold"
 
     def __init__(self, p=16, mib=256, dtype="f32", seed=4, op="sum", literal=False, schedule="ring",
-                 group=8):
+                 group=8, wire="fp32"):
         self.p, self.dtype, self.seed, self.op, self.literal = p, dtype, seed, op, literal
+        self.wire = wire
+        if wire == "bf16" and (dtype != "bf16" or schedule != "ring" or literal):
+            raise SystemExit("--wire bf16 needs --dtype bf16 and the fused ring")
         self.schedule = schedule
         self.group = group if schedule == "hierarchical" else None
         if self.group is not None and (group < 1 or p % group):
@@ -316,6 +320,8 @@ class AllReduce(Workload):
         self.kernel = ("ring_step" if literal else "fold" if schedule == "ring"
                        else "hier" if schedule == "hierarchical" else "schedule")
         tag = "" if schedule == "ring" else f"_{schedule}" + (f"_g{group}" if self.group else "")
+        if wire == "bf16":
+            self.kernel, tag = "wire", "_bf16wire"
         self.kernel_key = f"{self.kernel}_ar{tag}_{dtype}_p{p}_n{self.n}"
         # literal engine: set-up move + (p-1) reduce-scatter steps + (bf16: rounding
         # move) + (p-1) all-gather steps
@@ -325,6 +331,8 @@ class AllReduce(Workload):
         kind = "literal ring" if self.literal else f"fused {self.schedule.replace('_', ' ')}"
         if self.group is not None:
             kind += f" ({self.p // self.group} groups of {self.group})"
+        if self.wire == "bf16":
+            kind += " (bf16 partials on the wire)"
         cfg = {"workload": f"{kind} all-reduce: p={self.p} ranks x {self.mib} MiB {self.dtype} per rank",
                "p": self.p, "n_per_rank": self.n, "inputs": f"U(-1,1) seed {self.seed}"}
         if self.group is not None:
@@ -349,6 +357,10 @@ class AllReduce(Workload):
 
     def oracle_sample(self, frac):
         from oracle import ring, schedules
+        if self.wire == "bf16":
+            return oracle_prefix_sample(self.send, self.n, frac,
+                                        lambda xs: ring.ring_allreduce(xs, self.dtype, self.op, wire="bf16"),
+                                        2 * self.p * self.e, "oracle ring all-reduce, bf16 wire")
         if self.schedule == "hierarchical":
             return oracle_prefix_sample(
                 self.send, self.n, frac,
@@ -367,6 +379,8 @@ class AllReduce(Workload):
         if self.literal:
             self.lib.ccl_ring_allreduce_literal(self.send, self.recv, op=self.op,
                                                 workspace=self.ws, stream=stream)
+        elif self.wire == "bf16":
+            self.lib.ccl_allreduce_bf16_wire(self.send, self.recv, stream=stream)
         elif self.schedule == "hierarchical":
             self.lib.ccl_allreduce_hierarchical(self.send, self.recv, self.group, op=self.op,
                                                 stream=stream)
@@ -378,14 +392,16 @@ class AllReduce(Workload):
 
 
 class ReduceScatter(AllReduce):
-    def __init__(self, p=16, mib=192, dtype="bf16", seed=2):
-        super().__init__(p, mib, dtype, seed)
+    def __init__(self, p=16, mib=192, dtype="bf16", seed=2, wire="fp32"):
+        super().__init__(p, mib, dtype, seed, wire=wire)
         self.name = "reduce_scatter"
-        self.kernel_key = f"fold_rs_{dtype}_p{p}_n{self.n}"
+        self.kernel_key = (f"wire_rs_{dtype}_p{p}_n{self.n}" if wire == "bf16"
+                           else f"fold_rs_{dtype}_p{p}_n{self.n}")
 
     def config(self):
         c = super().config()
-        c["workload"] = f"fused reduce-scatter: p={self.p} ranks x {self.mib} MiB {self.dtype} per rank"
+        wire = " (bf16 partials on the wire)" if self.wire == "bf16" else ""
+        c["workload"] = f"fused reduce-scatter{wire}: p={self.p} ranks x {self.mib} MiB {self.dtype} per rank"
         return c
 
     def bytes_per_step(self):
@@ -397,12 +413,15 @@ class ReduceScatter(AllReduce):
                                    device=device) for k in range(self.p)]
 
     def step(self, stream):
-        self.lib.ccl_reduce_scatter(self.send, self.shards, stream=stream)
+        if self.wire == "bf16":
+            self.lib.ccl_reduce_scatter_bf16_wire(self.send, self.shards, stream=stream)
+        else:
+            self.lib.ccl_reduce_scatter(self.send, self.shards, stream=stream)
 
     def oracle_sample(self, frac):
         from oracle import ring
         return oracle_prefix_sample(self.send, self.n, frac,
-                                    lambda xs: ring.ring_reduce_scatter(xs, self.dtype, "sum"),
+                                    lambda xs: ring.ring_reduce_scatter(xs, self.dtype, "sum", self.wire),
                                     (self.p + 1) * self.e, "oracle ring reduce-scatter")
 
 
@@ -790,11 +809,12 @@ def make_workload(a) -> Workload:
         return Bucket()
     if a.workload == "allreduce":
         return AllReduce(p=a.p or 16, mib=a.mib or 256, dtype=a.dtype, schedule=a.schedule,
-                         group=a.group)
+                         group=a.group, wire=a.wire)
     if a.workload == "literal":
         return AllReduce(p=a.p or 8, mib=a.mib or 25, dtype=a.dtype, literal=True)
     if a.workload == "reduce_scatter":
-        return ReduceScatter(p=a.p or 16, mib=a.mib or 192, dtype=a.dtype if a.dtype != "f32" else "bf16")
+        return ReduceScatter(p=a.p or 16, mib=a.mib or 192, dtype=a.dtype if a.dtype != "f32" else "bf16",
+                             wire=a.wire)
     if a.workload == "all_gather":
         return AllGather(p=a.p or 16, mib=a.mib or 192, dtype=a.dtype if a.dtype != "f32" else "bf16")
     if a.workload == "zero":
@@ -1195,6 +1215,9 @@ def main(argv=None) -> int:
                     choices=["ring", "recursive_doubling", "rabenseifner", "binomial_tree", "naive",
                              "hierarchical"],
                     help="fold order of --workload allreduce")
+    ap.add_argument("--wire", default="fp32", choices=["fp32", "bf16"],
+                    help="bf16 all-reduce / reduce-scatter: partials travel in fp32 (default) or are "
+                         "rounded to bf16 at every hop")
     ap.add_argument("--group", type=int, default=8,
                     help="ranks per group of --schedule hierarchical (groups of consecutive ranks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

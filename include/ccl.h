@@ -128,6 +128,19 @@ ccl_status_t ccl_allreduce_schedule(const void* const* send, void* const* recv, 
                                     ccl_dtype_t dt, ccl_op_t op, ccl_schedule_t schedule,
                                     void* stream);
 
+/* bf16 all-reduce / reduce-scatter with bf16 on the wire: the ring of
+ * ccl_allreduce / ccl_reduce_scatter (same chunks, same order, same buffers
+ * and aliasing rules, bf16 data, SUM), except that every hop rounds the new
+ * partial to bf16 (nearest-even) before it travels on -- the partial a ring
+ * sends when its messages are bf16 ("Networks and Collective Communication"
+ * 5.1: each step moves one chunk; a bf16 chunk is half the bytes).  Chunk c
+ * = bf16(...bf16(bf16(x_{c+1} + x_{c+2}) + x_{c+3})... + x_c), each add in
+ * fp32.  For MAX / MIN rounding changes nothing: use ccl_allreduce. */
+ccl_status_t ccl_allreduce_bf16_wire(const void* const* send, void* const* recv, int p, size_t n,
+                                     void* stream);
+ccl_status_t ccl_reduce_scatter_bf16_wire(const void* const* send, void* const* recv, int p, size_t n,
+                                          void* stream);
+
 /* All-reduce with the result of the hierarchical (two-level ring) all-reduce
  * ("Networks and Collective Communication" 6.3; 6.1's two-dimensional
  * all-reduce on an a x b grid folds the same way), in one fused pass (same

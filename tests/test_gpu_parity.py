@@ -477,6 +477,77 @@ def test_schedule_argument_errors(lib):
         lib.ccl_allreduce_schedule(x, [torch.empty_like(t) for t in x], "naive", op="max")
 
 
+# ------------------------------------------------ bf16 on the wire
+WIRE_CASES = [(1, 10), (2, 4099), (3, 1001), (4, 70001), (8, 65536 + 3), (16, 1000), (72, 1000), (5, 4)]
+
+
+@pytest.mark.parametrize("p,n", WIRE_CASES)
+def test_bf16_wire_matches_oracle(lib, p, n):
+    x = make_inputs("bf16", p, n, seed=p * 13 + n)
+    send = [to_dev(v, "bf16") for v in x]
+    want, _, _ = ring.ring_allreduce(x, "bf16", wire="bf16")
+    outs = guarded_outputs(p, [n] * p, "bf16")
+    lib.ccl_allreduce_bf16_wire(send, [o.view for o in outs])
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], "bf16", f"bf16-wire AR rank {r}")
+        assert outs[r].guards_intact()
+    want_rs, _ = ring.ring_reduce_scatter(x, "bf16", wire="bf16")
+    shards = guarded_outputs(p, [ln for _, ln in ring.chunk_bounds(p, n)], "bf16", offset=GUARD + 1)
+    lib.ccl_reduce_scatter_bf16_wire(send, [g.view for g in shards])
+    for k in range(p):
+        assert_equal(to_host(shards[k].view), want_rs[k], "bf16", f"bf16-wire RS rank {k}")
+        assert shards[k].guards_intact()
+
+
+def test_bf16_wire_unaligned_and_in_place(lib):
+    p, n = 6, 10007
+    x = make_inputs("bf16", p, n, seed=21)
+    want, _, _ = ring.ring_allreduce(x, "bf16", wire="bf16")
+    ins = [Guarded(n, "bf16", offset=GUARD + 1) for _ in range(p)]
+    for g, v in zip(ins, x):
+        g.view.copy_(to_dev(v, "bf16"))
+    lib.ccl_allreduce_bf16_wire([g.view for g in ins], [g.view for g in ins])
+    for r in range(p):
+        assert_equal(to_host(ins[r].view), want[r], "bf16", f"in place rank {r}")
+        assert ins[r].guards_intact()
+
+
+def test_bf16_wire_hand_case_on_gpu(lib):
+    """The tie case of tests/test_oracle_bf16_wire.py on 3 x 4096 elements."""
+    n = 3 * 4096
+    send = [torch.full((n,), v, dtype=torch.bfloat16, device="cuda") for v in (2.0**-8, 1.0, 2.0**-8)]
+    recv = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    lib.ccl_allreduce_bf16_wire(send, recv)
+    want = np.repeat(np.array([1.0, 1.0 + 2.0**-7, 1.0], dtype=np.float32), 4096)
+    for r in range(3):
+        np.testing.assert_array_equal(recv[r].float().cpu().numpy(), want)
+    fp32 = [torch.empty_like(t) for t in recv]
+    lib.ccl_allreduce(send, fp32)
+    assert (fp32[0].float() == 1.0 + 2.0**-7).all()
+
+
+def test_bf16_wire_full_size_sampled(lib):
+    """The ZeRO reduce-scatter size (p=16, 192 MiB bf16 per rank), sampled."""
+    p, n = 16, 192 * (1 << 20) // 2
+    idx = sample_indices(n, p, 1 << 17, seed=77)
+    idx_t = torch.from_numpy(idx).cuda()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2)
+    send = [(torch.randn(n, generator=gen, device="cuda") * 1e-2).to(torch.bfloat16) for _ in range(p)]
+    cols = [to_host(v[idx_t]) for v in send]
+    recv = [torch.empty_like(v) for v in send]
+    lib.ccl_allreduce_bf16_wire(send, recv)
+    want = pointwise.allreduce_at_columns(cols, idx, n, "bf16", wire="bf16")
+    for r in (0, 7, 15):
+        assert_equal(to_host(recv[r][idx_t]), want, "bf16", f"bf16-wire 192 MiB rank {r}")
+
+
+def test_bf16_wire_rejects_other_dtypes(lib):
+    x = [torch.ones(8, device="cuda") for _ in range(2)]
+    with pytest.raises(ValueError):
+        lib.ccl_allreduce_bf16_wire(x, [torch.empty_like(t) for t in x])
+
+
 # ------------------------------------------- hierarchical / 2-D two-level ring
 # (p, group, n): 2 nodes x 8, 4 x 2, 3 x 3 with sub-chunks that start off the
 # 16-byte grid, one group (the flat ring), groups of one, tiny n (empty
