@@ -197,22 +197,26 @@ __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_con
   __shared__ int64_t pos[kMaxTokensPerCta][kMoeMaxK];
   __shared__ int dest[kMaxTokensPerCta][kMoeMaxK];
   __shared__ int expert[kMaxTokensPerCta][kMoeMaxK];
+  __shared__ char* rowp[kMaxTokensPerCta][kMoeMaxK];   // destination row, NULL if none
+  __shared__ float* sclp[kMaxTokensPerCta][kMoeMaxK];  // its block scales (FP8)
   pdl_enter();
   const int s = blockIdx.y;
   const int k = a.k, tpc = a.tpc;
+  const uint64_t h = a.hidden;
   const uint64_t t0 = static_cast<uint64_t>(blockIdx.x) * tpc;
   row_bases(a.counts, a.p, s, base);
   __syncthreads();
   token_rows(a, s, t0, tpc, base, dest, pos, expert, nullptr, static_cast<float (*)[kMoeMaxK]>(nullptr));
   __syncthreads();
-  if (a.rexp_given) {
-    for (int i = threadIdx.x; i < tpc * k; i += kThreads) {
-      const int tt = i / k, j = i - (i / k) * k;
-      const int d = dest[tt][j];
-      if (d >= 0 && a.rexp[d] != nullptr) a.rexp[d][pos[tt][j]] = expert[tt][j];
-    }
+  for (int i = threadIdx.x; i < tpc * k; i += kThreads) {
+    const int tt = i / k, j = i - (i / k) * k;
+    const int d = dest[tt][j];
+    const uint64_t row = static_cast<uint64_t>(pos[tt][j]);
+    rowp[tt][j] = (d >= 0) ? static_cast<char*>(a.recv[d]) + row * h * (FP8 ? 1 : 2) : nullptr;
+    sclp[tt][j] = (FP8 && d >= 0) ? a.scales[d] + row * (h / 128) : nullptr;
+    if (a.rexp_given && d >= 0 && a.rexp[d] != nullptr) a.rexp[d][row] = expert[tt][j];
   }
-  const uint64_t h = a.hidden;
+  __syncthreads();
   const uint32_t nv = static_cast<uint32_t>(h / EPI);  // items per token row
   const uint64_t left = a.tokens - t0;
   const uint32_t ntok = static_cast<uint32_t>(left < static_cast<uint64_t>(tpc) ? left : tpc);
@@ -228,7 +232,6 @@ __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_con
       v[u] = f - tt[u] * nv;
       if (f < total) {
         const char* row = xs + (t0 + tt[u]) * h * 2;
-#pragma unroll
         if constexpr (FP8) {
           // the item's 32 bytes are two 16-byte loads; they allocate in L1 so
           // that the second finds the sector the first brought in
@@ -249,10 +252,10 @@ __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_con
     for (int u = 0; u < U; ++u) {
       if (f0 + u * kThreads >= total) continue;  // whole aligned groups of 8 lanes drop out together
       if constexpr (!FP8) {
+        const uint4 q = make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
         for (int j = 0; j < k; ++j) {
-          const int d = dest[tt[u]][j];
-          if (d >= 0)
-            store_raw<kBF16, 8>(a.recv[d], static_cast<uint64_t>(pos[tt[u]][j]) * h + static_cast<uint64_t>(v[u]) * 8, w[u]);
+          char* row = rowp[tt[u]][j];
+          if (row != nullptr) st_stream16(row + static_cast<uint64_t>(v[u]) * 16, q);
         }
       } else {
         float x[16];
@@ -267,20 +270,22 @@ __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_con
         for (int off = 4; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(group, amax, off));
         const float inv = (amax > 0.0f) ? __fdiv_rn(448.0f, amax) : 1.0f;
         const float scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        // two codes per conversion (element 2e in the low byte, 2e+1 above it)
         uint32_t q[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t c = __nv_cvt_float_to_fp8(__fmul_rn(x[e], inv), __NV_SATFINITE, __NV_E4M3);
-          q[e >> 2] |= (c & 0xFFu) << (8 * (e & 3));
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t c2 = __nv_cvt_float2_to_fp8x2(
+              make_float2(__fmul_rn(x[2 * e], inv), __fmul_rn(x[2 * e + 1], inv)), __NV_SATFINITE, __NV_E4M3);
+          q[e >> 1] |= (c2 & 0xFFFFu) << (16 * (e & 1));
         }
+        const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
         const uint64_t blk = v[u] / 8;  // 8 items of 16 = one 128-element block
+        const bool lead = (threadIdx.x & 7) == 0;
         for (int j = 0; j < k; ++j) {
-          const int d = dest[tt[u]][j];
-          if (d < 0) continue;
-          const uint64_t row = static_cast<uint64_t>(pos[tt[u]][j]);
-          st_stream16(static_cast<char*>(a.recv[d]) + row * h + static_cast<uint64_t>(v[u]) * 16,
-                      make_uint4(q[0], q[1], q[2], q[3]));
-          if ((threadIdx.x & 7) == 0) a.scales[d][row * (h / 128) + blk] = scale;
+          char* row = rowp[tt[u]][j];
+          if (row == nullptr) continue;
+          st_stream16(row + static_cast<uint64_t>(v[u]) * 16, qv);
+          if (lead) sclp[tt[u]][j][blk] = scale;
         }
       }
     }
