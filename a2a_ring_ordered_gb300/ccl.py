@@ -47,6 +47,7 @@ def _load() -> ctypes.CDLL:
         "ccl_last_error": (ctypes.c_char_p, []),
         "ccl_kernel_launch_count": (u64, []),
         "ccl_chunk_bounds": (st, [i32, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
+        "ccl_device_error_flag": (st, [ctypes.POINTER(ctypes.c_uint), i32]),
         "ccl_allreduce": (st, [pp, pp, i32, sz, i32, i32, vp]),
         "ccl_allreduce_schedule": (st, [pp, pp, i32, sz, i32, i32, i32, vp]),
         "ccl_allreduce_hierarchical": (st, [pp, pp, i32, i32, sz, i32, i32, vp]),
@@ -171,6 +172,13 @@ def ccl_last_error() -> str:
 
 def ccl_kernel_launch_count() -> int:
     return LIB.ccl_kernel_launch_count()
+
+
+def ccl_device_error_flag(clear: bool = False) -> int:
+    """The device error word (nonzero once a bounded device-side wait ran out)."""
+    flag = ctypes.c_uint(0)
+    _check(LIB.ccl_device_error_flag(ctypes.byref(flag), 1 if clear else 0), "ccl_device_error_flag")
+    return int(flag.value)
 
 
 def ccl_chunk_bounds(p: int, n: int, c: int) -> tuple[int, int]:

@@ -4,6 +4,7 @@
 // Everything here is host code.  Invalid arguments are rejected before any
 // CUDA call, so the checks run (and are tested) on machines without a GPU.
 #include <stdarg.h>
+#include <stdlib.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -222,6 +223,14 @@ extern "C" uint64_t ccl_kernel_launch_count(void) {
   return g_launches.load(std::memory_order_relaxed);
 }
 
+extern "C" ccl_status_t ccl_device_error_flag(unsigned int* flag, int clear) {
+  clear_error();
+  if (flag == nullptr) return fail(CCL_ERR_INVALID_ARG, "flag is NULL");
+  cudaError_t err = read_device_error(flag, clear != 0);
+  if (err != cudaSuccess) return cuda_fail(err, "reading the device error word");
+  return CCL_OK;
+}
+
 extern "C" ccl_status_t ccl_chunk_bounds(int p, size_t n, int c, size_t* off, size_t* len) {
   clear_error();
   ccl_status_t st = check_p(p);
@@ -374,6 +383,39 @@ extern "C" ccl_status_t ccl_reduce_scatter(const void* const* send, void* const*
   return fused_reduce(kModeReduceScatter, send, recv, p, n, dt, op, stream);
 }
 
+namespace {
+// The bulk-copy fan-out (bulk_fanout.cu) is an alternative to the thread-store
+// all-gather and broadcast kernels, taken when the environment variable
+// CCL_FORCE_VARIANT is "tma" and the call is large, all device memory and
+// meets the bulk copies' 16-byte rule.  It is not the default: on GB300 the
+// thread stores reach 0.99 of the copy bandwidth at p = 16 and the best bulk
+// pipeline (two 64 KB stages) 0.95.
+#ifndef CCL_FANOUT_MIN_CHUNK
+#define CCL_FANOUT_MIN_CHUNK (1ull << 20)
+#endif
+constexpr uint64_t kFanoutMinChunk = CCL_FANOUT_MIN_CHUNK;
+
+bool device_memory(const void* ptr) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error state of a failed query
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice;
+}
+
+bool use_fanout(const FanoutArgs& f) {
+  const char* variant = getenv("CCL_FORCE_VARIANT");
+  if (variant == nullptr || strcmp(variant, "tma") != 0) return false;
+  if (f.chunk_bytes < kFanoutMinChunk || !fanout_supported(f)) return false;
+  for (int r = 0; r < f.p; ++r)
+    if (!device_memory(f.recv[r])) return false;
+  for (uint64_t c = 0; c < f.nchunks; ++c)
+    if (!device_memory(f.send[c])) return false;
+  return true;
+}
+}  // namespace
+
 extern "C" ccl_status_t ccl_all_gather(const void* const* send, void* const* recv, int p, size_t n,
                                        ccl_dtype_t dt, void* stream) {
   CCL_TRACE();
@@ -389,6 +431,22 @@ extern "C" ccl_status_t ccl_all_gather(const void* const* send, void* const* rec
   a.p = p;
   a.q = n / static_cast<uint64_t>(p);
   a.rem = n % static_cast<uint64_t>(p);
+  if (a.rem == 0) {
+    FanoutArgs f;
+    memset(&f, 0, sizeof(f));
+    for (int r = 0; r < p; ++r) {
+      f.send[r] = send[r];
+      f.recv[r] = recv[r];
+    }
+    f.p = p;
+    f.chunk_bytes = a.q * elem_bytes(dt);
+    f.nchunks = static_cast<uint64_t>(p);
+    if (use_fanout(f)) {
+      cudaError_t err = launch_fanout(f, as_stream(stream));
+      if (err != cudaSuccess) return cuda_fail(err, "all-gather bulk fan-out launch");
+      return CCL_OK;
+    }
+  }
   const bool vec = all_aligned16(send, p, const_cast<const void* const*>(recv));
   cudaError_t err = launch_gather(dt, vec, a, as_stream(stream));
   if (err != cudaSuccess) return cuda_fail(err, "all-gather kernel launch");
@@ -408,7 +466,7 @@ extern "C" ccl_status_t ccl_bucket_allreduce_scale_cast(const float* const* grad
   if (n == 0) return CCL_OK;
   const void* const* send = reinterpret_cast<const void* const*>(grads);
   uint64_t in_bytes[CCL_MAX_RANKS], out_bytes[CCL_MAX_RANKS];
-  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS] = {}, out[CCL_MAX_RANKS] = {};
   for (int r = 0; r < p; ++r) {
     in_bytes[r] = n * 4;
     out_bytes[r] = n * 2;
@@ -492,6 +550,20 @@ extern "C" ccl_status_t ccl_broadcast(const void* send, void* const* recv, int p
   a.send[0] = send;
   for (int r = 0; r < p; ++r) a.recv[r] = recv[r];
   a.p = p;
+  {
+    FanoutArgs f;
+    memset(&f, 0, sizeof(f));
+    f.send[0] = send;
+    for (int r = 0; r < p; ++r) f.recv[r] = recv[r];
+    f.p = p;
+    f.chunk_bytes = n * e;
+    f.nchunks = 1;
+    if (use_fanout(f)) {
+      cudaError_t err = launch_fanout(f, as_stream(stream));
+      if (err != cudaSuccess) return cuda_fail(err, "broadcast bulk fan-out launch");
+      return CCL_OK;
+    }
+  }
   bool vec = (reinterpret_cast<uintptr_t>(send) & 15) == 0;
   for (int r = 0; r < p; ++r) vec = vec && (reinterpret_cast<uintptr_t>(recv[r]) & 15) == 0;
   cudaError_t err = launch_broadcast(dt, vec, a, n, as_stream(stream));

@@ -50,6 +50,19 @@ struct GatherArgs {
   int p;
 };
 cudaError_t launch_gather(int dt, bool vec, const GatherArgs& a, cudaStream_t s);
+// Fan-out through bulk copies: chunk c (chunk_bytes from send[c], or from
+// send[0] when nchunks == 1) goes to byte offset c * chunk_bytes of every
+// recv[r].  All-gather: nchunks = p; broadcast: nchunks = 1.
+struct FanoutArgs {
+  const void* send[CCL_MAX_RANKS];
+  void* recv[CCL_MAX_RANKS];
+  uint64_t chunk_bytes, nchunks, tiles_per_chunk;
+  int p;
+};
+bool fanout_supported(const FanoutArgs& a);  // alignment rules of the bulk copies
+cudaError_t launch_fanout(FanoutArgs a, cudaStream_t s);
+// The device error word set by a bounded wait that ran out (0 if none).
+cudaError_t read_device_error(unsigned int* flag, bool clear);
 // Broadcast: send[0] (n elements) copied to recv[0..p-1]; `vec`: all 16-byte aligned.
 cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, cudaStream_t s);
 

@@ -97,6 +97,13 @@ const char* ccl_last_error(void);
 /* Number of kernels this library has launched in this process (all threads). */
 uint64_t ccl_kernel_launch_count(void);
 
+/* The device error word: nonzero once a bounded device-side wait ran out (the
+ * bulk-copy fan-out of ccl_all_gather / ccl_broadcast waits on its own copies
+ * with a bound; no wait of this library depends on another launch or rank).
+ * Synchronous (reads device memory); clear != 0 resets it to 0 afterwards.
+ * Errors: flag NULL -> CCL_ERR_INVALID_ARG; a failed copy -> CCL_ERR_CUDA. */
+ccl_status_t ccl_device_error_flag(unsigned int* flag, int clear);
+
 /* Chunk c of an n-element buffer cut into p chunks (the rule under CHUNKS AND
  * ORDER; numpy's array_split).  Host only.  Errors: p outside 1..CCL_MAX_RANKS,
  * c outside 0..p-1, or a NULL output pointer -> CCL_ERR_INVALID_ARG. */
@@ -170,14 +177,19 @@ ccl_status_t ccl_reduce_scatter(const void* const* send, void* const* recv, int 
  *   send[k]  p device pointers; send[k] holds len(k) elements (block k).
  *   recv[r]  p device pointers, each n elements; block k lands at off(k).
  *            In place is allowed only as send[k] == recv[k] + off(k)
- *            elements.  Pure copy: bit-exact for every dtype. */
+ *            elements.  Pure copy: bit-exact for every dtype.  With the
+ *            environment variable CCL_FORCE_VARIANT=tma, calls where p divides
+ *            n, blocks are >= 1 MiB and every buffer is 16-byte aligned device
+ *            memory run on the bulk-copy engine (one read into shared memory,
+ *            p bulk stores) instead of the default thread stores. */
 ccl_status_t ccl_all_gather(const void* const* send, void* const* recv, int p, size_t n,
                             ccl_dtype_t dt, void* stream);
 
 /* Broadcast ("Networks and Collective Communication" 4.1: the root's data is
  * copied to everyone).  send: the root's n elements; recv[r]: p outputs of n
  * elements; recv[root] == send is allowed (in place).  One read of the root's
- * data, p writes. */
+ * data, p writes (on the bulk-copy engine under the all-gather's opt-in and
+ * conditions, with n * bytes >= 1 MiB). */
 ccl_status_t ccl_broadcast(const void* send, void* const* recv, int p, size_t n, ccl_dtype_t dt,
                            int root, void* stream);
 

@@ -344,6 +344,64 @@ def test_all_to_allv_many_blocks(lib, p, row, hi):
         assert_equal(to_host(recv[d]), want[d], "bf16", f"rank {d}")
 
 
+# ------------------------------------------- bulk-copy fan-out (TMA bulk)
+# with CCL_FORCE_VARIANT=tma, all-gather / broadcast calls with blocks >= 1 MiB,
+# p | n and aligned device buffers run on the bulk-copy engine: whole tiles, a
+# partial last tile when a block is not a whole number of tiles, 1 to 24 ranks
+
+
+@pytest.fixture
+def tma(monkeypatch):
+    monkeypatch.setenv("CCL_FORCE_VARIANT", "tma")
+    yield
+
+
+
+@pytest.mark.parametrize("dtype,p,block", [("bf16", 16, 1 << 20), ("f32", 2, (1 << 18) + 12),
+                                           ("f32", 24, 1 << 18), ("bf16", 1, 1 << 21), ("f32", 5, 300_004)])
+def test_bulk_fanout_all_gather(lib, tma, dtype, p, block):
+    n = p * block
+    shards_np = make_inputs(dtype, p, block, seed=p + block)  # rank k's block
+    want, _ = ring.ring_all_gather(shards_np, dtype)
+    outs = guarded_outputs(p, [n] * p, dtype)
+    lib.ccl_device_error_flag(clear=True)
+    lib.ccl_all_gather([to_dev(v, dtype) for v in shards_np], [o.view for o in outs])
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"fan-out all-gather rank {r}")
+        assert outs[r].guards_intact()
+    assert lib.ccl_device_error_flag() == 0
+
+
+def test_bulk_fanout_all_gather_in_place(lib, tma):
+    p, block = 8, 1 << 18  # 1 MiB fp32 blocks
+    n = p * block
+    x = make_inputs("f32", p, n, seed=3)
+    want, _ = ring.ring_all_gather([x[k][k * block:(k + 1) * block].copy() for k in range(p)], "f32")
+    bufs = [to_dev(v, "f32") for v in x]  # block k already sits at off(k) of rank k's buffer
+    lib.ccl_all_gather([bufs[k][k * block:(k + 1) * block] for k in range(p)], bufs)
+    for r in range(p):
+        assert_equal(to_host(bufs[r]), want[r], "f32", f"in-place all-gather rank {r}")
+
+
+@pytest.mark.parametrize("dtype,p,n,root", [("f32", 16, (1 << 24) + 4, 0), ("bf16", 3, 1 << 20, 2)])
+def test_bulk_fanout_broadcast(lib, tma, dtype, p, n, root):
+    data = make_inputs(dtype, 1, n, seed=p + root)[0]  # the root's buffer
+    outs = guarded_outputs(p, [n] * p, dtype)
+    lib.ccl_broadcast(to_dev(data, dtype), [o.view for o in outs], root=root)
+    want = [data] * p
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"fan-out broadcast rank {r}")
+        assert outs[r].guards_intact()
+    # in place: the root's buffer is its own output
+    bufs = [torch.empty(n, dtype=torch.float32 if dtype == "f32" else torch.bfloat16, device="cuda")
+            for _ in range(p)]
+    bufs[root].copy_(to_dev(data, dtype))
+    lib.ccl_broadcast(bufs[root], bufs, root=root)
+    for r in range(p):
+        assert_equal(to_host(bufs[r]), want[r], dtype, f"in-place broadcast rank {r}")
+    assert lib.ccl_device_error_flag() == 0
+
+
 # -------------------------------------------------------- literal engine
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
 @pytest.mark.parametrize("p,n", [(1, 100), (2, 4099), (4, 1 << 16), (5, 13), (8, 70001), (16, 1000)])
