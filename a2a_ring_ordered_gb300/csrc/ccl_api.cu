@@ -847,8 +847,8 @@ extern "C" ccl_status_t ccl_all_to_all_heads(const void* const* send, void* cons
   if (send == nullptr || recv == nullptr) return fail(CCL_ERR_INVALID_ARG, "send or recv array is NULL");
   const uint64_t n = seq_per_rank * heads * head_dim;  // elements per rank, both layouts
   if (n == 0) return CCL_OK;
-  uint64_t b[CCL_MAX_RANKS];
-  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  uint64_t b[CCL_MAX_RANKS] = {};
+  Span in[CCL_MAX_RANKS] = {}, out[CCL_MAX_RANKS] = {};
   for (int r = 0; r < p; ++r) {
     b[r] = n * e;
     in[r] = span(send[r], b[r]);
@@ -1119,7 +1119,7 @@ extern "C" ccl_status_t ccl_ring_reduce_scatter_literal(const void* const* send,
     return CCL_OK;
   }
   const size_t e = elem_bytes(dt);
-  uint64_t in_b[CCL_MAX_RANKS], out_b[CCL_MAX_RANKS];
+  uint64_t in_b[CCL_MAX_RANKS] = {}, out_b[CCL_MAX_RANKS] = {};
   for (int r = 0; r < p; ++r) {
     uint64_t off, len;
     chunk(p, n, r, &off, &len);
