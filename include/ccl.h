@@ -54,9 +54,10 @@ typedef enum {
   CCL_ERR_INVALID_ARG = 1, /* bad p, pointer, size, alignment or aliasing */
   CCL_ERR_UNSUPPORTED = 2, /* valid arguments this build does not implement */
   CCL_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
-  CCL_ERR_TIMEOUT = 4      /* reserved for a bounded wait that gave up; every kernel of this
-                              library is one-shot (no kernel waits on a flag that another
-                              launch writes), so no entry point returns it */
+  CCL_ERR_TIMEOUT = 4      /* reserved: no kernel of this library waits on a flag that another
+                              launch writes, and a bounded wait on a kernel's own copies that
+                              runs out is reported by ccl_device_error_flag (kernels run
+                              asynchronously), so no entry point returns it */
 } ccl_status_t;
 
 typedef enum { CCL_F32 = 0, CCL_BF16 = 1, CCL_I32 = 2 } ccl_dtype_t;
