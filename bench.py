@@ -141,6 +141,7 @@ KERNEL_SOURCES = {
                  "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "hier": ["a2a_ring_ordered_gb300/csrc/hier_fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "wire": ["a2a_ring_ordered_gb300/csrc/wire_fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
+    "fanout": ["a2a_ring_ordered_gb300/csrc/bulk_fanout.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "gather": ["a2a_ring_ordered_gb300/csrc/gather.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "a2av": ["a2a_ring_ordered_gb300/csrc/a2av.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "ring_step": ["a2a_ring_ordered_gb300/csrc/ring_step.cu",
