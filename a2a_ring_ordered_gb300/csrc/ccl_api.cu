@@ -395,13 +395,15 @@ namespace {
 #endif
 constexpr uint64_t kFanoutMinChunk = CCL_FANOUT_MIN_CHUNK;
 
+// Memory of the current device (not host memory, not another GPU's).
 bool device_memory(const void* ptr) {
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
-    cudaGetLastError();  // clear the sticky-free error state of a failed query
+    cudaGetLastError();  // clear the (non-sticky) error of a failed query
     return false;
   }
-  return at.type == cudaMemoryTypeDevice;
+  int dev = -1;
+  return at.type == cudaMemoryTypeDevice && cudaGetDevice(&dev) == cudaSuccess && at.device == dev;
 }
 
 bool use_fanout(const FanoutArgs& f) {
