@@ -911,7 +911,7 @@ def cpu_baseline(wl: Workload) -> dict | None:
         return None
     frac = min(1.0, 0.01 * 1.0 / max(t1, 1e-6))  # one sample of about a second
     t_s, nb, desc = wl.oracle_sample(frac)
-    reps = max(1, min(30, int(12.0 / max(t_s, 1e-6))))
+    reps = max(1, min(200, int(12.0 / max(t_s, 1e-6))))  # about 12 s of host work
     times = [t_s]
     for _ in range(reps - 1):
         dt, nb, desc = wl.oracle_sample(frac)
