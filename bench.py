@@ -181,6 +181,11 @@ class Workload:
     dtype = "f32"
     kernel = "fold"          # dominant kernel (sources for the traffic digest)
     kernel_key = ""          # key in profiles/traffic.json
+    # NCCL's conventions (algbw = a rank's message bytes / time, busbw = algbw
+    # x the schedule factor: 2(p-1)/p all-reduce, (p-1)/p reduce-scatter and
+    # all-gather), for comparison with published collective numbers
+    nccl_bytes_per_rank = 0
+    nccl_factor = 0.0
     launches_per_step = 1
 
     def config(self) -> dict:
@@ -224,6 +229,14 @@ class Bucket(Workload):
 
     def bytes_per_step(self):
         return self.p * self.n * 4 + self.p * self.n * 2
+
+    @property
+    def nccl_bytes_per_rank(self):
+        return self.n * 4
+
+    @property
+    def nccl_factor(self):
+        return 2.0 * (self.p - 1) / self.p
 
     def host_inputs(self):
         from a2a_ring_ordered_gb300 import workloads
@@ -343,6 +356,14 @@ class AllReduce(Workload):
     def bytes_per_step(self):
         return 2 * self.p * self.n * self.e
 
+    @property
+    def nccl_bytes_per_rank(self):
+        return self.n * self.e
+
+    @property
+    def nccl_factor(self):
+        return 2.0 * (self.p - 1) / self.p
+
     def setup(self, lib, torch, device):
         self.lib, self.torch = lib, torch
         gen = torch.Generator(device=device)
@@ -408,6 +429,10 @@ class ReduceScatter(AllReduce):
     def bytes_per_step(self):
         return self.p * self.n * self.e + self.n * self.e
 
+    @property
+    def nccl_factor(self):
+        return (self.p - 1) / self.p
+
     def setup(self, lib, torch, device):
         super().setup(lib, torch, device)
         self.shards = [torch.empty(lib.ccl_chunk_bounds(self.p, self.n, k)[1], dtype=self.send[0].dtype,
@@ -457,6 +482,7 @@ class AllGather(ReduceScatter):
 
 
 class Zero(ReduceScatter):
+    nccl_bytes_per_rank = 0  # a chain of two collectives: no single NCCL figure
     """ZeRO chain: reduce-scatter of bf16 gradients (fp32 accumulation) then
     all-gather of the shards.  p=16, 192 MiB bf16 per rank, N(0, 1e-2), seed 2."""
     launches_per_step = 2
@@ -1107,6 +1133,11 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU, p virtual ranks in HBM"
     cfg["timing"] = ("eager Python calls" if a.eager else
                      f"CUDA graph of {group} steps replayed {a.steps // group} times")
+    nccl = None
+    if wl.nccl_bytes_per_rank:
+        algbw = wl.nccl_bytes_per_rank / (ms_step * 1e-3) / 1e9
+        nccl = {"algbw_gbs": round(algbw, 2), "busbw_gbs": round(algbw * wl.nccl_factor, 2),
+                "note": "NCCL conventions, for comparison with network figures only"}
     out = {
         "metric": "effective GB/s (primitive minimum bytes / step time) and fraction of HBM roofline",
         "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": a.steps,
@@ -1118,6 +1149,8 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
     }
     if e2e is not None:
         out["e2e"] = e2e
+    if nccl is not None:
+        out["nccl_style"] = nccl
     if hasattr(wl, "overlap_report"):
         out["overlap"] = wl.overlap_report()
     if world == 1 and not a.no_cpu_baseline:
