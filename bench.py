@@ -482,10 +482,10 @@ class AllGather(ReduceScatter):
 
 
 class Zero(ReduceScatter):
-    nccl_bytes_per_rank = 0  # a chain of two collectives: no single NCCL figure
     """ZeRO chain: reduce-scatter of bf16 gradients (fp32 accumulation) then
     all-gather of the shards.  p=16, 192 MiB bf16 per rank, N(0, 1e-2), seed 2."""
     launches_per_step = 2
+    nccl_bytes_per_rank = 0  # a chain of two collectives: no single NCCL figure
 
     def __init__(self, p=16, mib=192):
         super().__init__(p, mib, "bf16", 2)
