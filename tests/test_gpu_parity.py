@@ -472,7 +472,7 @@ def test_sweep_largest_sizes_sampled(lib, dtype, p, mib):
     sampled positions."""
     e = 4 if dtype == "f32" else 2
     n = mib * (1 << 20) // e
-    idx = sample_indices(n, p, 1 << 18, seed=p)
+    idx = sample_indices(n, p, 1 << 20, seed=p)  # >= 1 M sampled elements (plus every chunk edge)
     idx_t = torch.from_numpy(idx).cuda()
     gen = torch.Generator(device="cuda")
     gen.manual_seed(4)
