@@ -43,8 +43,8 @@ def reduce(x: list[np.ndarray], root: int = 0) -> list[np.ndarray | None]:
 def reduce_ring(x: list[np.ndarray], root: int = 0, dtype: str = "f32", op: str = "sum"):
     """Reduce built as the ring's reduce-scatter followed by a gather of the
     shards to the root (the pages fix no order for reduce; this reading gives
-    the root exactly the ring all-reduce's bits).  Returns (root result, list
-    with None for the other ranks)."""
+    the root exactly the ring all-reduce's bits).  Returns one entry per
+    rank: the result at index ``root``, None for the other ranks."""
     from .ring import ring_reduce_scatter
 
     shards, _ = ring_reduce_scatter(x, dtype, op)
