@@ -166,3 +166,80 @@ def test_random_all_to_allv(lib, seed):
     lib.ccl_all_to_allv([o.view for o in outs], counts.T.copy(), back, row)
     for s in range(p):
         assert_equal(to_host(back[s]), send_np[s], dtype, f"a2av combine seed {seed} rank {s}")
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_moe_route_dispatch_combine(lib, seed):
+    from oracle import moe
+    rng = np.random.default_rng(600 + seed)
+    p = int(rng.choice([1, 2, 3, 4, 8, 16]))
+    epr = int(rng.choice([1, 2, 4]))
+    E = p * epr
+    k = int(rng.integers(1, min(E, 8) + 1))
+    T = int(rng.choice([1, 5, 33, 300, 1000]))
+    h = 128 * int(rng.choice([1, 2, 3, 8]))
+    fp8 = bool(rng.integers(0, 2))
+    ids = workloads.moe_topk_routing(p, T, k, E, seed=seed)
+    if T > 2:
+        ids[0][1, 0] = -1  # routes nowhere
+    toks = workloads.normal(p, T * h, 1.0, seed + 1, dtype="bf16")
+    d_ids = [torch.from_numpy(i).cuda() for i in ids]
+    counts = torch.empty(p * p, dtype=torch.int64, device="cuda")
+    slots = [torch.empty(T, k, dtype=torch.int32, device="cuda") for _ in range(p)]
+    lib.ccl_moe_route(d_ids, E, counts, slots)
+    flat = [i.reshape(-1) for i in ids]
+    want_c, want_s, _ = moe.route(flat, p, E)
+    np.testing.assert_array_equal(counts.cpu().numpy().reshape(p, p), want_c)
+    for s in range(p):
+        np.testing.assert_array_equal(slots[s].cpu().numpy().reshape(-1), want_s[s])
+    rows = want_c.sum(axis=0)
+    if fp8:
+        recv = [torch.empty(int(m), h, dtype=torch.uint8, device="cuda") for m in rows]
+        scales = [torch.empty(int(m), h // 128, device="cuda") for m in rows]
+    else:
+        recv = [torch.empty(int(m), h, dtype=torch.bfloat16, device="cuda") for m in rows]
+        scales = None
+    rexp = [torch.empty(int(m), dtype=torch.int32, device="cuda") for m in rows]
+    lib.ccl_moe_dispatch([to_dev(t, "bf16").view(T, h) for t in toks], d_ids, counts, slots, E, recv, scales,
+                         rexp, fp8=fp8)
+    w_rows, w_scales, w_exp, _, _ = moe.dispatch(toks, flat, p, k, E, h, fp8=fp8)
+    for d in range(p):
+        got = recv[d].cpu()
+        got = got.numpy() if fp8 else got.view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(got, w_rows[d], err_msg=f"dispatch seed {seed} rank {d}")
+        np.testing.assert_array_equal(rexp[d].cpu().numpy(), w_exp[d])
+        if fp8:
+            np.testing.assert_array_equal(scales[d].cpu().numpy(), w_scales[d])
+    y = [workloads.normal(1, max(int(m) * h, 1), 1.0, seed + 10 + d, dtype="bf16")[0][: int(m) * h].reshape(int(m), h)
+         for d, m in enumerate(rows)]
+    gw = workloads.moe_gate_weights(p, T, k, seed=seed + 2)
+    out = [torch.empty(T, h, dtype=torch.bfloat16, device="cuda") for _ in range(p)]
+    lib.ccl_moe_combine([to_dev(v.reshape(-1), "bf16").view(-1, h) for v in y], d_ids,
+                        [torch.from_numpy(w).cuda() for w in gw], counts, slots, E, out)
+    want_out = moe.combine(y, flat, gw, p, k, E, h)
+    for s in range(p):
+        np.testing.assert_array_equal(out[s].cpu().view(torch.int16).numpy().view(np.uint16).reshape(-1),
+                                      want_out[s], err_msg=f"combine seed {seed} rank {s}")
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_ulysses(lib, seed):
+    rng = np.random.default_rng(700 + seed)
+    p = int(rng.choice([1, 2, 4, 8]))
+    H = p * int(rng.choice([1, 2, 3]))
+    D = int(rng.choice([1, 3, 8, 64, 128]))
+    sp = int(rng.choice([1, 7, 64, 129]))
+    dtype = str(rng.choice(["f32", "bf16"]))
+    n = sp * H * D
+    x = _inputs(dtype, p, n, seed)
+    send = _placed(x, dtype, int(rng.integers(0, 2)))
+    outs = [Guarded(n, dtype, offset=GUARD + int(rng.integers(0, 2))) for _ in range(p)]
+    lib.ccl_all_to_all_heads([b.view for b in send], [o.view for o in outs], sp, H, D)
+    want = collectives.ulysses_seq_to_heads(x, H, D)
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"Ulysses seed {seed} p={p} H={H} D={D} sp={sp}")
+        assert outs[r].guards_intact()
+    back = [Guarded(n, dtype, offset=GUARD) for _ in range(p)]
+    lib.ccl_all_to_all_heads([o.view for o in outs], [b.view for b in back], sp, H, D, inverse=True)
+    for r in range(p):
+        assert_equal(to_host(back[r].view), x[r], dtype, f"Ulysses inverse seed {seed} rank {r}")
