@@ -26,11 +26,10 @@
 namespace ccl {
 namespace {
 
-constexpr int kBatch = 8;  // loads in flight per thread
 
 // Fold VEC elements at element i: rank sequence (group g0, local l0), then the
-// rest of that group's ring, then the next group, ...
-template <int DT, int VEC>
+// rest of that group's ring, then the next group, ...; BATCH loads in flight.
+template <int DT, int VEC, int BATCH>
 __device__ __forceinline__ void fold_two_level(const FoldArgs& f, int a, int b, int g0, int l0,
                                                uint64_t i, typename Elem<DT>::Acc* tot) {
   using Acc = typename Elem<DT>::Acc;
@@ -40,10 +39,10 @@ __device__ __forceinline__ void fold_two_level(const FoldArgs& f, int a, int b, 
   int g = g0, loc = l0;  // next rank to load
   int li = 0;            // position of the next folded value inside its group's ring
   bool first_group = true;
-  for (int k0 = 0; k0 < p; k0 += kBatch) {
-    uint32_t raw[kBatch][W];
+  for (int k0 = 0; k0 < p; k0 += BATCH) {
+    uint32_t raw[BATCH][W];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
+    for (int j = 0; j < BATCH; ++j) {
       if (k0 + j < p) {
         load_raw<DT, VEC>(f.send[g * a + loc], i, raw[j]);
         if (++loc == a) loc = 0;
@@ -51,7 +50,7 @@ __device__ __forceinline__ void fold_two_level(const FoldArgs& f, int a, int b, 
       }
     }
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
+    for (int j = 0; j < BATCH; ++j) {
       if (k0 + j < p) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
@@ -77,7 +76,7 @@ __device__ __forceinline__ void write_all(const FoldArgs& f, uint64_t i, typenam
 }
 
 // f.q, f.rem: the level-1 split, floor(n / a) and n mod a.
-template <int DT, int VEC>
+template <int DT, int VEC, int BATCH>
 __global__ void __launch_bounds__(kThreads, 2) hier_fold_kernel(const __grid_constant__ FoldArgs f, int a, int b) {
   using Acc = typename Elem<DT>::Acc;
   pdl_enter();
@@ -93,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 2) hier_fold_kernel(const __grid_con
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   for (uint64_t v = v_lo + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi; v += stride) {
     Acc acc[VEC];
-    fold_two_level<DT, VEC>(f, a, b, g0, l0, v * VEC, acc);
+    fold_two_level<DT, VEC, BATCH>(f, a, b, g0, l0, v * VEC, acc);
     write_all<DT, VEC>(f, v * VEC, acc);
   }
   if (VEC > 1 && blockIdx.x == 0) {
@@ -104,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 2) hier_fold_kernel(const __grid_con
     for (uint64_t t = threadIdx.x; t < n_edge; t += kThreads) {
       const uint64_t i = (t < n_head) ? off + t : tail_begin + (t - n_head);
       Acc acc[1];
-      fold_two_level<DT, 1>(f, a, b, g0, l0, i, acc);
+      fold_two_level<DT, 1, BATCH>(f, a, b, g0, l0, i, acc);
       write_all<DT, 1>(f, i, acc);
     }
   }
@@ -112,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 2) hier_fold_kernel(const __grid_con
 
 constexpr int kVectorsPerThread = 2;
 
-template <int DT, int VEC>
+template <int DT, int VEC, int BATCH>
 cudaError_t launch_one(const FoldArgs& f, int a, cudaStream_t s) {
   const int b = f.p / a;
   const uint64_t longest = (f.q + 1) / static_cast<uint64_t>(b) + 1;  // elements of the largest sub-chunk
@@ -130,16 +129,23 @@ cudaError_t launch_one(const FoldArgs& f, int a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = CCL_PDL ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, hier_fold_kernel<DT, VEC>, f, a, b);
+  return cudaLaunchKernelEx(&cfg, hier_fold_kernel<DT, VEC, BATCH>, f, a, b);
+}
+
+// Loads in flight per thread: 16 ranks' worth from p = 9 on, 8 below (measured
+// on GB300: 16 lifts p = 16 and p = 72 by 2-7 % and costs p = 8 4 %).
+template <int DT, int VEC>
+cudaError_t launch_batch(const FoldArgs& f, int a, cudaStream_t s) {
+  return f.p > 8 ? launch_one<DT, VEC, 16>(f, a, s) : launch_one<DT, VEC, 8>(f, a, s);
 }
 
 }  // namespace
 
 cudaError_t launch_hier_fold(int dt, bool vec, const FoldArgs& f, int a, cudaStream_t s) {
   cudaError_t err = cudaErrorInvalidValue;
-  if (dt == kF32) err = vec ? launch_one<kF32, 4>(f, a, s) : launch_one<kF32, 1>(f, a, s);
-  else if (dt == kBF16) err = vec ? launch_one<kBF16, 8>(f, a, s) : launch_one<kBF16, 1>(f, a, s);
-  else if (dt == kI32) err = vec ? launch_one<kI32, 4>(f, a, s) : launch_one<kI32, 1>(f, a, s);
+  if (dt == kF32) err = vec ? launch_batch<kF32, 4>(f, a, s) : launch_batch<kF32, 1>(f, a, s);
+  else if (dt == kBF16) err = vec ? launch_batch<kBF16, 8>(f, a, s) : launch_batch<kBF16, 1>(f, a, s);
+  else if (dt == kI32) err = vec ? launch_batch<kI32, 4>(f, a, s) : launch_batch<kI32, 1>(f, a, s);
   if (err == cudaSuccess) note_launch();
   return err;
 }
