@@ -8,7 +8,7 @@ devices holding the experts it chose) and combine (the expert outputs come
 back) -- each device sending about tokens x k x d x bytes x (EP-1)/EP; the
 DeepSeek-V3 recipe dispatches in FP8 and combines in BF16.
 
-Readings (listed in DESIGN.md):
+Readings taken where the pages are silent:
 
 * expert e lives on rank e // (E / p); a token that chose k experts is sent as
   k rows, one per choice (the page's tokens x k accounting);

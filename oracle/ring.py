@@ -15,7 +15,7 @@ Training Collectives", "Ring AllReduce"):
   complete chunk it received most recently to the next device;
 * every device sends n/p per step, 2(p-1) steps in all.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 1. Chunk split when p does not divide n: numpy's ``array_split`` rule --
    the first (n mod p) chunks get floor(n/p)+1 elements, the rest floor(n/p).

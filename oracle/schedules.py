@@ -20,7 +20,7 @@ GPUs of a node, or one row of an a x b torus); a ring reduce-scatter inside
 every group, a ring all-reduce across the groups among the devices with the
 same index inside their group, then a ring all-gather inside every group.
 
-Readings (listed in the design doc): a receiver computes (received partial) +
+Readings taken where the pages are silent: a receiver computes (received partial) +
 (own value) -- IEEE addition is commutative, so only the pairing matters;
 the halving step pairs devices at distance p/2 first and a device keeps the
 lower half of its range when its bit for that distance is clear, so device i
@@ -176,7 +176,7 @@ def hierarchical(x, group, dtype="f32", op="sum"):
     """Two-level ring all-reduce over b = p / group groups of `group`
     consecutive ranks (group g = ranks g*a .. g*a + a - 1, a = group).
 
-    Readings (listed in the design doc): every ring is the ring of ``oracle.ring``
+    Readings taken where the pages are silent: every ring is the ring of ``oracle.ring``
     (rank order inside its ring, chunk rule, chunk c starts after its owner);
     device (g, l) owns chunk l of the a chunks after step 1; in step 2 the
     ring over the groups for chunk l has group g at position g and cuts that

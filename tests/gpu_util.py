@@ -10,7 +10,7 @@ GUARD = 64  # elements of guard band on each side of an output (keeps 16-byte al
 
 
 def ccl():
-    """The binding, built first (on the GPU machine the build happens there)."""
+    """The binding, with the library built first if it is out of date."""
     if not torch.cuda.is_available():
         raise RuntimeError("GPU tests need a CUDA device")
     from a2a_ring_ordered_gb300 import build
