@@ -48,6 +48,8 @@ def _load() -> ctypes.CDLL:
         "ccl_kernel_launch_count": (u64, []),
         "ccl_chunk_bounds": (st, [i32, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
         "ccl_device_error_flag": (st, [ctypes.POINTER(ctypes.c_uint), i32]),
+        "ccl_stream_check": (st, [vp]),
+        "ccl_selftest_bounded_wait": (st, [vp]),
         "ccl_allreduce": (st, [pp, pp, i32, sz, i32, i32, vp]),
         "ccl_allreduce_schedule": (st, [pp, pp, i32, sz, i32, i32, i32, vp]),
         "ccl_allreduce_hierarchical": (st, [pp, pp, i32, i32, sz, i32, i32, vp]),
@@ -181,7 +183,22 @@ def ccl_device_error_flag(clear: bool = False) -> int:
     return int(flag.value)
 
 
+def ccl_stream_check(stream=None) -> None:
+    """Synchronize the stream; raise CclError(CCL_ERR_TIMEOUT) if a bounded
+    device-side wait ran out since the last check."""
+    _check(LIB.ccl_stream_check(_stream(stream, torch.device("cuda", torch.cuda.current_device()))),
+           "ccl_stream_check")
+
+
+def ccl_selftest_bounded_wait(stream=None) -> None:
+    """Enqueue a kernel whose bounded wait runs out by construction (self-test
+    of the failure path; nothing faults)."""
+    _check(LIB.ccl_selftest_bounded_wait(_stream(stream, torch.device("cuda", torch.cuda.current_device()))),
+           "ccl_selftest_bounded_wait")
+
+
 def ccl_chunk_bounds(p: int, n: int, c: int) -> tuple[int, int]:
+    """(offset, length) of chunk c of an n-element buffer cut into p chunks."""
     off, ln = ctypes.c_size_t(), ctypes.c_size_t()
     _check(LIB.ccl_chunk_bounds(p, n, c, ctypes.byref(off), ctypes.byref(ln)), "ccl_chunk_bounds")
     return off.value, ln.value

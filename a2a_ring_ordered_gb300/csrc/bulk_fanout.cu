@@ -18,8 +18,9 @@
 // offset and length are multiples of 16 bytes -- the bulk copies' rule -- and
 // all chunks have the same length (p divides n for the all-gather).  Waits
 // are bounded: a wait that runs out sets a device error word (read with
-// ccl_device_error_flag), waits once more with a bound for the copies still
-// in flight, and the CTA returns.
+// ccl_device_error_flag, or turned into CCL_ERR_TIMEOUT by ccl_stream_check),
+// waits once more with a bound for the copies still in flight, and the CTA
+// returns.
 #include "device_common.cuh"
 
 namespace ccl {
@@ -59,9 +60,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-// true once the barrier's phase `parity` has completed; false after the bound
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kWaitLimit; ++i) {
+// true once the barrier's phase `parity` has completed; false after `limit`
+// tries
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit = kWaitLimit) {
+  for (long long i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
@@ -168,7 +170,25 @@ __global__ void __launch_bounds__(32) fanout_kernel(const __grid_constant__ Fano
   bulk_wait_all();
 }
 
+// Self-test of the bounded-wait path: one thread waits on an mbarrier that no
+// arrival or copy will ever complete, gives up after `limit` tries, records
+// the error word as the fan-out does, and returns.  Nothing is in flight.
+__global__ void __launch_bounds__(32) bounded_wait_probe_kernel(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_addr(&bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (!mbar_wait(smem_addr(&bar), 0, limit)) atomicExch(&g_device_error, 2u);
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_probe(cudaStream_t s) {
+  bounded_wait_probe_kernel<<<1, 32, 0, s>>>(1ll << 14);
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) note_launch();
+  return err;
+}
 
 bool fanout_supported(const FanoutArgs& a) {
   if (a.chunk_bytes == 0 || a.chunk_bytes % 16 != 0) return false;

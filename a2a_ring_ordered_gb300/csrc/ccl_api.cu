@@ -231,6 +231,25 @@ extern "C" ccl_status_t ccl_device_error_flag(unsigned int* flag, int clear) {
   return CCL_OK;
 }
 
+extern "C" ccl_status_t ccl_stream_check(void* stream) {
+  clear_error();
+  cudaError_t err = cudaStreamSynchronize(as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "synchronizing the stream");
+  unsigned int flag = 0;
+  if ((err = read_device_error(&flag, true)) != cudaSuccess) return cuda_fail(err, "reading the device error word");
+  if (flag != 0)
+    return fail(CCL_ERR_TIMEOUT, "a bounded device-side wait ran out (error word %u)", flag);
+  return CCL_OK;
+}
+
+extern "C" ccl_status_t ccl_selftest_bounded_wait(void* stream) {
+  CCL_TRACE();
+  clear_error();
+  cudaError_t err = launch_bounded_wait_probe(as_stream(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "bounded-wait probe launch");
+  return CCL_OK;
+}
+
 extern "C" ccl_status_t ccl_chunk_bounds(int p, size_t n, int c, size_t* off, size_t* len) {
   clear_error();
   ccl_status_t st = check_p(p);

@@ -63,6 +63,8 @@ bool fanout_supported(const FanoutArgs& a);  // alignment rules of the bulk copi
 cudaError_t launch_fanout(FanoutArgs a, cudaStream_t s);
 // The device error word set by a bounded wait that ran out (0 if none).
 cudaError_t read_device_error(unsigned int* flag, bool clear);
+// One-thread kernel whose mbarrier wait runs out by construction (self-test).
+cudaError_t launch_bounded_wait_probe(cudaStream_t s);
 // Broadcast: send[0] (n elements) copied to recv[0..p-1]; `vec`: all 16-byte aligned.
 cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, cudaStream_t s);
 

@@ -54,10 +54,9 @@ typedef enum {
   CCL_ERR_INVALID_ARG = 1, /* bad p, pointer, size, alignment or aliasing */
   CCL_ERR_UNSUPPORTED = 2, /* valid arguments this build does not implement */
   CCL_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
-  CCL_ERR_TIMEOUT = 4      /* reserved: no kernel of this library waits on a flag that another
-                              launch writes, and a bounded wait on a kernel's own copies that
-                              runs out is reported by ccl_device_error_flag (kernels run
-                              asynchronously), so no entry point returns it */
+  CCL_ERR_TIMEOUT = 4      /* a bounded device-side wait ran out (kernels run asynchronously,
+                              so ccl_stream_check reports it); no kernel of this library waits
+                              on a flag that another launch writes */
 } ccl_status_t;
 
 typedef enum { CCL_F32 = 0, CCL_BF16 = 1, CCL_I32 = 2 } ccl_dtype_t;
@@ -104,6 +103,18 @@ uint64_t ccl_kernel_launch_count(void);
  * Synchronous (reads device memory); clear != 0 resets it to 0 afterwards.
  * Errors: flag NULL -> CCL_ERR_INVALID_ARG; a failed copy -> CCL_ERR_CUDA. */
 ccl_status_t ccl_device_error_flag(unsigned int* flag, int clear);
+
+/* Failure check after asynchronous work: synchronizes `stream`, then returns
+ * CCL_ERR_TIMEOUT (and clears the word) if a bounded device-side wait ran out
+ * since the last check, CCL_OK otherwise; the context stays usable either
+ * way.  A failed synchronization -> CCL_ERR_CUDA. */
+ccl_status_t ccl_stream_check(void* stream);
+
+/* Self-test of that path: enqueues a one-thread kernel whose mbarrier wait
+ * can never complete, so it gives up after a short bound (well under a
+ * millisecond) and sets the error word; no copy is in flight and nothing
+ * faults.  The next ccl_stream_check on `stream` returns CCL_ERR_TIMEOUT. */
+ccl_status_t ccl_selftest_bounded_wait(void* stream);
 
 /* Chunk c of an n-element buffer cut into p chunks (the rule under CHUNKS AND
  * ORDER; numpy's array_split).  Host only.  Errors: p outside 1..CCL_MAX_RANKS,
