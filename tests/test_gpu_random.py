@@ -243,3 +243,34 @@ def test_random_ulysses(lib, seed):
     lib.ccl_all_to_all_heads([o.view for o in outs], [b.view for b in back], sp, H, D, inverse=True)
     for r in range(p):
         assert_equal(to_host(back[r].view), x[r], dtype, f"Ulysses inverse seed {seed} rank {r}")
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_literal_engine(lib, seed):
+    """The 2(p-1)-step engine: bits and per-rank byte counters against the
+    literal simulation, for all-reduce, reduce-scatter and all-gather."""
+    rng, p, n, dtype, shift = _draw(800 + seed)
+    op = str(rng.choice(["sum", "max", "min"]))
+    x = _inputs(dtype, p, n, seed)
+    send = _placed(x, dtype, shift)
+    outs = [Guarded(n, dtype, offset=GUARD + int(rng.integers(0, 2))) for _ in range(p)]
+    sent = lib.ccl_ring_allreduce_literal([b.view for b in send], [o.view for o in outs], op=op)
+    want, rs_b, ag_b = ring.ring_allreduce(x, dtype, op)
+    assert list(sent) == [a + b for a, b in zip(rs_b, ag_b)]
+    for r in range(p):
+        assert_equal(to_host(outs[r].view), want[r], dtype, f"literal AR seed {seed} p={p} n={n} {op} rank {r}")
+        assert outs[r].guards_intact()
+    shards = [Guarded(ln, dtype, offset=GUARD + shift) for _, ln in ring.chunk_bounds(p, n)]
+    sent_rs = lib.ccl_ring_reduce_scatter_literal([b.view for b in send], [s.view for s in shards], op=op)
+    want_rs, rs_only = ring.ring_reduce_scatter(x, dtype, op)
+    assert list(sent_rs) == list(rs_only)
+    for k in range(p):
+        assert_equal(to_host(shards[k].view), want_rs[k], dtype, f"literal RS seed {seed} rank {k}")
+        assert shards[k].guards_intact()
+    full = [Guarded(n, dtype, offset=GUARD) for _ in range(p)]
+    sent_ag = lib.ccl_ring_all_gather_literal([s.view for s in shards], [f.view for f in full])
+    want_ag, ag_only = ring.ring_all_gather(want_rs, dtype)
+    assert list(sent_ag) == list(ag_only)
+    for r in range(p):
+        assert_equal(to_host(full[r].view), want_ag[r], dtype, f"literal AG seed {seed} rank {r}")
+        assert full[r].guards_intact()
