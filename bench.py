@@ -805,11 +805,13 @@ class Ulysses(Workload):
         return {"workload": f"Ulysses head<->sequence all-to-all: p={self.p} ranks x {self.sp} tokens x "
                             f"{self.H} heads x {self.D} bf16, forward + inverse",
                 "p": self.p, "tokens_per_rank": self.sp, "heads": self.H, "head_dim": self.D,
-                "inputs": "N(0,1) drawn on the device"}
+                "inputs": "N(0,1) drawn on the device (torch Philox, seed 5)"}
 
     def setup(self, lib, torch, device):
         self.lib = lib
-        self.x = [torch.randn(self.n, device=device).to(torch.bfloat16) for _ in range(self.p)]
+        gen = torch.Generator(device=device)
+        gen.manual_seed(5)
+        self.x = [torch.randn(self.n, generator=gen, device=device).to(torch.bfloat16) for _ in range(self.p)]
         self.y = [torch.empty_like(t) for t in self.x]
         self.z = [torch.empty_like(t) for t in self.x]
 
