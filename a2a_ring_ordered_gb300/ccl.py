@@ -54,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "ccl_allreduce_schedule": (st, [pp, pp, i32, sz, i32, i32, i32, vp]),
         "ccl_allreduce_hierarchical": (st, [pp, pp, i32, i32, sz, i32, i32, vp]),
         "ccl_allreduce_bf16_wire": (st, [pp, pp, i32, sz, vp]),
+        "ccl_all_to_all": (st, [pp, pp, i32, sz, i32, vp]),
         "ccl_reduce_scatter_bf16_wire": (st, [pp, pp, i32, sz, vp]),
         "ccl_reduce_scatter": (st, [pp, pp, i32, sz, i32, i32, vp]),
         "ccl_all_gather": (st, [pp, pp, i32, sz, i32, vp]),
@@ -389,6 +390,19 @@ def ccl_bucket_allreduce_scale_cast(grads, out_bf16, scale: float | None = None,
                                                _ptr_array([t.data_ptr() for t in out]), p, n, s,
                                                _stream(stream, grads[0].device)),
            "ccl_bucket_allreduce_scale_cast")
+
+
+def ccl_all_to_all(send, recv, stream=None) -> None:
+    """Block transpose: recv[j] = block j of every send[i] (chunk rule), in
+    source order."""
+    send, recv = _tensors(send, "send"), _tensors(recv, "recv")
+    p, n = len(send), send[0].numel()
+    if len(recv) != p or recv[0].dtype != send[0].dtype:
+        raise ValueError("recv must hold p buffers of the send dtype")
+    _numel_check(send, [n] * p, "send")
+    _numel_check(recv, [p * ln for ln in _chunk_lengths(p, n)], "recv")
+    _check(LIB.ccl_all_to_all(_ptr_array([t.data_ptr() for t in send]), _ptr_array([t.data_ptr() for t in recv]),
+                              p, n, _dtype_code(send[0]), _stream(stream, send[0].device)), "ccl_all_to_all")
 
 
 def ccl_all_to_allv(send, counts, recv, row_elems: int, stream=None) -> None:

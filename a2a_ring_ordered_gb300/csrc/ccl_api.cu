@@ -966,6 +966,24 @@ extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* c
   return CCL_OK;
 }
 
+extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* recv, int p, size_t n,
+                                       ccl_dtype_t dt, void* stream) {
+  CCL_TRACE();
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  // block d of every source is chunk d (the chunk rule): counts[s][d] = len(d)
+  // elements, so destination d receives p blocks of len(d) in source order
+  static thread_local size_t counts[CCL_MAX_RANKS * CCL_MAX_RANKS];
+  for (int d = 0; d < p; ++d) {
+    uint64_t off, len;
+    chunk(p, n, d, &off, &len);
+    for (int src = 0; src < p; ++src) counts[static_cast<size_t>(src) * p + d] = len;
+  }
+  return ccl_all_to_allv(send, counts, recv, p, 1, dt, stream);
+}
+
 // ====================================================== literal ring engine
 namespace {
 

@@ -236,6 +236,14 @@ ccl_status_t ccl_gather(const void* const* send, void* recv, int p, size_t n, cc
 ccl_status_t ccl_bucket_allreduce_scale_cast(const float* const* grads, void* const* out_bf16,
                                              int p, size_t n, float scale, void* stream);
 
+/* All-to-all ("Networks and Collective Communication" 4.1: device i's block j
+ * goes to device j, a transpose).  send[i]: n elements cut into p blocks by
+ * the chunk rule; recv[j]: p * len(j) elements, block j of every source in
+ * source order.  ccl_all_to_allv with counts[s][d] = len(d) and one-element
+ * rows; applying it twice restores the inputs when p divides n. */
+ccl_status_t ccl_all_to_all(const void* const* send, void* const* recv, int p, size_t n, ccl_dtype_t dt,
+                            void* stream);
+
 /* All-to-all with per-pair counts: the MoE dispatch / combine block transpose
  * ("Networks and Collective Communication" 4.1: device i's block j goes to
  * device j; 7.4: MoE dispatch and combine).

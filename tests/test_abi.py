@@ -177,6 +177,18 @@ def test_all_to_allv_rejects_overlapping_receivers(lib):
                                    None) == lib.CCL_ERR_INVALID_ARG
 
 
+def test_all_to_all_checks(lib):
+    p = 4
+    s = [BASE + i * 4096 for i in range(p)]
+    r = [BASE + 65536 + i * 4096 for i in range(p)]
+    assert lib.LIB.ccl_all_to_all(lib_ptr_array(s), lib_ptr_array(r), p, 0, 0, None) == lib.CCL_OK
+    assert lib.LIB.ccl_all_to_all(lib_ptr_array(s), lib_ptr_array(r), 0, 8, 0, None) == lib.CCL_ERR_INVALID_ARG
+    # each destination receives 4 blocks of 4 f32 (64 bytes): 32 bytes apart overlaps
+    r_bad = [BASE + 65536 + i * 32 for i in range(p)]
+    assert lib.LIB.ccl_all_to_all(lib_ptr_array(s), lib_ptr_array(r_bad), p, 16, 0,
+                                  None) == lib.CCL_ERR_INVALID_ARG
+
+
 def test_literal_workspace_sizes_and_checks(lib):
     ws = lib.LIB.ccl_ring_literal_workspace_bytes
     assert ws(lib.CCL_KIND_ALLREDUCE, 4, 100, lib.CCL_F32) == 0

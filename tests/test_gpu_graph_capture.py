@@ -106,15 +106,17 @@ def test_all_to_allv_moe_and_ulysses_replay(lib):
     xu = workloads.normal(4, sp * H * D, 1.0, 46, dtype="bf16")
     su = [to_dev(v, "bf16") for v in xu]
     ru = [torch.empty_like(t) for t in su]
+    rt = [torch.empty_like(t) for t in su]
 
     def step(s):
         lib.ccl_all_to_allv(sa, counts, ra, row, stream=s)
         lib.ccl_moe_route(d_ids, E, counts_m, slots, stream=s)
         lib.ccl_moe_dispatch(d_x, d_ids, counts_m, slots, E, q, sc, fp8=True, stream=s)
         lib.ccl_all_to_all_heads(su, ru, sp, H, D, stream=s)
+        lib.ccl_all_to_all(su, rt, stream=s)
 
     g = _capture(step)
-    for t in ra + q + sc + ru:
+    for t in ra + q + sc + ru + rt:
         t.zero_()
     g.replay()
     torch.cuda.synchronize()
@@ -126,3 +128,5 @@ def test_all_to_allv_moe_and_ulysses_replay(lib):
         np.testing.assert_array_equal(sc[d].cpu().numpy(), w_sc[d])
     for r, w in enumerate(collectives.ulysses_seq_to_heads(xu, H, D)):
         assert_equal(to_host(ru[r]), w, "bf16", f"Ulysses rank {r}")
+    for r, w in enumerate(collectives.all_to_all(xu)):
+        assert_equal(to_host(rt[r]), w, "bf16", f"all-to-all rank {r}")

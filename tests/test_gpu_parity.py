@@ -323,6 +323,26 @@ def test_all_to_allv_ragged_rows(lib, row_elems, dtype, p):
         assert outs[d].guards_intact()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,n", [(1, 9), (2, 4099), (3, 1001), (5, 3), (8, 70001), (16, 1 << 20),
+                                 (72, 10000)])
+def test_all_to_all_equal_blocks(lib, dtype, p, n):
+    """The plain block transpose, ragged chunk-rule blocks included (n not a
+    multiple of p, and n < p where some blocks are empty)."""
+    x = make_inputs(dtype, p, n, seed=p * 7 + n)
+    want = collectives.all_to_all(x)
+    outs = [Guarded(len(want[j]), dtype, offset=GUARD + j % 3) for j in range(p)]
+    lib.ccl_all_to_all([to_dev(v, dtype) for v in x], [o.view for o in outs])
+    for j in range(p):
+        assert_equal(to_host(outs[j].view), want[j], dtype, f"A2A {dtype} p={p} n={n} rank {j}")
+        assert outs[j].guards_intact()
+    if n % p == 0:  # the transpose is its own inverse when all blocks are equal
+        back = [torch.empty_like(o.view) for o in outs]
+        lib.ccl_all_to_all([o.view for o in outs], back)
+        for j in range(p):
+            assert_equal(to_host(back[j]), x[j], dtype, f"A2A twice rank {j}")
+
+
 @pytest.mark.parametrize("p,row,hi", [(16, 64, 40), (48, 3, 6), (128, 8, 2)])
 def test_all_to_allv_many_blocks(lib, p, row, hi):
     """More blocks than a 4 KB parameter block holds: p=16 (256 blocks, one
