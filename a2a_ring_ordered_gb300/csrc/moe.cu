@@ -180,9 +180,8 @@ __device__ __forceinline__ void token_rows(const Args& a, int s, uint64_t t0, in
 }
 
 // One CTA per (tpc tokens, source).  The CTA's (token, vector) items are one
-// flat index range, U items per thread with their loads issued together, and
-// tpc is chosen so that the range is a whole number of passes (no idle lanes
-// in the last one).  Each vector of a token row is loaded once and stored to
+// flat index range, U items per thread with their loads issued together; tpc
+// is at most what one pass covers (see dispatch_tokens_per_cta).  Each vector of a token row is loaded once and stored to
 // the token's k destination rows.  bf16: 8 elements (16 bytes) per item.
 // FP8: 16 elements per item, and the 8 consecutive lanes holding a
 // 128-element block reduce its amax with shuffles (a row is a multiple of 128
@@ -350,12 +349,25 @@ __global__ void __launch_bounds__(kThreads) moe_combine_kernel(const __grid_cons
   }
 }
 
-// Tokens per CTA: the fewest (at most 16) that make the CTA's items a whole
-// number of passes of `per_pass` items.
+// Combine's tokens per CTA: the fewest (at most 16) that make the CTA's items
+// a whole number of passes of `per_pass` items.
 __host__ int tokens_per_cta(uint64_t items_per_token, uint64_t per_pass) {
   for (int t = 1; t <= kMaxTokensPerCta; ++t)
     if ((items_per_token * static_cast<uint64_t>(t)) % per_pass == 0) return t;
   return 8;
+}
+
+// Dispatch's tokens per CTA: as many as fit in one pass of `per_pass` items
+// (at least 1, at most 16), idle lanes in that pass notwithstanding.  Measured
+// on GB300 (p=8 x 4096 tokens, hidden 7168, top-8 of 256): 1 / 2 / 4 / 8 / 16
+// tokens per CTA ran the FP8 dispatch at 6.77 / 6.69 / 6.48 / 6.28 / 6.25
+// TB/s and the bf16 one at 6.86 / 6.67 / 6.58 / 6.48 / 6.33 -- many short
+// CTAs keep more token rows streaming at once and leave a shorter tail.  The
+// combine went the other way (2 tokens 6.76, 1 token 6.52) and keeps whole
+// passes.
+__host__ int dispatch_tokens_per_cta(uint64_t items_per_token, uint64_t per_pass) {
+  const uint64_t t = items_per_token == 0 ? kMaxTokensPerCta : per_pass / items_per_token;
+  return static_cast<int>(t < 1 ? 1 : (t > kMaxTokensPerCta ? kMaxTokensPerCta : t));
 }
 
 }  // namespace
@@ -386,7 +398,7 @@ cudaError_t launch_moe_route(const MoeRouteArgs& a, cudaStream_t s) {
 cudaError_t launch_moe_dispatch(const MoeDispatchArgs& args, bool fp8, cudaStream_t s) {
   constexpr int kU8 = 2, kU16 = 4;  // items per thread: FP8 (32-byte loads), bf16 (16-byte)
   MoeDispatchArgs a = args;
-  a.tpc = tokens_per_cta(a.hidden / (fp8 ? 16 : 8), static_cast<uint64_t>(kThreads) * (fp8 ? kU8 : kU16));
+  a.tpc = dispatch_tokens_per_cta(a.hidden / (fp8 ? 16 : 8), static_cast<uint64_t>(kThreads) * (fp8 ? kU8 : kU16));
   const dim3 grid(static_cast<unsigned>((a.tokens + a.tpc - 1) / a.tpc), a.p);
   cudaError_t err = fp8 ? launch_kernel(moe_dispatch_kernel<true, kU8>, grid, dim3(kThreads), s, a)
                         : launch_kernel(moe_dispatch_kernel<false, kU16>, grid, dim3(kThreads), s, a);
