@@ -172,7 +172,8 @@ def oracle_prefix_sample(tensors, n: int, frac: float, fn, bytes_per_elem_index:
     t0 = time.perf_counter()
     fn(xs)
     dt = time.perf_counter() - t0
-    return dt, int(m * bytes_per_elem_index), f"{what} on the first {m} of {n} elements of each of the {p} ranks"
+    whose = f"each of the {p} ranks" if p > 1 else "the root's buffer"
+    return dt, int(m * bytes_per_elem_index), f"{what} on the first {m} of {n} elements of {whose}"
 
 
 class Workload:
@@ -713,6 +714,22 @@ class Rooted(Workload):
         else:
             self.a, self.b = [mk(m) for m in sizes], torch.empty(self.n, dtype=tdt, device=device)
 
+    def oracle_sample(self, frac):
+        from oracle import collectives
+        p, e = self.p, self.e
+        if self.kind == "broadcast":
+            return oracle_prefix_sample([self.a], self.n, frac, lambda xs: collectives.broadcast(xs * p),
+                                        (1 + p) * e, f"oracle broadcast to {p} ranks")
+        if self.kind == "scatter":
+            return oracle_prefix_sample([self.a], self.n, frac, lambda xs: collectives.scatter(xs[0], p),
+                                        2 * e, f"oracle scatter to {p} ranks")
+        if self.kind == "reduce":
+            return oracle_prefix_sample(self.a, self.n, frac,
+                                        lambda xs: collectives.reduce_ring(xs, 0, self.dtype),
+                                        (p + 1) * e, "oracle reduce (ring reduce-scatter, gather to the root)")
+        return oracle_prefix_sample(self.a, self.n // p, frac, lambda xs: collectives.gather(xs),
+                                    2 * p * e, "oracle gather to the root")
+
     def step(self, stream):
         getattr(self.lib, f"ccl_{self.kind}")(self.a, self.b, stream=stream)
 
@@ -766,6 +783,26 @@ class MoeEp(Workload):
 
     def bytes_per_step(self):
         return sum(self._bytes())
+
+    def oracle_sample(self, frac):
+        """Route, dispatch and combine of the first frac*T tokens of every source."""
+        from oracle import moe
+        p, T, k, E, h = self.p, self.T, self.k, self.E, self.h
+        t1 = max(1, int(T * frac))
+        xs = [a.reshape(-1) for a in host_prefix(self.x, t1)]
+        ids = [i[:t1].reshape(-1).cpu().numpy() for i in self.ids]
+        w = [x[:t1].reshape(-1).cpu().numpy() for x in self.w]
+        counts, _, _ = moe.route(ids, p, E)
+        rows = counts.sum(axis=0)
+        ys = [host_prefix([self.y[d]], int(rows[d]))[0] for d in range(p)]
+        t0 = time.perf_counter()
+        moe.route(ids, p, E)
+        moe.dispatch(xs, ids, p, k, E, h, fp8=self.fp8)
+        moe.combine(ys, ids, w, p, k, E, h)
+        dt = time.perf_counter() - t0
+        nb = int(self.bytes_per_step() * t1 / T)
+        return dt, nb, (f"oracle route + {'FP8' if self.fp8 else 'bf16'} dispatch + combine of the first "
+                        f"{t1} of {T} tokens of each of the {p} sources")
 
     def _route(self, s):
         self.lib.ccl_moe_route(self.ids, self.E, self.counts, self.slots, stream=s)
@@ -831,6 +868,18 @@ class Ulysses(Workload):
     def parts(self):
         half = self.bytes_per_step() // 2
         return [("ulysses", half, self._fwd), ("ulysses", half, self._inv)]
+
+    def oracle_sample(self, frac):
+        """Forward and inverse exchange of the first frac*S/p tokens of every shard."""
+        from oracle import collectives
+        t1 = max(1, int(self.sp * frac))
+        xs = host_prefix(self.x, t1 * self.H * self.D)
+        t0 = time.perf_counter()
+        y = collectives.ulysses_seq_to_heads(xs, self.H, self.D)
+        collectives.ulysses_heads_to_seq(y, self.H, self.D)
+        dt = time.perf_counter() - t0
+        return dt, int(self.bytes_per_step() * t1 / self.sp), (
+            f"oracle forward + inverse exchange of the first {t1} of {self.sp} tokens of each of the {self.p} shards")
 
 
 def make_workload(a) -> Workload:
