@@ -211,6 +211,30 @@ class Workload:
     def oracle_sample(self, frac: float):
         raise NotImplementedError
 
+    def cpu_ranks_sample(self, frac: float):
+        """The same sample on the CPU-rank ring (one host thread per rank):
+        (seconds, algorithmic bytes, description, threads)."""
+        raise NotImplementedError
+
+
+def cpu_ranks_prefix_sample(tensors, n: int, frac: float, kind: str, dtype: str, bytes_per_elem_index: float,
+                            what: str, scale: float = 1.0, shards: bool = False):
+    """Time the CPU-rank ring on the first frac*n elements of every rank (as
+    chunk-rule blocks of that prefix when ``shards``)."""
+    from oracle import cpu_ranks, ring
+    p = len(tensors)
+    m = max(p, int(n * frac))
+    xs = host_prefix(tensors, m)
+    if shards:
+        xs = [xs[k][off:off + ln] for k, (off, ln) in enumerate(ring.chunk_bounds(p, m))]
+    t0 = time.perf_counter()
+    _, _, st, threads = cpu_ranks.ring(kind, xs, dtype, "sum", scale=scale, timeout_s=600.0)
+    dt = time.perf_counter() - t0
+    if st != cpu_ranks.OK:
+        raise RuntimeError(f"CPU-rank ring returned status {st}")
+    return dt, int(m * bytes_per_elem_index), (f"{what} on the first {m} of {n} elements of each of the "
+                                               f"{p} ranks, {threads} threads"), threads
+
 
 class Bucket(Workload):
     name = "ddp_bucket_allreduce_scale_cast"
@@ -314,6 +338,18 @@ class Bucket(Workload):
         dt = time.perf_counter() - t0
         return dt, self.p * m * 6, f"first {m} of {self.n} elements of each of the {self.p} ranks"
 
+    def cpu_ranks_sample(self, frac):
+        from oracle import cpu_ranks
+        m = max(self.p, int(self.n * frac))
+        xs = [v[:m] for v in self.x]
+        t0 = time.perf_counter()
+        _, _, st, threads = cpu_ranks.ring("bucket", xs, scale=self.scale, timeout_s=600.0)
+        dt = time.perf_counter() - t0
+        if st != cpu_ranks.OK:
+            raise RuntimeError(f"CPU-rank ring returned status {st}")
+        return dt, self.p * m * 6, (f"CPU-rank ring bucket on the first {m} of {self.n} elements of each of "
+                                    f"the {self.p} ranks, {threads} threads"), threads
+
 
 class AllReduce(Workload):
     kernel = "fold"
@@ -398,6 +434,12 @@ class AllReduce(Workload):
                                     lambda xs: ring.ring_allreduce(xs, self.dtype, self.op),
                                     2 * self.p * self.e, "oracle ring all-reduce")
 
+    def cpu_ranks_sample(self, frac):
+        if self.schedule != "ring" or self.wire != "fp32" or self.op != "sum":
+            raise NotImplementedError
+        return cpu_ranks_prefix_sample(self.send, self.n, frac, "allreduce", self.dtype, 2 * self.p * self.e,
+                                       "CPU-rank ring all-reduce")
+
     def step(self, stream):
         if self.literal:
             self.lib.ccl_ring_allreduce_literal(self.send, self.recv, op=self.op,
@@ -451,6 +493,12 @@ class ReduceScatter(AllReduce):
                                     lambda xs: ring.ring_reduce_scatter(xs, self.dtype, "sum", self.wire),
                                     (self.p + 1) * self.e, "oracle ring reduce-scatter")
 
+    def cpu_ranks_sample(self, frac):
+        if self.wire != "fp32":
+            raise NotImplementedError
+        return cpu_ranks_prefix_sample(self.send, self.n, frac, "reduce_scatter", self.dtype,
+                                       (self.p + 1) * self.e, "CPU-rank ring reduce-scatter")
+
 
 class AllGather(ReduceScatter):
     kernel = "gather"
@@ -480,6 +528,10 @@ class AllGather(ReduceScatter):
             ring.ring_all_gather(blocks, self.dtype)
         return oracle_prefix_sample(self.send, self.n, frac, gather, (self.p + 1) * self.e,
                                     "oracle ring all-gather")
+
+    def cpu_ranks_sample(self, frac):
+        return cpu_ranks_prefix_sample(self.send, self.n, frac, "all_gather", self.dtype, (self.p + 1) * self.e,
+                                       "CPU-rank ring all-gather", shards=True)
 
 
 class Zero(ReduceScatter):
@@ -519,6 +571,21 @@ class Zero(ReduceScatter):
         from oracle import ring
         return oracle_prefix_sample(self.send, self.n, frac, ring.zero_rs_then_ag,
                                     2 * (self.p + 1) * 2, "oracle ZeRO RS then AG")
+
+    def cpu_ranks_sample(self, frac):
+        from oracle import cpu_ranks
+        p = self.p
+        m = max(p, int(self.n * frac))
+        xs = host_prefix(self.send, m)
+        t0 = time.perf_counter()
+        shards, _, st, threads = cpu_ranks.ring("reduce_scatter", xs, "bf16", timeout_s=600.0)
+        if st == cpu_ranks.OK:
+            _, _, st, _ = cpu_ranks.ring("all_gather", shards, "bf16", timeout_s=600.0)
+        dt = time.perf_counter() - t0
+        if st != cpu_ranks.OK:
+            raise RuntimeError(f"CPU-rank ring returned status {st}")
+        return dt, m * 2 * (p + 1) * 2, (f"CPU-rank ring ZeRO RS then AG on the first {m} of {self.n} elements "
+                                         f"of each of the {p} ranks, {threads} threads"), threads
 
     def parts(self):
         rs = lambda s: self.lib.ccl_reduce_scatter(self.send, self.shards, stream=s)
@@ -994,9 +1061,24 @@ def cpu_baseline(wl: Workload) -> dict | None:
         dt, nb, desc = wl.oracle_sample(frac)
         times.append(dt)
     t = statistics.median(times)
-    return {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
-            "kind": "oracle", "sample": f"{desc}; median of {len(times)} runs",
-            "seconds_per_sample": round(t, 4)}
+    out = {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
+           "kind": "oracle", "sample": f"{desc}; median of {len(times)} runs",
+           "seconds_per_sample": round(t, 4)}
+    # the ring on CPU ranks (one host thread per virtual rank), same workload
+    try:
+        t1, _, _, _ = wl.cpu_ranks_sample(0.01)
+    except NotImplementedError:
+        return out
+    frac = min(1.0, 0.01 * 1.0 / max(t1, 1e-6))
+    times = []
+    for _ in range(max(1, min(200, int(12.0 / max(t1 / 0.01 * frac, 1e-6))))):
+        dt, nb, desc, threads = wl.cpu_ranks_sample(frac)
+        times.append(dt)
+    t = statistics.median(times)
+    out["cpu_ranks"] = {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": threads,
+                        "kind": "oracle_cpu_ranks", "sample": f"{desc}; median of {len(times)} runs",
+                        "seconds_per_sample": round(t, 4)}
+    return out
 
 
 def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:

@@ -94,3 +94,13 @@ def test_clock_summary_parses_samples():
 def test_warmup_below_three_is_rejected():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2", "--impl", "reference"])
+
+
+def test_cpu_rank_sample_times_the_same_workload():
+    """The CPU-rank ring baseline covers the same bytes as the oracle sample."""
+    wl = bench.Bucket()
+    wl.x = wl.host_inputs()
+    dt, nb, desc, threads = wl.cpu_ranks_sample(0.01)
+    dt1, nb1, _ = wl.oracle_sample(0.01)
+    assert nb == nb1 and dt > 0 and dt1 > 0
+    assert 1 <= threads <= wl.p and f"{threads} threads" in desc
