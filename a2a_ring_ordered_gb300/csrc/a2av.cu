@@ -18,6 +18,7 @@
 // that hold at least one source byte of the block.
 // HBM traffic: one read and one write of every moved byte.
 #include "device_common.cuh"
+#include "realign.cuh"
 
 namespace ccl {
 namespace {
@@ -29,28 +30,13 @@ __device__ __forceinline__ void copy_byte(uintptr_t dst, intptr_t shift) {
   *reinterpret_cast<unsigned char*>(dst) = b;
 }
 
-// Bytes [delta, delta+16) of the 32-byte pair (lo, hi), little-endian.
-__device__ __forceinline__ uint4 realign(const uint4 lo, const uint4 hi, int delta) {
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  const uint32_t sh = 8u * static_cast<uint32_t>(delta & 3);
-  uint4 o;
-#define CCL_REALIGN(Q)                             \
-  o.x = __funnelshift_r(w[Q + 0], w[Q + 1], sh);   \
-  o.y = __funnelshift_r(w[Q + 1], w[Q + 2], sh);   \
-  o.z = __funnelshift_r(w[Q + 2], w[Q + 3], sh);   \
-  o.w = __funnelshift_r(w[Q + 3], w[Q + 4], sh);
-  switch (delta >> 2) {
-    case 0: CCL_REALIGN(0) break;
-    case 1: CCL_REALIGN(1) break;
-    case 2: CCL_REALIGN(2) break;
-    default: CCL_REALIGN(3) break;
-  }
-#undef CCL_REALIGN
-  return o;
-}
-
 // Copy destination bytes [lo, hi); the source byte of destination byte x is
 // x + shift.  Called by all threads of the CTA with the same arguments.
+// REALIGN = false is launched only when every block of the call has source
+// and destination in the same 16-byte phase; it leaves out the realigning
+// path and its registers (64 against 128), and any other phase would still
+// be copied correctly, byte by byte.
+template <bool REALIGN>
 __device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
   const int tid = threadIdx.x;
   const uintptr_t ua = (lo + 15) & ~static_cast<uintptr_t>(15);
@@ -61,6 +47,10 @@ __device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
   }
   const uint64_t m = (ub - ua) / 16;  // whole 16-byte destination units
   const int delta = static_cast<int>(static_cast<uintptr_t>(shift) & 15);
+  if (!REALIGN && delta != 0) {
+    for (uintptr_t x = lo + tid; x < hi; x += kThreads) copy_byte(x, shift);
+    return;
+  }
   if (delta == 0) {
     for (uint64_t u0 = 0; u0 < m; u0 += static_cast<uint64_t>(kThreads) * kUnitsPerThread) {
       uint4 v[kUnitsPerThread];
@@ -75,25 +65,31 @@ __device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
         if (u < m) st_stream16(reinterpret_cast<void*>(ua + 16 * u), v[j]);
       }
     }
-  } else {
+  } else if constexpr (REALIGN) {
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    // source granule under unit u: ua + 16u + shift - delta (16-byte aligned)
+    // source granule under unit u: ua + 16u + shift - delta (16-byte aligned).
+    // A warp takes 32 consecutive units per group, kUnitsPerThread groups
+    // (kThreads units apart) with their loads issued together.
     const uintptr_t g0 = ua + shift - delta;
-    for (uint64_t k0 = static_cast<uint64_t>(warp) * 32; k0 < m; k0 += kThreads) {
-      const uint64_t u = k0 + lane;
-      uint4 cur = make_uint4(0, 0, 0, 0);
-      uint4 extra = make_uint4(0, 0, 0, 0);
-      // granule u holds bytes of unit u (u < m) or the last bytes of unit u-1 (u == m)
-      if (u <= m) cur = ld_once16(reinterpret_cast<const void*>(g0 + 16 * u));
-      if (lane == 31 && u < m) extra = ld_once16(reinterpret_cast<const void*>(g0 + 16 * (u + 1)));
-      uint4 nxt;
-      nxt.x = __shfl_down_sync(0xFFFFFFFFu, cur.x, 1);
-      nxt.y = __shfl_down_sync(0xFFFFFFFFu, cur.y, 1);
-      nxt.z = __shfl_down_sync(0xFFFFFFFFu, cur.z, 1);
-      nxt.w = __shfl_down_sync(0xFFFFFFFFu, cur.w, 1);
-      if (lane == 31) nxt = extra;
-      if (u < m) st_stream16(reinterpret_cast<void*>(ua + 16 * u), realign(cur, nxt, delta));
+    for (uint64_t k0 = static_cast<uint64_t>(warp) * 32; k0 < m;
+         k0 += static_cast<uint64_t>(kThreads) * kUnitsPerThread) {
+      uint4 cur[kUnitsPerThread], extra[kUnitsPerThread];
+#pragma unroll
+      for (int j = 0; j < kUnitsPerThread; ++j) {
+        const uint64_t u = k0 + static_cast<uint64_t>(j) * kThreads + lane;
+        cur[j] = make_uint4(0, 0, 0, 0);
+        extra[j] = make_uint4(0, 0, 0, 0);
+        // granule u holds bytes of unit u (u < m) or the last bytes of unit u-1 (u == m)
+        if (u <= m) cur[j] = ld_once16(reinterpret_cast<const void*>(g0 + 16 * u));
+        if (lane == 31 && u < m) extra[j] = ld_once16(reinterpret_cast<const void*>(g0 + 16 * (u + 1)));
+      }
+#pragma unroll
+      for (int j = 0; j < kUnitsPerThread; ++j) {
+        const uint64_t u = k0 + static_cast<uint64_t>(j) * kThreads + lane;
+        const uint4 nxt = next_lane(cur[j], extra[j], lane);
+        if (u < m) st_stream16(reinterpret_cast<void*>(ua + 16 * u), realign16(cur[j], nxt, delta));
+      }
     }
   }
   // bytes before the first and after the last whole unit (at most 15 + 15)
@@ -102,7 +98,7 @@ __device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
   if (tid < n_edge) copy_byte(tid < n_head ? lo + tid : ub + (tid - n_head), shift);
 }
 
-template <int CAP>
+template <int CAP, bool REALIGN>
 __global__ void __launch_bounds__(kThreads) a2av_kernel(const __grid_constant__ A2AArgsT<CAP> a) {
   pdl_enter();
   for (uint64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
@@ -122,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) a2av_kernel(const __grid_constant__ 
     if (tlo < d0) tlo = d0;
     if (thi > d_end) thi = d_end;
     const intptr_t shift = reinterpret_cast<intptr_t>(d.src) - reinterpret_cast<intptr_t>(d.dst);
-    copy_tile(tlo, thi, shift);
+    copy_tile<REALIGN>(tlo, thi, shift);
   }
 }
 
@@ -139,15 +135,20 @@ cudaError_t launch_a2av(const A2AArgs& a, cudaStream_t s) {
   uint64_t g = a.total_tiles;
   if (g > (1u << 30)) g = 1u << 30;
   const dim3 grid(static_cast<unsigned>(g));
+  bool phased = false;  // some block's source and destination differ in 16-byte phase
+  for (int i = 0; i < a.ndesc && !phased; ++i)
+    phased = ((reinterpret_cast<uintptr_t>(a.d[i].src) - reinterpret_cast<uintptr_t>(a.d[i].dst)) & 15) != 0;
   cudaError_t err;
   if (a.ndesc <= kA2ASmallDesc) {  // the common case: a 4 KB parameter block
     A2AArgsT<kA2ASmallDesc> small;
     small.total_tiles = a.total_tiles;
     small.ndesc = a.ndesc;
     for (int i = 0; i < a.ndesc; ++i) small.d[i] = a.d[i];
-    err = launch_kernel(a2av_kernel<kA2ASmallDesc>, grid, dim3(kThreads), s, small);
+    err = phased ? launch_kernel(a2av_kernel<kA2ASmallDesc, true>, grid, dim3(kThreads), s, small)
+                 : launch_kernel(a2av_kernel<kA2ASmallDesc, false>, grid, dim3(kThreads), s, small);
   } else {
-    err = launch_kernel(a2av_kernel<kA2AMaxDesc>, grid, dim3(kThreads), s, a);
+    err = phased ? launch_kernel(a2av_kernel<kA2AMaxDesc, true>, grid, dim3(kThreads), s, a)
+                 : launch_kernel(a2av_kernel<kA2AMaxDesc, false>, grid, dim3(kThreads), s, a);
   }
   if (err == cudaSuccess) note_launch();
   return err;

@@ -19,6 +19,7 @@
 // (all-reduce, bucket) or 1 write (reduce-scatter) of the output type --
 // exactly the primitives' minimum bytes.
 #include "device_common.cuh"
+#include "realign.cuh"
 
 namespace ccl {
 namespace {
@@ -102,11 +103,27 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ 
   const int first = (c + 1 == p) ? 0 : c + 1;      // the rank that starts chunk c
 
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
-  for (uint64_t v = v_lo + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi;
-       v += stride) {
-    Acc acc[VEC];
-    fold_elements<DT_IN, VEC, OP>(a, p, first, v * VEC, acc);
-    emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc);
+  if (MODE == kModeReduceScatter && VEC > 1 && (ch.off % VEC) != 0) {
+    // shard unaligned: whole warps step together so that neighbouring lanes
+    // can hand each other the halves of the shard's aligned vectors
+    const int lane = threadIdx.x & 31;
+    for (uint64_t vb = v_lo + static_cast<uint64_t>(blockIdx.x) * kThreads + (threadIdx.x & ~31u); vb < v_hi;
+         vb += stride) {
+      const uint64_t v = vb + lane;
+      Acc acc[VEC] = {};
+      if (v < v_hi) fold_elements<DT_IN, VEC, OP>(a, p, first, v * VEC, acc);
+      uint32_t w[words_for(VEC, Elem<DT_OUT>::kBytes)];
+      pack_out<DT_OUT, VEC>(acc, w);
+      if constexpr (VEC * Elem<DT_OUT>::kBytes == 16)
+        store_shard_realigned<DT_OUT, VEC>(a.recv[c], ch.off, v, v_hi, lane, w);
+    }
+  } else {
+    for (uint64_t v = v_lo + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi;
+         v += stride) {
+      Acc acc[VEC];
+      fold_elements<DT_IN, VEC, OP>(a, p, first, v * VEC, acc);
+      emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc);
+    }
   }
 
   if (VEC > 1 && blockIdx.x == 0) {
@@ -186,10 +203,23 @@ __global__ void __launch_bounds__(kThreads) fold_unrolled_kernel(const __grid_co
        base += static_cast<uint64_t>(gridDim.x) * kSpan) {
     Acc acc[U][VEC];
     fold_vectors<DT_IN, VEC, OP, BATCH, U>(a, p, first, base + threadIdx.x, v_hi, acc);
+    if (MODE == kModeReduceScatter && (ch.off % VEC) != 0) {
+      // shard unaligned: lanes hand each other the halves of its aligned
+      // vectors (the loop is uniform over the CTA, so every lane is here)
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
-      if (v < v_hi) emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc[u]);
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+        uint32_t w[words_for(VEC, Elem<DT_OUT>::kBytes)];
+        pack_out<DT_OUT, VEC>(acc[u], w);
+        if constexpr (VEC * Elem<DT_OUT>::kBytes == 16)
+          store_shard_realigned<DT_OUT, VEC>(a.recv[c], ch.off, v, v_hi, threadIdx.x & 31, w);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+        if (v < v_hi) emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc[u]);
+      }
     }
   }
 
@@ -234,8 +264,9 @@ cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
 // Small p (sums only) goes to fold_unrolled_kernel with (ranks per batch,
 // vectors per thread) = (2, 8), (4, 4) or (8, 2) for 16-byte fp32 / int32
 // vectors.  A bf16 vector widens to 8 fp32 accumulators and a bucket vector
-// is 32 bytes, so those use (2, 4) and (4, 2) and leave p > 4 to fold_kernel
-// (at most 32 accumulators per thread either way).
+// is 32 bytes, so those use (2, 4) and (4, 2) (at most 32 accumulators per
+// thread); bf16 takes (8, 2) for p = 5..8 as well, the bucket leaves p > 4
+// to fold_kernel.
 template <int DT_IN, int DT_OUT, int OP, int MODE>
 cudaError_t launch_typed(bool vec, const FoldArgs& a, cudaStream_t s) {
   if (!vec) return launch_one<DT_IN, DT_OUT, 1, OP, MODE>(a, s);
@@ -261,7 +292,13 @@ cudaError_t launch_typed(bool vec, const FoldArgs& a, cudaStream_t s) {
         return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 4, kHalve ? 2 : 4>(a, s);
       return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 4, 1>(a, s);
     }
-    if constexpr (!kHalve) {
+    // p <= 8 with 16-byte vectors of 4 words (fp32, int32, and bf16 in and
+    // out): 8 ranks x 2 vectors.  Measured for bf16 on GB300 against the
+    // general kernel: all-reduce p = 6 0.92 -> 1.03 and p = 8 1.03 -> 1.05,
+    // reduce-scatter p = 8 0.94 -> 1.07 of the copy bandwidth at 256 MiB -
+    // 1 GiB per rank.  (The bucket's 32-byte fp32 vectors would need 128
+    // registers of loads: it stays on fold_kernel.)
+    if constexpr (!kHalve || DT_IN == kBF16) {
       if (a.p <= 8) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 8, 2>(a, s);
     }
   }

@@ -8,6 +8,7 @@
 // side uses 16-byte loads too whenever off(k) keeps it aligned.
 // HBM traffic: n reads + p*n writes of the element type.
 #include "device_common.cuh"
+#include "realign.cuh"
 
 namespace ccl {
 namespace {
@@ -30,7 +31,9 @@ __device__ __forceinline__ void load_elems(const void* base, uint64_t i, uint32_
   }
 }
 
-template <int DT, int VEC, int U>
+// REALIGN = false is launched only when every block starts on a whole vector
+// of the outputs, and leaves the realigning path out.
+template <int DT, int VEC, int U, bool REALIGN>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
   constexpr int W = (VEC * Elem<DT>::kBytes + 3) / 4;
   pdl_enter();
@@ -42,6 +45,14 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
   const uint64_t v_hi = end / VEC;
   const void* src = a.send[k];
   const bool src_aligned = (ch.off % VEC) == 0;
+  // Block k unaligned in the outputs (off(k) not a multiple of VEC): output
+  // vector v takes the source bytes [((v - q) * VEC - s) * B, + 16), i.e.
+  // aligned source granule v - q - 1 from byte `phase` on, continued in
+  // granule v - q, which the next lane loads (s = off(k) mod VEC, q = off(k)
+  // div VEC).  Every granule loaded holds at least one byte of block k.
+  const uint64_t q = ch.off / VEC;
+  const int phase = 16 - static_cast<int>(ch.off % VEC) * Elem<DT>::kBytes;
+  const int lane = threadIdx.x & 31;
 
   // U vectors per thread (t, t + kThreads, ...): their loads are issued
   // together, then each is stored to the p outputs
@@ -49,15 +60,44 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
   for (uint64_t base = v_lo + static_cast<uint64_t>(blockIdx.x) * kSpan; base < v_hi;
        base += static_cast<uint64_t>(gridDim.x) * kSpan) {
     uint32_t w[U][W];
+    if constexpr (!REALIGN || VEC == 1) {
+      // (REALIGN = false is not launched with a block off the output vectors;
+      // the element-wise loads are there so that no load could be misaligned)
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
-      if (v < v_hi) {
-        if (VEC == 1 || src_aligned) {
-          load_raw<DT, VEC>(src, v * VEC - ch.off, w[u]);
-        } else {
-          load_elems<DT, VEC>(src, v * VEC - ch.off, w[u]);
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+        if (v < v_hi) {
+          if (VEC == 1 || src_aligned) {
+            load_raw<DT, VEC>(src, v * VEC - ch.off, w[u]);
+          } else {
+            load_elems<DT, VEC>(src, v * VEC - ch.off, w[u]);
+          }
         }
+      }
+    } else if (src_aligned) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+        if (v < v_hi) load_raw<DT, VEC>(src, v * VEC - ch.off, w[u]);
+      }
+    } else {
+      const char* g = static_cast<const char*>(src);
+      uint4 cur[U], extra[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+        cur[u] = make_uint4(0, 0, 0, 0);
+        extra[u] = make_uint4(0, 0, 0, 0);
+        if (v <= v_hi) cur[u] = ld_once16(g + 16 * (v - q - 1));
+        if (lane == 31 && v < v_hi) extra[u] = ld_once16(g + 16 * (v - q));
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint4 o = realign16(cur[u], next_lane(cur[u], extra[u], lane), phase);
+        w[u][0] = o.x;
+        w[u][1] = o.y;
+        w[u][2] = o.z;
+        w[u][3] = o.w;
       }
     }
     for (int r = 0; r < p; ++r) {
@@ -91,7 +131,11 @@ cudaError_t launch_one(const GatherArgs& a, cudaStream_t s) {
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.p));
-  return launch_kernel(gather_kernel<DT, VEC, U>, grid, dim3(kThreads), s, a);
+  bool realign = false;  // some block starts inside a vector of the outputs
+  for (uint64_t k = 0; k < static_cast<uint64_t>(a.p) && VEC > 1 && !realign; ++k)
+    realign = (k * a.q + (k < a.rem ? k : a.rem)) % VEC != 0;  // off(k), the chunk rule
+  if (realign) return launch_kernel(gather_kernel<DT, VEC, U, true>, grid, dim3(kThreads), s, a);
+  return launch_kernel(gather_kernel<DT, VEC, U, false>, grid, dim3(kThreads), s, a);
 }
 
 template <int DT>

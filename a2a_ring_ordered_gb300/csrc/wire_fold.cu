@@ -13,6 +13,7 @@
 // in flight.  Chunk edges off the 16-byte grid are folded element-wise by
 // CTA (0, c).
 #include "device_common.cuh"
+#include "realign.cuh"
 
 namespace ccl {
 namespace {
@@ -88,10 +89,22 @@ __global__ void __launch_bounds__(kThreads) wire_fold_kernel(const __grid_consta
        base += static_cast<uint64_t>(gridDim.x) * kSpan) {
     float acc[U][VEC];
     fold_wire<VEC, BATCH, U>(a, first, base + threadIdx.x, v_hi, acc);
+    if (MODE == kModeReduceScatter && VEC > 1 && (ch.off % VEC) != 0) {
+      // shard unaligned: lanes hand each other the halves of its aligned
+      // vectors (the loop is uniform over the CTA, so every lane is here)
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
-      if (v < v_hi) emit_wire<VEC, MODE>(a, c, ch, v * VEC, acc[u]);
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+        uint32_t w[(VEC * 2 + 3) / 4];
+        pack_out<kBF16, VEC>(acc[u], w);
+        if constexpr (VEC == 8) store_shard_realigned<kBF16, VEC>(a.recv[c], ch.off, v, v_hi, threadIdx.x & 31, w);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
+        if (v < v_hi) emit_wire<VEC, MODE>(a, c, ch, v * VEC, acc[u]);
+      }
     }
   }
   if (VEC > 1 && blockIdx.x == 0) {

@@ -136,14 +136,18 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workloads
 KERNEL_SOURCES = {
-    "fold": ["a2a_ring_ordered_gb300/csrc/fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
+    "fold": ["a2a_ring_ordered_gb300/csrc/fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh",
+             "a2a_ring_ordered_gb300/csrc/realign.cuh"],
     "schedule": ["a2a_ring_ordered_gb300/csrc/schedule_fold.cu",
                  "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "hier": ["a2a_ring_ordered_gb300/csrc/hier_fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
-    "wire": ["a2a_ring_ordered_gb300/csrc/wire_fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
+    "wire": ["a2a_ring_ordered_gb300/csrc/wire_fold.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh",
+             "a2a_ring_ordered_gb300/csrc/realign.cuh"],
     "fanout": ["a2a_ring_ordered_gb300/csrc/bulk_fanout.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
-    "gather": ["a2a_ring_ordered_gb300/csrc/gather.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
-    "a2av": ["a2a_ring_ordered_gb300/csrc/a2av.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
+    "gather": ["a2a_ring_ordered_gb300/csrc/gather.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh",
+               "a2a_ring_ordered_gb300/csrc/realign.cuh"],
+    "a2av": ["a2a_ring_ordered_gb300/csrc/a2av.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh",
+             "a2a_ring_ordered_gb300/csrc/realign.cuh"],
     "ring_step": ["a2a_ring_ordered_gb300/csrc/ring_step.cu",
                   "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
     "moe": ["a2a_ring_ordered_gb300/csrc/moe.cu", "a2a_ring_ordered_gb300/csrc/device_common.cuh"],
@@ -1292,14 +1296,18 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
 
 
 def run_sweep(a) -> int:
-    """Message-size sweep of the fused all-reduce: one JSON line per point.
+    """Message-size sweep of one collective (``--sweep-collective``, default
+    the fused all-reduce): one JSON line per point.
 
-    Per point, K calls are captured in a CUDA graph (small messages are
-    launch-bound, and host-side call overhead would otherwise leave the GPU
-    idle between kernels) and the graph is replayed under CUDA events on the
-    replay stream.  The calls rotate over enough buffer sets that the rotated
-    footprint is at least twice the L2 where memory allows, so mid-size
-    messages are not served from L2 left by the previous call.
+    The message size is a rank's full vector (n elements): all-reduce and
+    all-to-all move p*n in and p*n out, reduce-scatter p*n in and n out,
+    all-gather n in and p*n out (the primitive's minimum bytes).  Per point,
+    K calls are captured in a CUDA graph (small messages are launch-bound, and
+    host-side call overhead would otherwise leave the GPU idle between
+    kernels) and the graph is replayed under CUDA events on the replay stream.
+    The calls rotate over enough buffer sets that the rotated footprint is at
+    least twice the L2 where memory allows, so mid-size messages are not
+    served from L2 left by the previous call.
     """
     import torch
     from a2a_ring_ordered_gb300 import ccl as lib
@@ -1307,11 +1315,14 @@ def run_sweep(a) -> int:
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     peak, peak_src = measured_peak_gbs()
+    kind = a.sweep_collective
     dtypes = [a.dtype] if a.sweep_dtype_only else ["f32", "bf16"]
     ps = [a.p] if a.p else [2, 4, 8, 16, 72]
     gen = torch.Generator(device=device)
     gen.manual_seed(4)
     s = torch.cuda.Stream(device)
+    call = {"allreduce": lib.ccl_allreduce, "reduce_scatter": lib.ccl_reduce_scatter,
+            "all_gather": lib.ccl_all_gather, "all_to_all": lib.ccl_all_to_all}[kind]
     for dt in dtypes:
         e = 4 if dt == "f32" else 2
         tdt = torch.float32 if dt == "f32" else torch.bfloat16
@@ -1320,24 +1331,40 @@ def run_sweep(a) -> int:
             for lg in range(10, top + 1, a.sweep_stride):
                 nbytes_rank = 1 << lg
                 n = nbytes_rank // e
-                foot = 2 * p * nbytes_rank
+                lens = [lib.ccl_chunk_bounds(p, n, k)[1] for k in range(p)]
+                in_sizes = lens if kind == "all_gather" else [n] * p
+                out_sizes = (lens if kind == "reduce_scatter" else
+                             [p * ln for ln in lens] if kind == "all_to_all" else [n] * p)
+                # every rank buffer starts on a 256-byte boundary of its arena,
+                # as separately allocated buffers would
+                pad = 256 // e
+                rnd = lambda m: -(-m // pad) * pad
+                n_in, n_out = sum(rnd(m) for m in in_sizes), sum(rnd(m) for m in out_sizes)
+                foot = (sum(in_sizes) + sum(out_sizes)) * e  # the primitive's minimum bytes
                 sets = int(min(64, max(1, -(-2 * L2_BYTES // foot))))
-                arena_in = (torch.rand(sets * p * n, generator=gen, device=device) * 2 - 1).to(tdt)
-                arena_out = torch.empty(sets * p * n, dtype=tdt, device=device)
-                views = [([arena_in[(j * p + r) * n:(j * p + r + 1) * n] for r in range(p)],
-                          [arena_out[(j * p + r) * n:(j * p + r + 1) * n] for r in range(p)])
-                         for j in range(sets)]
+                arena_in = (torch.rand(sets * n_in, generator=gen, device=device) * 2 - 1).to(tdt)
+                arena_out = torch.empty(sets * n_out, dtype=tdt, device=device)
+
+                def split(t, sizes):
+                    out, off = [], 0
+                    for m in sizes:
+                        out.append(t[off:off + m])
+                        off += rnd(m)
+                    return out
+
+                views = [(split(arena_in[j * n_in:(j + 1) * n_in], in_sizes),
+                          split(arena_out[j * n_out:(j + 1) * n_out], out_sizes)) for j in range(sets)]
                 est_us = max(2.0, foot / (peak * 1e3))
                 k = int(min(4000, max(2 * sets, 20000.0 / est_us)))
                 with torch.cuda.stream(s):
                     for j in range(min(sets, 3)):  # warm-up outside capture
-                        lib.ccl_allreduce(views[j][0], views[j][1], stream=s)
+                        call(views[j][0], views[j][1], stream=s)
                 s.synchronize()
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=s):
                     for i in range(k):
                         snd, rcv = views[i % sets]
-                        lib.ccl_allreduce(snd, rcv, stream=s)
+                        call(snd, rcv, stream=s)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 reps = 3
                 with torch.cuda.stream(s):  # replay() launches on the current stream
@@ -1348,14 +1375,15 @@ def run_sweep(a) -> int:
                     e1.record(s)
                 torch.cuda.synchronize(device)
                 ms = e0.elapsed_time(e1) / (reps * k)
-                algo = 2 * p * n * e
+                algo = foot
                 gbs = algo / (ms * 1e-3) / 1e9
+                bus = {"allreduce": 2 * (p - 1) / p}.get(kind, (p - 1) / p)
                 print(json.dumps({
-                    "sweep": "allreduce", "dtype": dt, "p": p, "bytes_per_rank": nbytes_rank,
+                    "sweep": kind, "dtype": dt, "p": p, "bytes_per_rank": nbytes_rank,
                     "us_per_call": round(ms * 1e3, 3), "effective_gbs": round(gbs, 1),
                     "frac_of_hbm": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src,
                     "algbw_gbs": round(nbytes_rank / (ms * 1e-3) / 1e9, 2),
-                    "busbw_gbs": round(nbytes_rank / (ms * 1e-3) / 1e9 * 2 * (p - 1) / p, 2),
+                    "busbw_gbs": round(nbytes_rank / (ms * 1e-3) / 1e9 * bus, 2),
                     "buffer_sets": sets, "rotated_footprint_mb": round(sets * foot / 1e6, 1),
                     "calls_per_graph": k}), flush=True)
                 del g, views, arena_in, arena_out
@@ -1394,6 +1422,9 @@ def main(argv=None) -> int:
                     help="all-reduce message-size sweep (1 KiB..1 GiB per rank), one line per point")
     ap.add_argument("--sweep-stride", type=int, default=1, help="log2 step between sweep sizes")
     ap.add_argument("--sweep-dtype-only", action="store_true", help="sweep only --dtype")
+    ap.add_argument("--sweep-collective", default="allreduce",
+                    choices=["allreduce", "reduce_scatter", "all_gather", "all_to_all"],
+                    help="collective of --sweep")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

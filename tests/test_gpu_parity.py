@@ -512,6 +512,62 @@ def test_sweep_largest_sizes_sampled(lib, dtype, p, mib):
         assert torch.equal(recv[r].view(view), recv[0].view(view))
 
 
+# ------------------------------------ chunks off the 16-byte grid, many warps
+UNALIGNED_BIG = [(72, 72 * 20011 + 29), (3, 3 * 400009 + 2), (7, 7 * 100003 + 5)]
+
+
+def _bits(t):
+    return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("p,n", UNALIGNED_BIG)
+def test_unaligned_chunks_span_many_warps(lib, dtype, p, n):
+    """Chunk offsets off the 16-byte grid, chunks spanning many warps and
+    grid-stride passes: the reduce-scatter's realigned shard stores and the
+    all-gather's realigned block loads.  Sampled indices (every chunk edge
+    included) against the oracle; AG(RS) == AR and RS == AR's chunks on every
+    element; guard bands intact."""
+    x = make_inputs(dtype, p, n, seed=p + n)
+    idx = sample_indices(n, p, 1 << 16, seed=p)
+    want = pointwise.allreduce_at_columns([v[idx] for v in x], idx, n, dtype)
+    send = [to_dev(v, dtype) for v in x]
+    del x
+    ar = [torch.empty_like(t) for t in send]
+    lib.ccl_allreduce(send, ar)
+    assert_equal(to_host(ar[0][torch.from_numpy(idx).cuda()]), want, dtype, "AR")
+    bounds = ring.chunk_bounds(p, n)
+    shards = [Guarded(ln, dtype) for _, ln in bounds]
+    lib.ccl_reduce_scatter(send, [g.view for g in shards])
+    for k, (off, ln) in enumerate(bounds):
+        sel = (idx >= off) & (idx < off + ln)
+        got = to_host(shards[k].view[torch.from_numpy(idx[sel] - off).cuda()])
+        assert_equal(got, want[sel], dtype, f"RS rank {k}")
+        assert torch.equal(_bits(shards[k].view), _bits(ar[0][off:off + ln])), f"RS == AR chunk {k}"
+        assert shards[k].guards_intact()
+    out = [Guarded(n, dtype, offset=GUARD + (4 if dtype != "bf16" else 8) * (r % 2)) for r in range(p)]
+    lib.ccl_all_gather([g.view for g in shards], [o.view for o in out])
+    for r in range(p):
+        assert torch.equal(_bits(out[r].view), _bits(ar[0])), f"AG(RS) rank {r}"
+        assert out[r].guards_intact()
+
+
+@pytest.mark.parametrize("p,n", [(72, 72 * 20011 + 29), (3, 3 * 400009 + 2), (9, 9 * 50021 + 4)])
+def test_bf16_wire_reduce_scatter_unaligned_shards(lib, p, n):
+    x = make_inputs("bf16", p, n, seed=p * 3 + n)
+    idx = sample_indices(n, p, 1 << 16, seed=p + 1)
+    want = pointwise.allreduce_at_columns([v[idx] for v in x], idx, n, "bf16", wire="bf16")
+    send = [to_dev(v, "bf16") for v in x]
+    bounds = ring.chunk_bounds(p, n)
+    shards = [Guarded(ln, "bf16") for _, ln in bounds]
+    lib.ccl_reduce_scatter_bf16_wire(send, [g.view for g in shards])
+    for k, (off, ln) in enumerate(bounds):
+        sel = (idx >= off) & (idx < off + ln)
+        got = to_host(shards[k].view[torch.from_numpy(idx[sel] - off).cuda()])
+        assert_equal(got, want[sel], "bf16", f"wire RS rank {k}")
+        assert shards[k].guards_intact()
+
+
 # ------------------------------------------------ other all-reduce schedules
 SCHED_CASES = [(s, p, n) for s in ("recursive_doubling", "rabenseifner") for p, n in
                [(2, 4099), (4, 1000), (8, 70001), (16, 65536), (128, 1000)]] + \
