@@ -45,7 +45,12 @@ __device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
     for (uintptr_t x = lo + tid; x < hi; x += kThreads) copy_byte(x, shift);
     return;
   }
-  const uint64_t m = (ub - ua) / 16;  // whole 16-byte destination units
+  // Units are counted from ua rounded down to 512 bytes, so that every warp's
+  // 32 stores fill a whole 512-byte span (whole 128-byte lines); the units
+  // before ua (u < u_first) stay idle.
+  const uintptr_t uo = ua & ~static_cast<uintptr_t>(511);
+  const uint64_t u_first = (ua - uo) / 16;
+  const uint64_t m = (ub - uo) / 16;  // one past the last whole 16-byte destination unit
   const int delta = static_cast<int>(static_cast<uintptr_t>(shift) & 15);
   if (!REALIGN && delta != 0) {
     for (uintptr_t x = lo + tid; x < hi; x += kThreads) copy_byte(x, shift);
@@ -57,21 +62,21 @@ __device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
 #pragma unroll
       for (int j = 0; j < kUnitsPerThread; ++j) {
         const uint64_t u = u0 + static_cast<uint64_t>(j) * kThreads + tid;
-        if (u < m) v[j] = ld_once16(reinterpret_cast<const void*>(ua + 16 * u + shift));
+        if (u >= u_first && u < m) v[j] = ld_once16(reinterpret_cast<const void*>(uo + 16 * u + shift));
       }
 #pragma unroll
       for (int j = 0; j < kUnitsPerThread; ++j) {
         const uint64_t u = u0 + static_cast<uint64_t>(j) * kThreads + tid;
-        if (u < m) st_stream16(reinterpret_cast<void*>(ua + 16 * u), v[j]);
+        if (u >= u_first && u < m) st_stream16(reinterpret_cast<void*>(uo + 16 * u), v[j]);
       }
     }
   } else if constexpr (REALIGN) {
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    // source granule under unit u: ua + 16u + shift - delta (16-byte aligned).
+    // source granule under unit u: uo + 16u + shift - delta (16-byte aligned).
     // A warp takes 32 consecutive units per group, kUnitsPerThread groups
     // (kThreads units apart) with their loads issued together.
-    const uintptr_t g0 = ua + shift - delta;
+    const uintptr_t g0 = uo + shift - delta;
     for (uint64_t k0 = static_cast<uint64_t>(warp) * 32; k0 < m;
          k0 += static_cast<uint64_t>(kThreads) * kUnitsPerThread) {
       uint4 cur[kUnitsPerThread], extra[kUnitsPerThread];
@@ -81,14 +86,16 @@ __device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
         cur[j] = make_uint4(0, 0, 0, 0);
         extra[j] = make_uint4(0, 0, 0, 0);
         // granule u holds bytes of unit u (u < m) or the last bytes of unit u-1 (u == m)
-        if (u <= m) cur[j] = ld_once16(reinterpret_cast<const void*>(g0 + 16 * u));
-        if (lane == 31 && u < m) extra[j] = ld_once16(reinterpret_cast<const void*>(g0 + 16 * (u + 1)));
+        if (u >= u_first && u <= m) cur[j] = ld_once16(reinterpret_cast<const void*>(g0 + 16 * u));
+        if (lane == 31 && u >= u_first && u < m)
+          extra[j] = ld_once16(reinterpret_cast<const void*>(g0 + 16 * (u + 1)));
       }
 #pragma unroll
       for (int j = 0; j < kUnitsPerThread; ++j) {
         const uint64_t u = k0 + static_cast<uint64_t>(j) * kThreads + lane;
         const uint4 nxt = next_lane(cur[j], extra[j], lane);
-        if (u < m) st_stream16(reinterpret_cast<void*>(ua + 16 * u), realign16(cur[j], nxt, delta));
+        if (u >= u_first && u < m)
+          st_stream16(reinterpret_cast<void*>(uo + 16 * u), realign16(cur[j], nxt, delta));
       }
     }
   }
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) a2av_kernel(const __grid_constant__ 
     const A2ADesc& d = a.d[lo];
     const uintptr_t d0 = reinterpret_cast<uintptr_t>(d.dst);
     const uintptr_t d_end = d0 + d.bytes;
-    const uintptr_t base = d0 & ~static_cast<uintptr_t>(15);
+    const uintptr_t base = d0 & ~static_cast<uintptr_t>(511);  // tiles on 512-byte boundaries
     const uint64_t k = t - d.tile0;
     uintptr_t tlo = base + k * kA2ATileBytes;
     uintptr_t thi = tlo + kA2ATileBytes;
@@ -126,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) a2av_kernel(const __grid_constant__ 
 
 uint64_t a2a_tiles_for(const char* dst, uint64_t bytes) {
   if (bytes == 0) return 0;
-  const uint64_t lead = reinterpret_cast<uintptr_t>(dst) & 15;
+  const uint64_t lead = reinterpret_cast<uintptr_t>(dst) & 511;  // tiles start on 512-byte boundaries
   return (lead + bytes + kA2ATileBytes - 1) / kA2ATileBytes;
 }
 

@@ -90,7 +90,11 @@ __device__ __forceinline__ void emit(const FoldArgs& a, int p, int c, const Chun
   }
 }
 
-template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE>
+// REALIGN (reduce-scatter only) adds the realigned shard stores for chunks
+// off the vector grid; the host picks it only when some chunk is, so that
+// the aligned kernel keeps its registers (128 against 109 for bf16, which
+// cost the p = 16 reduce-scatter 1 %).
+template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE, bool REALIGN>
 __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ FoldArgs a) {
   using Acc = typename Elem<DT_IN>::Acc;
   pdl_enter();
@@ -103,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ 
   const int first = (c + 1 == p) ? 0 : c + 1;      // the rank that starts chunk c
 
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
-  if (MODE == kModeReduceScatter && VEC > 1 && (ch.off % VEC) != 0) {
+  if (MODE == kModeReduceScatter && REALIGN && VEC > 1 && (ch.off % VEC) != 0) {
     // shard unaligned: whole warps step together so that neighbouring lanes
     // can hand each other the halves of the shard's aligned vectors
     const int lane = threadIdx.x & 31;
@@ -115,11 +119,21 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ 
       uint32_t w[words_for(VEC, Elem<DT_OUT>::kBytes)];
       pack_out<DT_OUT, VEC>(acc, w);
       if constexpr (VEC * Elem<DT_OUT>::kBytes == 16)
-        store_shard_realigned<DT_OUT, VEC>(a.recv[c], ch.off, v, v_hi, lane, w);
+        // (lanes start at v_lo here: 0 for v_lo spares the registers of the
+        // check for lanes before it)
+        store_shard_realigned<DT_OUT, VEC>(a.recv[c], ch.off, v, 0, v_hi, lane, w);
     }
   } else {
-    for (uint64_t v = v_lo + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi;
+    // Vectors are counted from v_lo rounded down to 32, so that every warp's
+    // 32 vectors fill whole 512-byte spans of the buffers (whole 128-byte
+    // lines for the stores); lanes before v_lo (the previous chunk's) stay
+    // idle.  Measured on GB300: the p = 72 all-reduce (chunks off the 512-byte
+    // grid) 0.99 -> 1.03 of the copy bandwidth.  The reduce-scatter, whose
+    // one output is a separate shard, keeps v_lo (1 % faster at p = 72).
+    const uint64_t v_start = (MODE == kModeReduceScatter) ? v_lo : (v_lo & ~static_cast<uint64_t>(31));
+    for (uint64_t v = v_start + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi;
          v += stride) {
+      if (v < v_lo) continue;
       Acc acc[VEC];
       fold_elements<DT_IN, VEC, OP>(a, p, first, v * VEC, acc);
       emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc);
@@ -150,7 +164,7 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ 
 // each element is the same ring walk as in fold_kernel.
 template <int DT_IN, int VEC, int OP, int BATCH, int U>
 __device__ __forceinline__ void fold_vectors(const FoldArgs& a, int p, int first, uint64_t v0,
-                                             uint64_t v_hi,
+                                             uint64_t v_lo, uint64_t v_hi,
                                              typename Elem<DT_IN>::Acc (&acc)[U][VEC]) {
   constexpr int WI = words_for(VEC, Elem<DT_IN>::kBytes);
   uint32_t raw[BATCH][U][WI];
@@ -162,7 +176,7 @@ __device__ __forceinline__ void fold_vectors(const FoldArgs& a, int p, int first
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint64_t v = v0 + static_cast<uint64_t>(u) * kThreads;
-        if (v < v_hi) load_raw<DT_IN, VEC>(src, v * VEC, raw[b][u]);
+        if (v >= v_lo && v < v_hi) load_raw<DT_IN, VEC>(src, v * VEC, raw[b][u]);
       }
       r = (r + 1 == p) ? 0 : r + 1;
     }
@@ -198,11 +212,14 @@ __global__ void __launch_bounds__(kThreads) fold_unrolled_kernel(const __grid_co
   const uint64_t v_hi = end / VEC;
   const int first = (c + 1 == p) ? 0 : c + 1;
 
+  // counted from v_lo rounded down to 32 (whole warps on 512-byte spans, as
+  // in fold_kernel); lanes before v_lo stay idle
+  const uint64_t v_start = v_lo & ~static_cast<uint64_t>(31);
   constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
-  for (uint64_t base = v_lo + static_cast<uint64_t>(blockIdx.x) * kSpan; base < v_hi;
+  for (uint64_t base = v_start + static_cast<uint64_t>(blockIdx.x) * kSpan; base < v_hi;
        base += static_cast<uint64_t>(gridDim.x) * kSpan) {
     Acc acc[U][VEC];
-    fold_vectors<DT_IN, VEC, OP, BATCH, U>(a, p, first, base + threadIdx.x, v_hi, acc);
+    fold_vectors<DT_IN, VEC, OP, BATCH, U>(a, p, first, base + threadIdx.x, v_lo, v_hi, acc);
     if (MODE == kModeReduceScatter && (ch.off % VEC) != 0) {
       // shard unaligned: lanes hand each other the halves of its aligned
       // vectors (the loop is uniform over the CTA, so every lane is here)
@@ -212,13 +229,13 @@ __global__ void __launch_bounds__(kThreads) fold_unrolled_kernel(const __grid_co
         uint32_t w[words_for(VEC, Elem<DT_OUT>::kBytes)];
         pack_out<DT_OUT, VEC>(acc[u], w);
         if constexpr (VEC * Elem<DT_OUT>::kBytes == 16)
-          store_shard_realigned<DT_OUT, VEC>(a.recv[c], ch.off, v, v_hi, threadIdx.x & 31, w);
+          store_shard_realigned<DT_OUT, VEC>(a.recv[c], ch.off, v, v_lo, v_hi, threadIdx.x & 31, w);
       }
     } else {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
-        if (v < v_hi) emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc[u]);
+        if (v >= v_lo && v < v_hi) emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc[u]);
       }
     }
   }
@@ -239,7 +256,7 @@ __global__ void __launch_bounds__(kThreads) fold_unrolled_kernel(const __grid_co
 
 template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE, int BATCH, int U>
 cudaError_t launch_unrolled(const FoldArgs& a, cudaStream_t s) {
-  const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
+  const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC + 31;  // + the lanes before v_lo
   constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
   uint64_t gx = (per_chunk + kSpan - 1) / kSpan;
   if (gx < 1) gx = 1;
@@ -253,12 +270,18 @@ constexpr int kVectorsPerThread = 2;
 
 template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE>
 cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
-  const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
+  const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC + 31;  // + the lanes before v_lo
   uint64_t gx = (per_chunk + kThreads * kVectorsPerThread - 1) / (kThreads * kVectorsPerThread);
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.p));
-  return launch_kernel(fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE>, grid, dim3(kThreads), s, a);
+  if constexpr (MODE == kModeReduceScatter && VEC > 1) {
+    bool realign = false;  // some chunk starts off the vector grid (off(c), the chunk rule)
+    for (uint64_t c = 0; c < static_cast<uint64_t>(a.p) && !realign; ++c)
+      realign = (c * a.q + (c < a.rem ? c : a.rem)) % VEC != 0;
+    if (realign) return launch_kernel(fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, true>, grid, dim3(kThreads), s, a);
+  }
+  return launch_kernel(fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, false>, grid, dim3(kThreads), s, a);
 }
 
 // Small p (sums only) goes to fold_unrolled_kernel with (ranks per batch,

@@ -50,28 +50,30 @@ __device__ __forceinline__ uint4 next_lane(const uint4 v, const uint4 own_next, 
 // Reduce-scatter shard store when the chunk's offset `off` is not a multiple
 // of VEC (VEC * bytes == 16).  All 32 lanes of the warp call it together;
 // lane l holds the packed outputs w of input vector v = v0 + l (elements
-// [v * VEC, v * VEC + VEC) of the chunk, valid when v < v_hi).  Element t of
-// lane v lands at shard position (v - q) * VEC - s + t (q = off div VEC,
-// s = off mod VEC), so shard vector J = v - q is lane v's elements [s, VEC)
-// followed by lane v + 1's [0, s): the lane stores it whole when its
+// [v * VEC, v * VEC + VEC) of the chunk, valid when v_lo <= v < v_hi).
+// Element t of lane v lands at shard position (v - q) * VEC - s + t (q = off
+// div VEC, s = off mod VEC), so shard vector J = v - q is lane v's elements
+// [s, VEC) followed by lane v + 1's [0, s): the lane stores it whole when its
 // neighbour is in the warp and valid.  Lane 31 and the last valid lane store
-// their elements [s, VEC) one by one, lane 0 its elements [0, s); the
-// chunk's own head and tail edges are left to the element-wise edge path.
+// their elements [s, VEC) one by one, lane 0 and the first valid lane their
+// elements [0, s); the chunk's own head and tail edges are left to the
+// element-wise edge path.
 template <int DT_OUT, int VEC>
-__device__ __forceinline__ void store_shard_realigned(void* shard, uint64_t off, uint64_t v, uint64_t v_hi,
-                                                      int lane, const uint32_t* w) {
+__device__ __forceinline__ void store_shard_realigned(void* shard, uint64_t off, uint64_t v, uint64_t v_lo,
+                                                      uint64_t v_hi, int lane, const uint32_t* w) {
   static_assert(VEC * Elem<DT_OUT>::kBytes == 16, "one 16-byte vector per lane");
   const uint4 own = make_uint4(w[0], w[1], w[2], w[3]);
   const uint4 nxt = next_lane(own, own, lane);
-  if (v >= v_hi) return;
+  if (v < v_lo || v >= v_hi) return;
   const int s = static_cast<int>(off % VEC);
   const uint64_t J = v - off / VEC;
   const bool whole = lane < 31 && v + 1 < v_hi;
+  const bool first = lane == 0 || v == v_lo;
   if (whole) st_stream16(static_cast<char*>(shard) + J * 16, realign16(own, nxt, s * Elem<DT_OUT>::kBytes));
   // element t lands at J * VEC - s + t (t fixed per unrolled step, so w stays in registers)
 #pragma unroll
   for (int t = 0; t < VEC; ++t) {
-    if ((t >= s && !whole) || (t < s && lane == 0)) store_one<DT_OUT>(shard, J * VEC - s + t, w, t);
+    if ((t >= s && !whole) || (t < s && first)) store_one<DT_OUT>(shard, J * VEC - s + t, w, t);
   }
 }
 

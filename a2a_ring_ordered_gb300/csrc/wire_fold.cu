@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) wire_fold_kernel(const __grid_consta
         const uint64_t v = base + threadIdx.x + static_cast<uint64_t>(u) * kThreads;
         uint32_t w[(VEC * 2 + 3) / 4];
         pack_out<kBF16, VEC>(acc[u], w);
-        if constexpr (VEC == 8) store_shard_realigned<kBF16, VEC>(a.recv[c], ch.off, v, v_hi, threadIdx.x & 31, w);
+        if constexpr (VEC == 8) store_shard_realigned<kBF16, VEC>(a.recv[c], ch.off, v, v_lo, v_hi, threadIdx.x & 31, w);
       }
     } else {
 #pragma unroll
