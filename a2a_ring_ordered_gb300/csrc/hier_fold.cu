@@ -90,7 +90,11 @@ __global__ void __launch_bounds__(kThreads, 2) hier_fold_kernel(const __grid_con
   const int g0 = (m + 1 == b) ? 0 : m + 1;
 
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
-  for (uint64_t v = v_lo + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi; v += stride) {
+  // counted from v_lo rounded down to 32, so that a warp's 32 stores fill a
+  // whole 512-byte span of every output; lanes before v_lo stay idle
+  const uint64_t v_start = v_lo & ~static_cast<uint64_t>(31);
+  for (uint64_t v = v_start + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; v < v_hi; v += stride) {
+    if (v < v_lo) continue;
     Acc acc[VEC];
     fold_two_level<DT, VEC, BATCH>(f, a, b, g0, l0, v * VEC, acc);
     write_all<DT, VEC>(f, v * VEC, acc);
@@ -115,7 +119,7 @@ template <int DT, int VEC, int BATCH>
 cudaError_t launch_one(const FoldArgs& f, int a, cudaStream_t s) {
   const int b = f.p / a;
   const uint64_t longest = (f.q + 1) / static_cast<uint64_t>(b) + 1;  // elements of the largest sub-chunk
-  const uint64_t per_sub = (longest + VEC - 1) / VEC;
+  const uint64_t per_sub = (longest + VEC - 1) / VEC + 31;  // + the lanes before v_lo
   uint64_t gx = (per_sub + kThreads * kVectorsPerThread - 1) / (kThreads * kVectorsPerThread);
   if (gx < 1) gx = 1;
   if (gx > (1u << 30)) gx = 1u << 30;
