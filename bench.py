@@ -1012,6 +1012,27 @@ def cpu_cores_used() -> int:
     return 1  # numpy element-wise arithmetic runs on one thread
 
 
+def host_description() -> dict:
+    """The host the CPU baselines ran on: cores available to this process
+    (nproc) and the machine / CPU model."""
+    import platform
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu part", "processor name") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"host_cores": cores, "machine": platform.machine(), "cpu": model}
+
+
 def run_reference(a, wl: Workload, rank: int, world: int) -> dict | None:
     """The oracle, as it stands, on the host cores: each step a bounded sample."""
     if rank != 0:
@@ -1044,7 +1065,7 @@ def run_reference(a, wl: Workload, rank: int, world: int) -> dict | None:
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "impl": "reference", "config": cfg,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores_used(),
-                         "kind": "oracle", "sample": desc},
+                         "kind": "oracle", "sample": desc, **host_description()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -1067,7 +1088,7 @@ def cpu_baseline(wl: Workload) -> dict | None:
     t = statistics.median(times)
     out = {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
            "kind": "oracle", "sample": f"{desc}; median of {len(times)} runs",
-           "seconds_per_sample": round(t, 4)}
+           "seconds_per_sample": round(t, 4), **host_description()}
     # the ring on CPU ranks (one host thread per virtual rank), same workload
     try:
         t1, _, _, _ = wl.cpu_ranks_sample(0.01)
