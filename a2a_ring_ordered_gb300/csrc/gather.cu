@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
   // 512-byte spans (whole 128-byte lines) of each output; lanes before v_lo
   // (the previous block's) stay idle.  Measured on GB300: the p = 72 bf16
   // all-gather 0.85 -> 0.99 of the copy bandwidth.  The aligned kernel keeps
-  // v_lo (its fewer registers ran the p = 16 all-gather 4 % slower).
+  // v_lo: with the extra guards it compiled to 64 registers instead of 77
+  // (4 CTAs per SM instead of 3) and ran the p = 16 all-gather 4 % slower.
   const uint64_t v_start = REALIGN ? (v_lo & ~static_cast<uint64_t>(31)) : v_lo;
 
   // U vectors per thread (t, t + kThreads, ...): their loads are issued
