@@ -150,9 +150,20 @@ template <int DT>
 cudaError_t launch_typed(bool vec, const GatherArgs& a, cudaStream_t s) {
   // 8 vectors (128 bytes) of loads in flight per thread before its p x 8
   // stores: at p = 16 that is 0.977 -> 1.022 of the copy bandwidth over 4
-  // vectors, 8 outrunning 2 and 4 and matching 32-byte stores
-  if (vec) return launch_one<DT, 16 / Elem<DT>::kBytes, 8>(a, s);
-  return launch_one<DT, 1, 1>(a, s);
+  // vectors, 8 outrunning 2 and 4 and matching 32-byte stores.  Mid-size
+  // calls whose grid would be under 8 CTAs per SM take 2 vectors per thread
+  // (4x the CTAs) instead, as the fold kernels do: measured on GB300 for
+  // bf16, p = 16 at 8 / 16 MiB per rank 0.74 -> 0.82 / 0.75 -> 0.98 of the
+  // copy bandwidth, p = 2 at 8 MiB 0.59 -> 0.75.  (The broadcast, tried the
+  // same way, went up at p = 4 and down at p = 16, and keeps 8.)
+  if (!vec) return launch_one<DT, 1, 1>(a, s);
+  constexpr int VEC = 16 / Elem<DT>::kBytes;
+  const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
+  const int sms = current_sm_count();
+  const uint64_t want_ctas = 8ull * static_cast<uint64_t>(sms > 0 ? sms : 1);
+  if ((per_chunk + kThreads * 8 - 1) / (kThreads * 8) * static_cast<uint64_t>(a.p) < want_ctas)
+    return launch_one<DT, VEC, 2>(a, s);
+  return launch_one<DT, VEC, 8>(a, s);
 }
 
 // Broadcast: one 1-D pass over the root's buffer (send[0]); each of a

@@ -510,6 +510,7 @@ class AllGather(ReduceScatter):
     def __init__(self, p=16, mib=192, dtype="bf16", seed=2):
         super().__init__(p, mib, dtype, seed)
         self.name = "all_gather"
+        self.kernel = "gather"  # (the base class set "fold")
         self.kernel_key = f"gather_{dtype}_p{p}_n{self.n}"
 
     def config(self):
