@@ -16,10 +16,16 @@ Readings taken where the pages are silent:
   token, then by choice (a stable order); ``slot`` is a row's index among the
   rows that its source sends to the same destination, so its row in d's
   buffer is sum_{s' < s} counts[s'][d] + slot;
-* FP8 dispatch quantises each row in blocks of 128 elements: inv = 448 /
-  amax and code = e4m3(x * inv) (fp32 division, fp32 product, e4m3 rounded to
-  nearest even with saturation to +-448); the block's scale amax / 448 travels
-  as fp32 for dequantisation (an all-zero block gets inv = scale = 1);
+* FP8 dispatch quantises each row in blocks of 128 elements, the per-tile
+  scaling of the DeepSeek-V3 Technical Report that section 7.4 points to
+  (its fine-grained quantisation, section 3.3): the block's scaling factor
+  scale = amax / 448 maps the largest magnitude onto e4m3's largest finite
+  value, quantisation divides by it and dequantisation multiplies by it, so
+  code = e4m3(x / scale) (fp32 divisions, each correctly rounded; e4m3
+  rounded to nearest even with saturation to +-448).  The report does not
+  print the formula; dividing by the factor is the plain meaning of a scaling
+  factor that dequantisation multiplies by.  scale travels as fp32; an
+  all-zero block gets scale = 1;
 * combine: token t's output = bf16( sum_j w[t][j] * y_j ) accumulated in fp32
   in choice order, each product and each sum rounded (no fused multiply-add);
 * expert ids outside [0, E) route nowhere (slot -1) and contribute nothing.
@@ -102,17 +108,13 @@ def _row_offsets(counts: np.ndarray) -> np.ndarray:
 
 
 def quantize_rows_fp8(rows_f32: np.ndarray):
-    """Per 128-element block: inv = 448 / amax, code = e4m3(x * inv), scale =
-    amax / 448 (inv = scale = 1 for an all-zero block).  Returns (codes uint8,
-    scales float32)."""
+    """Per 128-element block: scale = amax / 448 (1 for an all-zero block),
+    code = e4m3(x / scale).  Returns (codes uint8, scales float32)."""
     r, h = rows_f32.shape
     blocks = rows_f32.reshape(r, h // FP8_BLOCK, FP8_BLOCK)
     amax = np.abs(blocks).max(axis=2).astype(np.float32)
-    nz = amax > 0
-    safe = np.where(nz, amax, np.float32(1.0)).astype(np.float32)
-    inv = np.where(nz, np.float32(FP8_MAX) / safe, np.float32(1.0)).astype(np.float32)
-    scale = np.where(nz, safe / np.float32(FP8_MAX), np.float32(1.0)).astype(np.float32)
-    q = f32_to_e4m3((blocks * inv[:, :, None]).astype(np.float32))
+    scale = np.where(amax > 0, amax / np.float32(FP8_MAX), np.float32(1.0)).astype(np.float32)
+    q = f32_to_e4m3((blocks / scale[:, :, None]).astype(np.float32))
     return q.reshape(r, h), scale
 
 

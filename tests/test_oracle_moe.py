@@ -119,20 +119,54 @@ def test_combine_weighted_sum_integer_exact():
 
 
 def test_fp8_rows_within_half_ulp():
+    """Dequantised codes are within half an e4m3 ulp of the input.
+
+    With s the block's scale, v = fl(x / s) = (x / s)(1 + d1), c the e4m3 code
+    of v and d = fl(c * s) = c s (1 + d2) (|d1|, |d2| <= u = 2^-24):
+    d - x = (c - v) s + x d1 + c s d2.  A normal code is within half an ulp
+    of v, |c - v| <= 2^-4 |v|, so |d - x| <= |x| 2^-4 [(1 + u) + 16u +
+    17u(1 + u)] <= |x| 2^-4 (1 + 34u).  A subnormal code is within 2^-10 of
+    v and |x| < 2^-6 s (1 + u), so |d - x| <= 2^-10 s (1 + 33u).  Saturation
+    at 448 moves v by at most 3u * 448.  The check runs in float64 so that
+    its own arithmetic adds no rounding."""
     p, T, k, E, h = 2, 32, 2, 4, 256
+    slack = 34 * 2.0**-24
     ids = _routing(p, T, k, E, 6)
     toks = workloads.normal(p, T * h, 3.0, 6, dtype="bf16")
     recv, scales, _, counts, slots = moe.dispatch(toks, ids, p, k, E, h, fp8=True)
     base = np.vstack([np.zeros((1, p), np.int64), np.cumsum(counts, 0)[:-1]])
     for s in range(p):
-        x = bf16_to_f32(toks[s]).reshape(T, h)
+        x = bf16_to_f32(toks[s]).reshape(T, h).astype(np.float64)
         for i in range(T * k):
             d = ids[s][i] // (E // p)
             pos = base[s][d] + slots[s][i]
-            deq = moe.e4m3_to_f32(recv[d][pos]).reshape(-1, 128) * scales[d][pos][:, None]
-            err = np.abs(deq - x[i // k].reshape(-1, 128))
-            bound = np.maximum(np.abs(x[i // k].reshape(-1, 128)) * 2.0**-4,
-                               scales[d][pos][:, None] * 2.0**-10) * (1 + 1e-5)
+            sc = scales[d][pos].astype(np.float64)[:, None]
+            deq = (moe.e4m3_to_f32(recv[d][pos]).reshape(-1, 128) * scales[d][pos][:, None]).astype(np.float64)
+            xb = x[i // k].reshape(-1, 128)
+            err = np.abs(deq - xb)
+            bound = np.maximum(np.abs(xb) * 2.0**-4, sc * 2.0**-10) * (1 + slack)
             assert (err <= bound).all()
-            amax = np.abs(x[i // k].reshape(-1, 128)).max(axis=1)
+            amax = np.abs(xb).max(axis=1).astype(np.float32)
             np.testing.assert_array_equal(scales[d][pos], (amax / np.float32(448)).astype(np.float32))
+
+
+def test_fp8_codes_are_the_e4m3_of_x_over_scale():
+    """The block's codes are torch's e4m3 cast of torch's fp32 quotient x / s
+    (both correctly rounded; |x / s| stays at or below 448 (1 + 2u), which
+    rounds to 448, so torch's cast never reaches its NaN range); an all-zero
+    block has scale 1 and zero codes; the largest magnitude maps to +-448."""
+    rng = np.random.default_rng(11)
+    rows = (rng.standard_normal((64, 512)) * rng.uniform(1e-3, 50.0, (64, 1))).astype(np.float32)
+    rows[3] = 0.0
+    rows[5, :128] = 0.0
+    rows[7, 200] = -1e4  # one large outlier in block 1
+    codes, scales = moe.quantize_rows_fp8(rows)
+    xb = torch.from_numpy(rows.reshape(64, 4, 128))
+    sc = torch.from_numpy(scales)[:, :, None]
+    want = (xb / sc).to(torch.float8_e4m3fn).view(torch.uint8).numpy().reshape(64, 512)
+    np.testing.assert_array_equal(codes, want)
+    assert (scales[3] == 1.0).all() and (codes[3] == 0).all() and scales[5, 0] == 1.0
+    blocks = np.abs(rows.reshape(64, 4, 128))
+    at_max = blocks == blocks.max(axis=2, keepdims=True)
+    nz = blocks.max(axis=2, keepdims=True) > 0
+    assert ((codes.reshape(64, 4, 128) & 0x7F)[at_max & nz] == 0x7E).all()
