@@ -186,8 +186,10 @@ __device__ __forceinline__ void token_rows(const Args& a, int s, uint64_t t0, in
 // FP8: 16 elements per item, and the 8 consecutive lanes holding a
 // 128-element block reduce its amax with shuffles (a row is a multiple of 128
 // elements, so an aligned group of 8 items never straddles two blocks or two
-// tokens); inv = 448 / amax, code = e4m3(x * inv) rounded to nearest even and
-// saturating; the block scale amax / 448 is stored for dequantisation.
+// tokens); the block's scaling factor scale = amax / 448 is stored for
+// dequantisation and code = e4m3(x / scale), rounded to nearest even and
+// saturating (the DeepSeek-V3 per-tile scaling that section 7.4 of
+// "Networks and Collective Communication" points to).
 template <bool FP8, int U>
 __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_constant__ MoeDispatchArgs a) {
   constexpr int EPI = FP8 ? 16 : 8;  // elements per item
@@ -267,14 +269,15 @@ __global__ void __launch_bounds__(kThreads) moe_dispatch_kernel(const __grid_con
         const unsigned group = 0xFFu << (threadIdx.x & 24);
 #pragma unroll
         for (int off = 4; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(group, amax, off));
-        const float inv = (amax > 0.0f) ? __fdiv_rn(448.0f, amax) : 1.0f;
+        // the block's scaling factor; quantisation divides by it (one
+        // correctly rounded fp32 division per element)
         const float scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
         // two codes per conversion (element 2e in the low byte, 2e+1 above it)
         uint32_t q[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const uint32_t c2 = __nv_cvt_float2_to_fp8x2(
-              make_float2(__fmul_rn(x[2 * e], inv), __fmul_rn(x[2 * e + 1], inv)), __NV_SATFINITE, __NV_E4M3);
+              make_float2(__fdiv_rn(x[2 * e], scale), __fdiv_rn(x[2 * e + 1], scale)), __NV_SATFINITE, __NV_E4M3);
           q[e >> 1] |= (c2 & 0xFFFFu) << (16 * (e & 1));
         }
         const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
