@@ -12,6 +12,7 @@ tensors (torch only provides the device memory and the stream).
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from typing import Sequence
 
@@ -148,10 +149,17 @@ def _stream(stream, device) -> int:
     return int(stream.cuda_stream)
 
 
-def _chunk_lengths(p: int, n: int) -> list[int]:
-    """Expected per-rank shard sizes (the library's chunk rule), for size checks."""
-    q, r = divmod(n, p)
-    return [q + (1 if k < r else 0) for k in range(p)]
+@functools.lru_cache(maxsize=512)
+def _chunk_lengths(p: int, n: int) -> tuple[int, ...]:
+    """Expected per-rank shard sizes, for size checks: the lengths the
+    library's own ``ccl_chunk_bounds`` gives (asked once per (p, n), so the
+    binding keeps no copy of the chunk rule and adds no per-call cost)."""
+    lens = []
+    off, ln = ctypes.c_size_t(), ctypes.c_size_t()
+    for c in range(p):
+        _check(LIB.ccl_chunk_bounds(p, n, c, ctypes.byref(off), ctypes.byref(ln)), "ccl_chunk_bounds")
+        lens.append(ln.value)
+    return tuple(lens)
 
 
 def _numel_check(ts, want, name):

@@ -11,6 +11,7 @@
 #include <atomic>
 #include <mutex>
 
+#include <cuda.h>  // driver types only (CUcontext, CUresult); nothing links the driver
 #include <nvtx3/nvToolsExt.h>
 
 #include "ccl_internal.h"
@@ -1234,10 +1235,46 @@ namespace {
 
 constexpr int kMaxScratchDevices = 256;
 std::mutex g_scratch_mutex;
-void* g_scratch_address[kMaxScratchDevices];  // per device; NULL until looked up
+struct ScratchCache {
+  unsigned long long ctx_id;  // the context the address belongs to
+  void* address;              // NULL until looked up
+};
+ScratchCache g_scratch[kMaxScratchDevices];  // per device ordinal
 
-// Device address of the static scratch on the current device.  Looked up once
-// per device, on the first call made with that device current.
+// The process-unique id of the calling thread's current CUDA context, 0 when
+// the thread has none yet.  The two driver calls are resolved through the
+// runtime (cudaGetDriverEntryPointByVersion), so the library does not link
+// the driver library itself.
+ccl_status_t current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  if (get_current == nullptr || get_id == nullptr) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    cudaError_t err = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1);
+    if (err == cudaSuccess)
+      err = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaGetDriverEntryPointByVersion");
+    if (q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return fail(CCL_ERR_UNSUPPORTED, "the driver lacks cuCtxGetCurrent / cuCtxGetId");
+    get_current = reinterpret_cast<GetCurrent>(f1);
+    get_id = reinterpret_cast<GetId>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return fail(CCL_ERR_CUDA, "cuCtxGetCurrent failed");
+  *id = 0;
+  if (ctx != nullptr && get_id(ctx, id) != CUDA_SUCCESS) return fail(CCL_ERR_CUDA, "cuCtxGetId failed");
+  return CCL_OK;
+}
+
+// Device address of the static scratch in the current device's context.
+// Looked up on the first call made with that device current, and again
+// whenever the current context is not the one the cached address came from
+// (after cudaDeviceReset the primary context is re-created and the module,
+// with its array, is loaded again at another address).
 ccl_status_t static_scratch_address(void** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -1246,13 +1283,20 @@ ccl_status_t static_scratch_address(void** out) {
     return fail(CCL_ERR_UNSUPPORTED, "device %d beyond the %d devices the static scratch tracks",
                 dev, kMaxScratchDevices);
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_address[dev] == nullptr) {
+  unsigned long long ctx = 0;
+  ccl_status_t st = current_context_id(&ctx);
+  if (st != CCL_OK) return st;
+  ScratchCache& c = g_scratch[dev];
+  if (c.address == nullptr || ctx == 0 || ctx != c.ctx_id) {
     void* addr = nullptr;
+    // makes the device's context current on this thread if it was not
     err = cudaGetSymbolAddress(&addr, ccl_static_scratch);
     if (err != cudaSuccess) return cuda_fail(err, "cudaGetSymbolAddress(static scratch)");
-    g_scratch_address[dev] = addr;
+    if ((st = current_context_id(&ctx)) != CCL_OK) return st;
+    c.address = addr;
+    c.ctx_id = ctx;
   }
-  *out = g_scratch_address[dev];
+  *out = c.address;
   return CCL_OK;
 }
 

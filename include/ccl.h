@@ -385,8 +385,16 @@ ccl_status_t ccl_ring_all_gather_literal(const void* const* send, void* const* r
  *   - p*n*4 > CCL_STATIC_SCRATCH_BYTES (p*n above 8,388,608 elements)
  *     -> CCL_ERR_INVALID_ARG, checked before anything is enqueued.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture begins.
+ *     (cudaGetSymbolAddress) with that device current, and looks it up again
+ *     when the current context is no longer the one the address came from
+ *     (after cudaDeviceReset re-creates the device's context).  Make that
+ *     first call before any stream capture begins.
+ *   - The array's memory is reserved when the library's device code is
+ *     loaded into a context.  With the CUDA runtime's default lazy module
+ *     loading that happens at the first call, and that first call can fail
+ *     with CCL_ERR_CUDA if the device has no memory left at that moment.
+ *     Callers that must not fail later make one small warm-up call (n >= 1)
+ *     at initialisation; every later call on that context allocates nothing.
  *   - All calls share the one array, which keeps the last call's contents
  *     (nothing in it needs to start at zero: each call overwrites every byte
  *     it reads).  Calls whose GPU work overlaps -- on different streams, or
