@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
         "ccl_last_error": (ctypes.c_char_p, []),
         "ccl_kernel_launch_count": (u64, []),
         "ccl_chunk_bounds": (st, [i32, sz, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
+        "ccl_fold_plan": (st, [i32, i32, i32, i32, sz, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
         "ccl_device_error_flag": (st, [ctypes.POINTER(ctypes.c_uint), i32]),
         "ccl_stream_check": (st, [vp]),
         "ccl_selftest_bounded_wait": (st, [vp]),
@@ -211,6 +212,20 @@ def ccl_chunk_bounds(p: int, n: int, c: int) -> tuple[int, int]:
     off, ln = ctypes.c_size_t(), ctypes.c_size_t()
     _check(LIB.ccl_chunk_bounds(p, n, c, ctypes.byref(off), ctypes.byref(ln)), "ccl_chunk_bounds")
     return off.value, ln.value
+
+
+def ccl_fold_plan(p: int, n: int, dtype: str = "f32", op: str = "sum", bucket: bool = False,
+                  aligned: bool = True, sm_count: int = 0) -> tuple[int, int]:
+    """(ranks per load batch, vectors per thread) of the fused fold kernel a
+    call of p ranks x n elements takes; (0, 0) is the general kernel.
+    sm_count <= 0 asks the current device."""
+    codes = {"f32": CCL_F32, "bf16": CCL_BF16, "i32": CCL_I32}
+    if dtype not in codes:
+        raise ValueError(f"dtype must be one of {sorted(codes)}")
+    b, v = ctypes.c_int(), ctypes.c_int()
+    _check(LIB.ccl_fold_plan(1 if bucket else 0, codes[dtype], _op_code(op), p, n, 1 if aligned else 0,
+                             sm_count, ctypes.byref(b), ctypes.byref(v)), "ccl_fold_plan")
+    return b.value, v.value
 
 
 def ccl_plan_buckets(numel, elem_bytes: int = 4, cap_bytes: int = 25 * 1024 * 1024):

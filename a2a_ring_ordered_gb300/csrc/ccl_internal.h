@@ -32,6 +32,15 @@ struct FoldArgs {
 // `vec`: every pointer is 16-byte aligned, so 16-byte vectors may be used.
 cudaError_t launch_fold(int mode, int dt, int op, bool vec, const FoldArgs& a, cudaStream_t s);
 
+// The fold kernel a call takes: fold_unrolled_kernel with `batch` ranks'
+// loads issued together and `vectors` vectors per thread, or fold_kernel
+// when batch == 0.  dt_in / dt_out: element types (kF32 -> kBF16 is the
+// bucket); q = floor(n / p); sms = the device's SM count.
+struct FoldPlan {
+  int batch, vectors;
+};
+FoldPlan fold_plan(int dt_in, int dt_out, int op, int p, uint64_t q, bool vec, int sms);
+
 // Fold in another schedule's order (schedule_fold.cu): `linear` = the naive
 // root's rank-order fold; otherwise the pairwise tree over ranks in identity
 // or (`reversed`) bit-reversed order.

@@ -284,46 +284,31 @@ cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
   return launch_kernel(fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, false>, grid, dim3(kThreads), s, a);
 }
 
-// Small p (sums only) goes to fold_unrolled_kernel with (ranks per batch,
-// vectors per thread) = (2, 8), (4, 4) or (8, 2) for 16-byte fp32 / int32
-// vectors.  A bf16 vector widens to 8 fp32 accumulators and a bucket vector
-// is 32 bytes, so those use (2, 4) and (4, 2) (at most 32 accumulators per
-// thread); bf16 takes (8, 2) for p = 5..8 as well, the bucket leaves p > 4
-// to fold_kernel.
+// Instantiations of fold_unrolled_kernel per launch_typed; the choice among
+// them is fold_plan's (below), so that one host function states it.
 template <int DT_IN, int DT_OUT, int OP, int MODE>
 cudaError_t launch_typed(bool vec, const FoldArgs& a, cudaStream_t s) {
   if (!vec) return launch_one<DT_IN, DT_OUT, 1, OP, MODE>(a, s);
   constexpr int VEC = vec_width<DT_IN, DT_OUT>();
   if constexpr (OP == CCL_SUM) {
     constexpr bool kHalve = VEC > 4;
-    // Mid-size messages: with many vectors per thread the grid can be only one
-    // or two CTAs per SM, and the SMs that got two finish last.  Below about
-    // 8 CTAs per SM take fewer vectors per thread instead (2 at p <= 2 for
-    // every type: measured on GB300, bf16 at 8 MiB per rank 0.74 -> 0.77 of
-    // the copy bandwidth against 1, fp32 at 1-4 MiB 10-20 % slower with 4).
-    const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
-    const int sms = current_sm_count();
-    const uint64_t want_ctas = 8ull * static_cast<uint64_t>(sms > 0 ? sms : 1);
-    auto ctas = [&](int u) { return (per_chunk + kThreads * u - 1) / (kThreads * u) * a.p; };
-    if (a.p <= 2) {
-      if (ctas(kHalve ? 4 : 8) >= want_ctas)
-        return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 2, kHalve ? 4 : 8>(a, s);
-      return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 2, 2>(a, s);
+    const FoldPlan pl = fold_plan(DT_IN, DT_OUT, OP, a.p, a.q, true, current_sm_count());
+#define CCL_UNROLLED(B, U) \
+  if (pl.batch == B && pl.vectors == U) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, B, U>(a, s);
+    CCL_UNROLLED(2, 2)
+    CCL_UNROLLED(4, 1)
+    if constexpr (kHalve) {
+      CCL_UNROLLED(2, 4)
+      CCL_UNROLLED(4, 2)
+    } else {
+      CCL_UNROLLED(2, 8)
+      CCL_UNROLLED(4, 4)
     }
-    if (a.p <= 4) {
-      if (ctas(kHalve ? 2 : 4) >= want_ctas)
-        return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 4, kHalve ? 2 : 4>(a, s);
-      return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 4, 1>(a, s);
-    }
-    // p <= 8 with 16-byte vectors of 4 words (fp32, int32, and bf16 in and
-    // out): 8 ranks x 2 vectors.  Measured for bf16 on GB300 against the
-    // general kernel: all-reduce p = 6 0.92 -> 1.03 and p = 8 1.03 -> 1.05,
-    // reduce-scatter p = 8 0.94 -> 1.07 of the copy bandwidth at 256 MiB -
-    // 1 GiB per rank.  (The bucket's 32-byte fp32 vectors would need 128
-    // registers of loads: it stays on fold_kernel.)
     if constexpr (!kHalve || DT_IN == kBF16) {
-      if (a.p <= 8) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, 8, 2>(a, s);
+      CCL_UNROLLED(8, 2)
     }
+#undef CCL_UNROLLED
+    if (pl.batch != 0) return cudaErrorInvalidConfiguration;  // a plan with no instantiation
   }
   return launch_one<DT_IN, DT_OUT, VEC, OP, MODE>(a, s);
 }
@@ -346,6 +331,42 @@ cudaError_t launch_mode(int dt, int op, bool vec, const FoldArgs& a, cudaStream_
 }
 
 }  // namespace
+
+// Small p (sums only) goes to fold_unrolled_kernel with (ranks per batch,
+// vectors per thread) = (2, 8), (4, 4) or (8, 2) for 16-byte fp32 / int32
+// vectors.  A bf16 vector widens to 8 fp32 accumulators and a bucket vector
+// is 32 bytes, so those use (2, 4) and (4, 2) (at most 32 accumulators per
+// thread); bf16 takes (8, 2) for p = 5..8 as well, the bucket leaves p > 4
+// to fold_kernel.
+//
+// Mid-size messages: with many vectors per thread the grid can be only one
+// or two CTAs per SM, and the SMs that got two finish last.  Below about 8
+// CTAs per SM take fewer vectors per thread instead (2 at p <= 2 for every
+// type: measured on GB300, bf16 at 8 MiB per rank 0.74 -> 0.77 of the copy
+// bandwidth against 1, fp32 at 1-4 MiB 10-20 % slower with 4).
+//
+// p <= 8 with 16-byte vectors of 4 words (fp32, int32, and bf16 in and out):
+// 8 ranks x 2 vectors.  Measured for bf16 on GB300 against the general
+// kernel: all-reduce p = 6 0.92 -> 1.03 and p = 8 1.03 -> 1.05,
+// reduce-scatter p = 8 0.94 -> 1.07 of the copy bandwidth at 256 MiB - 1 GiB
+// per rank.  (The bucket's 32-byte fp32 vectors would need 128 registers of
+// loads: it stays on fold_kernel.)
+FoldPlan fold_plan(int dt_in, int dt_out, int op, int p, uint64_t q, bool vec, int sms) {
+  if (!vec || op != CCL_SUM || p < 1) return FoldPlan{0, 0};
+  const int in_bytes = (dt_in == kBF16) ? 2 : 4;
+  const int v = (dt_in == kF32 && dt_out == kBF16) ? 8 : 16 / in_bytes;  // vec_width
+  const bool halve = v > 4;
+  const uint64_t per_chunk = (q + 1 + v - 1) / v;
+  const uint64_t want_ctas = 8ull * static_cast<uint64_t>(sms > 0 ? sms : 1);
+  auto ctas = [&](int u) {
+    return (per_chunk + static_cast<uint64_t>(kThreads) * u - 1) / (static_cast<uint64_t>(kThreads) * u) *
+           static_cast<uint64_t>(p);
+  };
+  if (p <= 2) return ctas(halve ? 4 : 8) >= want_ctas ? FoldPlan{2, halve ? 4 : 8} : FoldPlan{2, 2};
+  if (p <= 4) return ctas(halve ? 2 : 4) >= want_ctas ? FoldPlan{4, halve ? 2 : 4} : FoldPlan{4, 1};
+  if (p <= 8 && (!halve || dt_in == kBF16)) return FoldPlan{8, 2};
+  return FoldPlan{0, 0};
+}
 
 cudaError_t launch_fold(int mode, int dt, int op, bool vec, const FoldArgs& a, cudaStream_t s) {
   cudaError_t err = cudaErrorInvalidValue;

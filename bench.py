@@ -74,16 +74,68 @@ def committed_traffic(kernel_key: str, files: list[str]) -> float | None:
     return float(rec["dram_bytes_per_launch"])
 
 
+class _Nvml:
+    """The few NVML queries the clock record needs, through ctypes (query
+    only: nothing here sets a clock, a limit or a mode)."""
+
+    SM_CLOCK = 1  # NVML_CLOCK_SM
+    # clocks-event reason bits (nvmlClocksEventReason*)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(self.h)) != 0:
+            raise OSError("nvmlDeviceGetHandleByIndex_v2 failed")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        u = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM_CLOCK, ctypes.byref(u)) != 0:
+            raise OSError("nvmlDeviceGetMaxClockInfo failed")
+        self.max_mhz = float(u.value)
+
+    def sample(self) -> list[str]:
+        ct = self.ct
+        mhz, mw, bits = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        ok_c = self.lib.nvmlDeviceGetClockInfo(self.h, self.SM_CLOCK, ct.byref(mhz)) == 0
+        ok_p = self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw)) == 0
+        ok_r = self.reasons_fn(self.h, ct.byref(bits)) == 0
+        act = lambda b: ("Active" if (bits.value & b) else "Not Active") if ok_r else "[N/A]"
+        return [str(mhz.value) if ok_c else "[N/A]", str(self.max_mhz),
+                f"{mw.value / 1000.0:.2f}" if ok_p else "[N/A]",
+                act(0x8), act(0x40), act(0x20), act(0x4)]
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons every 200 ms, with host timestamps."""
+    """SM clock, power and clock-event (throttle) reasons during the timed
+    region: NVML polled every 2 ms from a thread (query only), so even a
+    timed region of about a millisecond is bracketed by samples; nvidia-smi
+    every 200 ms where NVML cannot be loaded."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.002
 
     def __init__(self, gpu_index: int):
         self.samples: list[tuple[float, list[str]]] = []
         self.proc = None
+        self.nvml = None
+        self._stop = threading.Event()
+        try:
+            self.nvml = _Nvml(gpu_index)
+            self.source = "NVML, every 2 ms"
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
+        except (OSError, AttributeError):
+            self.nvml = None
+        self.source = "nvidia-smi, every 200 ms"
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
@@ -94,11 +146,19 @@ class ClockSampler:
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
+    def _poll(self):
+        while not self._stop.is_set():
+            self.samples.append((time.time(), self.nvml.sample()))
+            self._stop.wait(self.PERIOD_S)
+
     def _read(self):
         for line in self.proc.stdout:
             self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
 
     def stop(self):
+        self._stop.set()
+        if self.nvml is not None:
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -108,14 +168,16 @@ class ClockSampler:
 
     def summary(self, t0: float, t1: float) -> dict:
         inside = [s for t, s in self.samples if t0 <= t <= t1]
-        note = "samples inside the timed region"
-        if not inside and self.samples:  # region shorter than the sampling period
-            t_mid = 0.5 * (t0 + t1)
-            inside = [min(self.samples, key=lambda ts: abs(ts[0] - t_mid))[1]]
-            note = "nearest sample (timed region shorter than 200 ms)"
+        note = f"samples inside the timed region ({self.source})"
+        if len(inside) < 2 and self.samples:  # a region shorter than two periods
+            before = [ts for ts in self.samples if ts[0] < t0]
+            after = [ts for ts in self.samples if ts[0] > t1]
+            inside = ([before[-1][1]] if before else []) + inside + ([after[0][1]] if after else [])
+            note = (f"samples inside the timed region plus the last one before and the first one "
+                    f"after it ({self.source}; the region is shorter than two periods)")
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
+                    "note": "no clock source (NVML and nvidia-smi unavailable)"}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for s in inside for i in range(4)
                           if len(s) > 3 + i and s[3 + i].lower().startswith("active")})
@@ -1350,7 +1412,7 @@ def run_sweep(a) -> int:
         tdt = torch.float32 if dt == "f32" else torch.bfloat16
         for p in ps:
             top = 28 if p == 72 else 30  # p=72 up to 256 MiB per rank, else 1 GiB
-            for lg in range(10, top + 1, a.sweep_stride):
+            for lg in range(max(10, a.sweep_lo), min(top, a.sweep_hi) + 1, a.sweep_stride):
                 nbytes_rank = 1 << lg
                 n = nbytes_rank // e
                 lens = [lib.ccl_chunk_bounds(p, n, k)[1] for k in range(p)]
@@ -1444,6 +1506,8 @@ def main(argv=None) -> int:
                     help="all-reduce message-size sweep (1 KiB..1 GiB per rank), one line per point")
     ap.add_argument("--sweep-stride", type=int, default=1, help="log2 step between sweep sizes")
     ap.add_argument("--sweep-dtype-only", action="store_true", help="sweep only --dtype")
+    ap.add_argument("--sweep-lo", type=int, default=10, help="log2 of the smallest per-rank message (bytes)")
+    ap.add_argument("--sweep-hi", type=int, default=30, help="log2 of the largest per-rank message (bytes)")
     ap.add_argument("--sweep-collective", default="allreduce",
                     choices=["allreduce", "reduce_scatter", "all_gather", "all_to_all"],
                     help="collective of --sweep")

@@ -134,3 +134,41 @@ def hierarchical_at_columns(cols: list[np.ndarray], idx: np.ndarray, n: int, gro
                 tot = part if tot is None else combine(tot, part, "sum")
             out[mask] = tot
     return f32_to_bf16_rne(out) if dtype == "bf16" else out
+
+
+def all_gather_source(p: int, n: int, idx: np.ndarray):
+    """Where the all-gather's output element ``idx`` comes from ("Networks and
+    Collective Communication" section 4.1: rank k contributes block k, which
+    lands at off(k) of every rank's output): the contributing rank k (the
+    chunk holding idx) and the position idx - off(k) in its block."""
+    idx = np.asarray(idx, dtype=np.int64)
+    k = chunk_of(p, n, idx)
+    offs = np.array([off for off, _ in chunk_bounds(p, n)], dtype=np.int64)
+    return k, idx - offs[k]
+
+
+def all_to_all_source(p: int, n: int, j: int, idx: np.ndarray):
+    """Where rank j's all-to-all output element ``idx`` comes from (section
+    4.1, the transpose: rank j receives block j of every rank, in source
+    order, so its output is p blocks of len(j)): the source rank
+    idx // len(j) and the position off(j) + idx mod len(j) in its buffer."""
+    idx = np.asarray(idx, dtype=np.int64)
+    off, ln = chunk_bounds(p, n)[j]
+    if idx.size and (idx.min() < 0 or idx.max() >= p * ln):
+        raise IndexError("index out of range")
+    return idx // ln, off + idx % ln
+
+
+def all_to_allv_source(counts: np.ndarray, d: int, rows: np.ndarray):
+    """Where destination d's received row ``rows`` comes from in the
+    row-granular all-to-allv (the layout of ``oracle.collectives.all_to_allv``:
+    d holds its blocks in source order, source s holds its blocks in
+    destination order): the source rank s and the row of s's send buffer."""
+    counts = np.asarray(counts, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    recv_start = np.concatenate([[0], np.cumsum(counts[:, d])])      # d's block from s starts here
+    if rows.size and (rows.min() < 0 or rows.max() >= recv_start[-1]):
+        raise IndexError("row out of range")
+    src = np.searchsorted(recv_start, rows, side="right") - 1
+    send_start = np.concatenate([np.zeros((counts.shape[0], 1), np.int64), np.cumsum(counts, axis=1)], axis=1)
+    return src, send_start[src, d] + (rows - recv_start[src])

@@ -81,14 +81,43 @@ def test_reference_arm_nonzero_rank_prints_nothing():
 
 def test_clock_summary_parses_samples():
     s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.source = "test"
     s.samples = [(10.0, ["1900", "2070", "800.5", "Not Active", "Not Active", "Not Active", "Active"]),
                  (10.2, ["1950", "2070", "810.0", "Not Active", "Not Active", "Not Active", "Not Active"]),
                  (99.0, ["300", "2070", "90", "Not Active", "Not Active", "Not Active", "Not Active"])]
     out = s.summary(9.9, 10.3)
     assert out["sm_mhz"] == 1925 and out["sm_max_mhz"] == 2070
     assert out["reasons"] == ["sw_power_cap"] and out["samples"] == 2
-    short = s.summary(50.0, 50.01)  # region shorter than the period: nearest sample
-    assert short["samples"] == 1
+    # a region shorter than two periods: bracketed by the samples around it
+    short = s.summary(50.0, 50.01)
+    assert short["samples"] == 2 and short["sm_mhz"] == (1950 + 300) / 2
+    assert "before" in short["note"]
+
+
+def test_nvml_sample_decodes_clocks_power_and_reasons():
+    """The NVML poller (query calls only) against a fake library: SM clock,
+    power in W and the clock-event reason bits it reports."""
+    import ctypes
+
+    class Fake:
+        def nvmlDeviceGetClockInfo(self, h, kind, out):
+            ctypes.cast(out, ctypes.POINTER(ctypes.c_uint))[0] = 1965 if kind == 1 else 0
+            return 0
+
+        def nvmlDeviceGetPowerUsage(self, h, out):
+            ctypes.cast(out, ctypes.POINTER(ctypes.c_uint))[0] = 812_500
+            return 0
+
+        def reasons(self, h, out):
+            ctypes.cast(out, ctypes.POINTER(ctypes.c_ulonglong))[0] = 0x4 | 0x40
+            return 0
+
+    n = bench._Nvml.__new__(bench._Nvml)
+    n.ct, n.lib, n.h, n.max_mhz = ctypes, Fake(), ctypes.c_void_p(), 2070.0
+    n.reasons_fn = n.lib.reasons
+    smp = n.sample()
+    assert smp[:3] == ["1965", "2070.0", "812.50"]
+    assert smp[3:] == ["Not Active", "Active", "Not Active", "Active"]  # hw, hw_thermal, sw_thermal, sw_power
 
 
 def test_warmup_below_three_is_rejected():

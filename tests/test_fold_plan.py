@@ -1,0 +1,81 @@
+"""Host checks of the fused fold kernel's variant choice (``ccl_fold_plan``).
+
+Runs without a GPU (the plan is host code; the SM count is passed in).  The
+guard walks the size classes of every (kind, dtype, p) and requires that each
+variant the plan can pick has a GPU parity case in ``fold_variants.CASES`` for
+that kind and dtype, so a new variant or a moved threshold cannot leave a
+kernel instantiation untested.
+"""
+from __future__ import annotations
+
+import pytest
+
+import fold_variants
+
+SM_COUNTS = (132, 144, 148, 152, 160)
+
+
+def _lib():
+    from a2a_ring_ordered_gb300 import build
+
+    build.build()
+    from a2a_ring_ordered_gb300 import ccl
+
+    return ccl
+
+
+def _sizes():
+    out = {0, 1, 2, 3}
+    for k in range(1, 32):
+        for base in (1 << k, 3 << (k - 1)):
+            out.update((base - 1, base, base + 1))
+    return sorted(out)
+
+
+def _reachable(lib, dtype, bucket):
+    seen = set()
+    for p in range(1, 17):
+        for n in _sizes():
+            for sms in SM_COUNTS:
+                seen.add(lib.ccl_fold_plan(p, n, dtype, "sum", bucket=bucket, sm_count=sms))
+    return seen
+
+
+@pytest.mark.parametrize("kind", fold_variants.KINDS)
+def test_every_reachable_fold_variant_has_a_gpu_case(kind):
+    lib = _lib()
+    dtypes = ("f32",) if kind == "bucket" else ("f32", "bf16", "i32")
+    for dt in dtypes:
+        reach = _reachable(lib, dt, kind == "bucket")
+        covered = {plan for (k, d, _, _, plan) in fold_variants.CASES if k == kind and d == dt}
+        missing = reach - covered
+        assert not missing, f"{kind} {dt}: variants {sorted(missing)} have no GPU parity case"
+
+
+@pytest.mark.parametrize("case", fold_variants.CASES, ids=fold_variants.case_id)
+def test_gpu_cases_select_their_variant_on_a_152_sm_device(case):
+    kind, dt, p, n, plan = case
+    lib = _lib()
+    assert lib.ccl_fold_plan(p, n, dt, "sum", bucket=kind == "bucket", sm_count=152) == plan
+    assert n % p != 0 or p == 1, "cases keep ragged chunk edges"
+
+
+def test_max_min_and_unaligned_calls_take_the_general_kernel():
+    lib = _lib()
+    for dt in ("f32", "bf16", "i32"):
+        for p in (1, 2, 4, 8):
+            assert lib.ccl_fold_plan(p, 1 << 24, dt, "max", sm_count=152) == (0, 0)
+            assert lib.ccl_fold_plan(p, 1 << 24, dt, "min", sm_count=152) == (0, 0)
+            assert lib.ccl_fold_plan(p, 1 << 24, dt, "sum", aligned=False, sm_count=152) == (0, 0)
+
+
+def test_fold_plan_rejects_bad_arguments():
+    lib = _lib()
+    with pytest.raises(lib.CclError):
+        lib.ccl_fold_plan(0, 10)
+    with pytest.raises(lib.CclError):
+        lib.ccl_fold_plan(129, 10)
+    with pytest.raises(lib.CclError):
+        lib.ccl_fold_plan(4, 10, "bf16", bucket=True)
+    with pytest.raises(lib.CclError):
+        lib.ccl_fold_plan(4, 10, "f32", "max", bucket=True)

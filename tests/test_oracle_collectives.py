@@ -193,3 +193,50 @@ def test_ulysses_is_an_all_to_all_of_contiguous_segments():
     x = workloads.normal(p, p, 1.0, 0)  # shard s: [1 token, H = p heads, D = 1]
     np.testing.assert_array_equal(np.concatenate(collectives.ulysses_seq_to_heads(x, p, 1)),
                                   np.concatenate(collectives.all_to_all(x)))
+
+
+@pytest.mark.parametrize("p", [1, 2, 3, 5, 7])
+@pytest.mark.parametrize("n", [0, 1, 4, 13, 23])
+def test_pointwise_sources_match_the_whole_buffer_collectives(p, n):
+    """The per-element source maps (used to check huge outputs at sampled
+    positions) agree at every position with the whole-buffer all-gather (and
+    the literal ring all-gather) and the block-transpose all-to-all, on inputs
+    whose every value names its rank and position."""
+    from oracle import pointwise
+
+    x = [np.arange(n, dtype=np.int64) + 1000 * r for r in range(p)]
+    parts = [x[k][off:off + ln] for k, (off, ln) in enumerate(ring.chunk_bounds(p, n))]
+    ag = collectives.all_gather(parts)
+    ring_ag, _ = ring.ring_all_gather([v.astype(np.int32) for v in parts], "i32")
+    idx = np.arange(n, dtype=np.int64)
+    k, pos = pointwise.all_gather_source(p, n, idx)
+    got = np.array([parts[a][b] for a, b in zip(k, pos)], dtype=np.int64)
+    for r in range(p):
+        np.testing.assert_array_equal(got, ag[r])
+        np.testing.assert_array_equal(got.astype(np.int32), ring_ag[r])
+    a2a = collectives.all_to_all(x)
+    for j in range(p):
+        m = len(a2a[j])
+        src, spos = pointwise.all_to_all_source(p, n, j, np.arange(m, dtype=np.int64))
+        got = np.array([x[a][b] for a, b in zip(src, spos)], dtype=np.int64)
+        np.testing.assert_array_equal(got, a2a[j])
+
+
+@pytest.mark.parametrize("p,seed", [(1, 0), (3, 1), (5, 2), (8, 3)])
+def test_all_to_allv_source_matches_the_whole_buffer_exchange(p, seed):
+    """The per-row source map agrees with ``collectives.all_to_allv`` at every
+    received row, with empty blocks among the counts; every value names its
+    source rank and row."""
+    from oracle import pointwise
+
+    rng = np.random.default_rng(seed)
+    counts = rng.integers(0, 4, size=(p, p))
+    counts[rng.random((p, p)) < 0.3] = 0
+    row = 3
+    send = [np.repeat(np.arange(counts[s].sum(), dtype=np.int64) + 1000 * s, row) for s in range(p)]
+    recv = collectives.all_to_allv(send, counts, row)
+    for d in range(p):
+        m = len(recv[d]) // row
+        src, srow = pointwise.all_to_allv_source(counts, d, np.arange(m, dtype=np.int64))
+        got = np.array([send[a][b * row] for a, b in zip(src, srow)], dtype=np.int64)
+        np.testing.assert_array_equal(got, recv[d][::row])
