@@ -2,131 +2,239 @@
 // ("Networks and Collective Communication" section 4.1: device i's block j
 // goes to device j, a transpose; section 7.4: MoE dispatch and combine).
 //
-// The host turns the p x p row counts into a list of contiguous byte blocks
-// (source s's block for d -> destination d's block from s).  Blocks are cut
-// into 32 KB tiles measured in destination space, and one CTA copies one
-// tile, so the work is balanced by bytes however skewed the counts are (a
-// Zipf-hot expert receives far more rows than the others).
+// Destination j's buffer holds one block from every source i, in source
+// order: block i is rows [cs_i, cs_{i+1}) of recv[j] and starts at row rs_i
+// of send[i].  The plain all-to-all takes cs and rs from the chunk rule
+// (cs_i = i * len(j), rs_i = off(j), one element per row); the all-to-allv
+// takes rs from a row-prefix table in the kernel's parameter block and scans
+// the table's column for cs on the device.  Nothing is allocated and any
+// p <= 85 is one launch (the plain all-to-all: any p).
 //
-// Inside a tile, whole 16-byte destination units are copied with 16-byte
-// loads and stores.  When source and destination differ in 16-byte phase
-// (rows whose size is not a multiple of 16 bytes), each lane of a warp loads
-// the aligned 16-byte source granule under its unit, takes the next granule
-// from its neighbour with a warp shuffle, and funnel-shifts the pair into the
-// destination's alignment; the few bytes before the first and after the last
-// whole unit are copied one by one.  Every load touches only aligned granules
-// that hold at least one source byte of the block.
-// HBM traffic: one read and one write of every moved byte.
+// Work is cut into 32 KB tiles of destination space (tile boundaries on 512
+// bytes of the destination's address), one CTA per tile, so the work is
+// balanced by bytes however skewed the counts are.  The CTA puts the
+// destination's block bounds in shared memory, and each thread writes whole
+// aligned 16-byte destination units (a warp's 32 stores fill whole 128-byte
+// lines):
+//  * a unit inside one block is one aligned 16-byte source load when source
+//    and destination share the 16-byte phase, else two aligned source
+//    granules whose bytes are funnel-shifted into place;
+//  * a unit that straddles blocks (small blocks, block edges) is assembled
+//    element by element from its blocks and still stored whole;
+//  * only the units at the ends of the destination buffer, partly outside
+//    it, are stored element by element.
+// Every load touches only aligned granules that hold at least one byte of a
+// block, and element loads are element-aligned.  HBM traffic: one read and
+// one write of every moved byte.
 #include "device_common.cuh"
 #include "realign.cuh"
 
 namespace ccl {
 namespace {
 
-constexpr int kUnitsPerThread = static_cast<int>(kA2ATileBytes / 16 / kThreads);  // 8
+constexpr int kUnitsPerTile = static_cast<int>(kA2ATileBytes / 16);  // 2048
+constexpr int kUnitsPerThread = kUnitsPerTile / kThreads;             // 8
 
-__device__ __forceinline__ void copy_byte(uintptr_t dst, intptr_t shift) {
-  const unsigned char b = __ldg(reinterpret_cast<const unsigned char*>(dst + shift));
-  *reinterpret_cast<unsigned char*>(dst) = b;
+// Bounds of destination j's blocks, in bytes: block i covers destination
+// bytes [dst0 + cs[i], dst0 + cs[i+1]) and its first byte comes from src[i].
+struct Blocks {
+  uint64_t* cs;       // p + 1 entries (shared memory)
+  const char** src;   // p entries (shared memory)
+  uintptr_t dst0;
+  int p;
+};
+
+// The block holding destination byte offset `x` (x < cs[p]): the last i in
+// [lo, hi] whose block starts at or before x (an empty block starts where
+// the next one does, so the one found is never empty).
+__device__ __forceinline__ int block_of(const Blocks& b, uint64_t x, int lo, int hi) {
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (b.cs[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
-// Copy destination bytes [lo, hi); the source byte of destination byte x is
-// x + shift.  Called by all threads of the CTA with the same arguments.
-// REALIGN = false is launched only when every block of the call has source
-// and destination in the same 16-byte phase; it leaves out the realigning
-// path and its registers (64 against 128), and any other phase would still
-// be copied correctly, byte by byte.
-template <bool REALIGN>
-__device__ void copy_tile(uintptr_t lo, uintptr_t hi, intptr_t shift) {
-  const int tid = threadIdx.x;
-  const uintptr_t ua = (lo + 15) & ~static_cast<uintptr_t>(15);
-  const uintptr_t ub = hi & ~static_cast<uintptr_t>(15);
-  if (ua >= ub) {  // no whole destination unit: byte by byte
-    for (uintptr_t x = lo + tid; x < hi; x += kThreads) copy_byte(x, shift);
-    return;
-  }
-  // Units are counted from ua rounded down to 512 bytes, so that every warp's
-  // 32 stores fill a whole 512-byte span (whole 128-byte lines); the units
-  // before ua (u < u_first) stay idle.
-  const uintptr_t uo = ua & ~static_cast<uintptr_t>(511);
-  const uint64_t u_first = (ua - uo) / 16;
-  const uint64_t m = (ub - uo) / 16;  // one past the last whole 16-byte destination unit
-  const int delta = static_cast<int>(static_cast<uintptr_t>(shift) & 15);
-  if (!REALIGN && delta != 0) {
-    for (uintptr_t x = lo + tid; x < hi; x += kThreads) copy_byte(x, shift);
-    return;
-  }
-  if (delta == 0) {
-    for (uint64_t u0 = 0; u0 < m; u0 += static_cast<uint64_t>(kThreads) * kUnitsPerThread) {
-      uint4 v[kUnitsPerThread];
-#pragma unroll
-      for (int j = 0; j < kUnitsPerThread; ++j) {
-        const uint64_t u = u0 + static_cast<uint64_t>(j) * kThreads + tid;
-        if (u >= u_first && u < m) v[j] = ld_once16(reinterpret_cast<const void*>(uo + 16 * u + shift));
-      }
-#pragma unroll
-      for (int j = 0; j < kUnitsPerThread; ++j) {
-        const uint64_t u = u0 + static_cast<uint64_t>(j) * kThreads + tid;
-        if (u >= u_first && u < m) st_stream16(reinterpret_cast<void*>(uo + 16 * u), v[j]);
-      }
-    }
-  } else if constexpr (REALIGN) {
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    // source granule under unit u: uo + 16u + shift - delta (16-byte aligned).
-    // A warp takes 32 consecutive units per group, kUnitsPerThread groups
-    // (kThreads units apart) with their loads issued together.
-    const uintptr_t g0 = uo + shift - delta;
-    for (uint64_t k0 = static_cast<uint64_t>(warp) * 32; k0 < m;
-         k0 += static_cast<uint64_t>(kThreads) * kUnitsPerThread) {
-      uint4 cur[kUnitsPerThread], extra[kUnitsPerThread];
-#pragma unroll
-      for (int j = 0; j < kUnitsPerThread; ++j) {
-        const uint64_t u = k0 + static_cast<uint64_t>(j) * kThreads + lane;
-        cur[j] = make_uint4(0, 0, 0, 0);
-        extra[j] = make_uint4(0, 0, 0, 0);
-        // granule u holds bytes of unit u (u < m) or the last bytes of unit u-1 (u == m)
-        if (u >= u_first && u <= m) cur[j] = ld_once16(reinterpret_cast<const void*>(g0 + 16 * u));
-        if (lane == 31 && u >= u_first && u < m)
-          extra[j] = ld_once16(reinterpret_cast<const void*>(g0 + 16 * (u + 1)));
-      }
-#pragma unroll
-      for (int j = 0; j < kUnitsPerThread; ++j) {
-        const uint64_t u = k0 + static_cast<uint64_t>(j) * kThreads + lane;
-        const uint4 nxt = next_lane(cur[j], extra[j], lane);
-        if (u >= u_first && u < m)
-          st_stream16(reinterpret_cast<void*>(uo + 16 * u), realign16(cur[j], nxt, delta));
-      }
-    }
-  }
-  // bytes before the first and after the last whole unit (at most 15 + 15)
-  const int n_head = static_cast<int>(ua - lo);
-  const int n_edge = n_head + static_cast<int>(hi - ub);
-  if (tid < n_edge) copy_byte(tid < n_head ? lo + tid : ub + (tid - n_head), shift);
+__device__ __forceinline__ uint32_t load_elem(const char* p, int e) {
+  return (e == 4) ? ld_once4(p) : ld_once2(p);
 }
 
-template <int CAP, bool REALIGN>
-__global__ void __launch_bounds__(kThreads) a2av_kernel(const __grid_constant__ A2AArgsT<CAP> a) {
-  pdl_enter();
-  for (uint64_t t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
-    // the block that owns tile t: the last one whose first tile is <= t
-    int lo = 0, hi = a.ndesc - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.d[mid].tile0 <= t) lo = mid; else hi = mid - 1;
+// Destination unit [ua, ua + 16) element by element: the valid bytes are
+// [max(ua, vlo), min(ua + 16, vhi)); block i holds the first of them.
+// Inside the buffer the elements are assembled and stored as one 16-byte
+// unit; at the buffer's ends each element is stored on its own.
+__device__ __noinline__ void unit_by_elements(const uint64_t* cs, const char* const* src, uintptr_t dst0,
+                                              uintptr_t ua, uintptr_t vlo, uintptr_t vhi, int i, int e) {
+  const uintptr_t x0 = ua > vlo ? ua : vlo;
+  const uintptr_t x1 = ua + 16 < vhi ? ua + 16 : vhi;
+  const bool whole = x0 == ua && x1 == ua + 16;
+  uint32_t w[4] = {0, 0, 0, 0};
+  for (uintptr_t x = x0; x < x1; x += e) {
+    const uint64_t off = x - dst0;
+    while (cs[i + 1] <= off) ++i;
+    const uint32_t v = load_elem(src[i] + (off - cs[i]), e);
+    if (whole) {
+      const int k = static_cast<int>(x - ua);
+      w[k >> 2] |= (e == 4) ? v : (v << (8 * (k & 3)));
+    } else if (e == 4) {
+      st_stream4(reinterpret_cast<void*>(x), v);
+    } else {
+      st_stream2(reinterpret_cast<void*>(x), v);
     }
-    const A2ADesc& d = a.d[lo];
-    const uintptr_t d0 = reinterpret_cast<uintptr_t>(d.dst);
-    const uintptr_t d_end = d0 + d.bytes;
-    const uintptr_t base = d0 & ~static_cast<uintptr_t>(511);  // tiles on 512-byte boundaries
-    const uint64_t k = t - d.tile0;
-    uintptr_t tlo = base + k * kA2ATileBytes;
-    uintptr_t thi = tlo + kA2ATileBytes;
-    if (tlo < d0) tlo = d0;
-    if (thi > d_end) thi = d_end;
-    const intptr_t shift = reinterpret_cast<intptr_t>(d.src) - reinterpret_cast<intptr_t>(d.dst);
-    copy_tile<REALIGN>(tlo, thi, shift);
   }
+  if (whole) st_stream16(reinterpret_cast<void*>(ua), make_uint4(w[0], w[1], w[2], w[3]));
+}
+
+// SHIFT: some block's source and destination differ in 16-byte phase (the
+// host checks); without it each thread keeps 8 units' loads in flight,
+// with it 4 units' two granules.  64 registers, 4 CTAs per SM.
+template <class P, bool SHIFT>
+__global__ void __launch_bounds__(kThreads, 4) a2a_kernel(const __grid_constant__ P a) {
+  __shared__ uint64_t s_cs[P::kCap + 1];
+  __shared__ const char* s_src[P::kCap];
+  bool entered = false;
+  const int p = a.p;
+  const uint64_t rb = a.row_bytes;
+  const uint64_t total_tiles = a.tile0[a.ndest];
+  for (uint64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+    // this tile's destination (uniform over the CTA)
+    int c = 0;
+    {
+      int lo = 0, hi = a.ndest - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.tile0[mid] <= t) lo = mid; else hi = mid - 1;
+      }
+      c = lo;
+    }
+    const int j = a.j0 + c;
+    // block bounds of destination j, in bytes
+    if (a.plain) {
+      const uint64_t len = a.q + (static_cast<uint64_t>(j) < a.rem ? 1 : 0);
+      const uint64_t off = static_cast<uint64_t>(j) * a.q + (static_cast<uint64_t>(j) < a.rem ? j : a.rem);
+      for (int i = threadIdx.x; i <= p; i += kThreads) {
+        s_cs[i] = static_cast<uint64_t>(i) * len * rb;
+        if (i < p) s_src[i] = a.send[i] + off * rb;
+      }
+    } else if (threadIdx.x < 32) {
+      // exclusive scan of the column's counts (rows of source i for j)
+      const int stride = a.ndest + 1;
+      uint64_t carry = 0;
+      for (int i0 = 0; i0 < p; i0 += 32) {
+        const int i = i0 + static_cast<int>(threadIdx.x);
+        uint64_t rs = 0, cnt = 0;
+        if (i < p) {
+          rs = static_cast<uint64_t>(a.table[i * stride + c]);
+          cnt = static_cast<uint64_t>(a.table[i * stride + c + 1]) - rs;
+        }
+        uint64_t incl = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+          if (static_cast<int>(threadIdx.x) >= d) incl += v;
+        }
+        if (i < p) {
+          s_cs[i] = (carry + incl - cnt) * rb;
+          s_src[i] = a.send[i] + rs * rb;
+        }
+        carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      if (threadIdx.x == 0) s_cs[p] = carry * rb;
+    }
+    __syncthreads();
+
+    Blocks b{s_cs, s_src, reinterpret_cast<uintptr_t>(a.recv[j]), p};
+    const uintptr_t vlo0 = b.dst0, vhi0 = b.dst0 + s_cs[p];
+    const uintptr_t tlo = (b.dst0 & ~static_cast<uintptr_t>(511)) + (t - a.tile0[c]) * kA2ATileBytes;
+    const uintptr_t vlo = tlo > vlo0 ? tlo : vlo0;
+    const uintptr_t vhi = tlo + kA2ATileBytes < vhi0 ? tlo + kA2ATileBytes : vhi0;
+    // the blocks this tile touches
+    const int ia = block_of(b, vlo - b.dst0, 0, p - 1);
+    const int ib = block_of(b, vhi - 1 - b.dst0, ia, p - 1);
+    if (!entered) {
+      // The CTA's first tile (one CTA per tile: its only one): its source
+      // bytes are prefetched into L2 before waiting on the previous grid
+      // (the block bounds come from the parameters alone), so that the loads
+      // of the first wave overlap the previous grid's drain and every CTA's
+      // second pass (SHIFT) finds its data on the way.  Measured on GB300
+      // against no prefetch: MoE dispatch / combine (p = 8, 8 KiB rows)
+      // 0.91 -> 1.05 of the copy bandwidth, p = 72 all-to-all 0.86 -> 1.01
+      // at 8 MiB per rank.  The prefetch is a hint and cannot change a
+      // result: L2 is the device's point of coherence, and the loads after
+      // pdl_enter() read L2, not L1 (which a prefetch does not fill).
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      for (int i = ia + warp; i <= ib; i += kThreads / 32) {
+        const uintptr_t bs = b.dst0 + s_cs[i], be = b.dst0 + s_cs[i + 1];
+        const uintptr_t lo = vlo > bs ? vlo : bs, hi = vhi < be ? vhi : be;
+        if (lo >= hi) continue;
+        const uintptr_t s0 = reinterpret_cast<uintptr_t>(s_src[i]) + (lo - bs), s1 = s0 + (hi - lo);
+        for (uintptr_t line = (s0 & ~static_cast<uintptr_t>(127)) + 128 * lane; line < s1; line += 128 * 32)
+          prefetch_l2(reinterpret_cast<const void*>(line));
+      }
+      pdl_enter();
+      entered = true;
+    }
+
+    // units t, t + kThreads, ... of the tile, U at a time with their loads
+    // issued together
+    constexpr int U = SHIFT ? 4 : 8;
+#pragma unroll 1
+    for (int w0 = 0; w0 < kUnitsPerThread; w0 += U) {
+      uint4 g0[U], g1[U];
+      // per unit: -1 outside the tile's bytes, else (block << 5) | (whole << 4) | phase
+      int code[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uintptr_t ua = tlo + 16 * static_cast<uintptr_t>((w0 + u) * kThreads + threadIdx.x);
+        code[u] = -1;
+        if (ua + 16 <= vlo || ua >= vhi) continue;
+        const uintptr_t x0 = ua > vlo ? ua : vlo;
+        const int i = (ia == ib) ? ia : block_of(b, x0 - b.dst0, ia, ib);
+        code[u] = i << 5;
+        const uintptr_t bs = b.dst0 + s_cs[i], be = b.dst0 + s_cs[i + 1];
+        if (ua >= bs && ua + 16 <= be) {
+          const uintptr_t src = reinterpret_cast<uintptr_t>(s_src[i]) + (ua - bs);
+          const int dl = static_cast<int>(src & 15);
+          const char* g = reinterpret_cast<const char*>(src - dl);
+          if constexpr (SHIFT) {
+            code[u] |= 16 | dl;
+            g0[u] = ld_l1_16(g);
+            if (dl != 0) g1[u] = ld_l1_16(g + 16);
+          } else if (dl == 0) {
+            // (not launched with a phase shift; element-wise if it were)
+            code[u] |= 16;
+            g0[u] = ld_once16(g);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uintptr_t ua = tlo + 16 * static_cast<uintptr_t>((w0 + u) * kThreads + threadIdx.x);
+        if (code[u] < 0) continue;
+        if (code[u] & 16) {
+          uint4 o = g0[u];
+          if constexpr (SHIFT) {
+            if (code[u] & 15) o = realign16(g0[u], g1[u], code[u] & 15);
+          }
+          st_stream16(reinterpret_cast<void*>(ua), o);
+        } else {
+          unit_by_elements(s_cs, s_src, b.dst0, ua, vlo, vhi, code[u] >> 5, a.elem);
+        }
+      }
+    }
+    __syncthreads();  // the block bounds are rewritten for the next tile
+  }
+  if (!entered) pdl_enter();
+}
+
+template <class P>
+cudaError_t launch_params(const P& a, bool shift, cudaStream_t s) {
+  const uint64_t tiles = a.tile0[a.ndest];
+  if (tiles == 0) return cudaSuccess;
+  const uint64_t g = tiles < (1ull << 31) - 1 ? tiles : (1ull << 31) - 1;
+  const dim3 grid(static_cast<unsigned>(g));
+  return shift ? launch_kernel(a2a_kernel<P, true>, grid, dim3(kThreads), s, a)
+               : launch_kernel(a2a_kernel<P, false>, grid, dim3(kThreads), s, a);
 }
 
 }  // namespace
@@ -137,27 +245,24 @@ uint64_t a2a_tiles_for(const char* dst, uint64_t bytes) {
   return (lead + bytes + kA2ATileBytes - 1) / kA2ATileBytes;
 }
 
-cudaError_t launch_a2av(const A2AArgs& a, cudaStream_t s) {
-  if (a.total_tiles == 0 || a.ndesc == 0) return cudaSuccess;
-  uint64_t g = a.total_tiles;
-  if (g > (1u << 30)) g = 1u << 30;
-  const dim3 grid(static_cast<unsigned>(g));
-  bool phased = false;  // some block's source and destination differ in 16-byte phase
-  for (int i = 0; i < a.ndesc && !phased; ++i)
-    phased = ((reinterpret_cast<uintptr_t>(a.d[i].src) - reinterpret_cast<uintptr_t>(a.d[i].dst)) & 15) != 0;
-  cudaError_t err;
-  if (a.ndesc <= kA2ASmallDesc) {  // the common case: a 4 KB parameter block
-    A2AArgsT<kA2ASmallDesc> small;
-    small.total_tiles = a.total_tiles;
-    small.ndesc = a.ndesc;
-    for (int i = 0; i < a.ndesc; ++i) small.d[i] = a.d[i];
-    err = phased ? launch_kernel(a2av_kernel<kA2ASmallDesc, true>, grid, dim3(kThreads), s, small)
-                 : launch_kernel(a2av_kernel<kA2ASmallDesc, false>, grid, dim3(kThreads), s, small);
-  } else {
-    err = phased ? launch_kernel(a2av_kernel<kA2AMaxDesc, true>, grid, dim3(kThreads), s, a)
-                 : launch_kernel(a2av_kernel<kA2AMaxDesc, false>, grid, dim3(kThreads), s, a);
-  }
-  if (err == cudaSuccess) note_launch();
+cudaError_t launch_a2a(const A2ASmall& a, bool shift, cudaStream_t s) {
+  cudaError_t err = launch_params(a, shift, s);
+  if (err == cudaSuccess && a.tile0[a.ndest] != 0) note_launch();
+  return err;
+}
+cudaError_t launch_a2a(const A2APlain& a, bool shift, cudaStream_t s) {
+  cudaError_t err = launch_params(a, shift, s);
+  if (err == cudaSuccess && a.tile0[a.ndest] != 0) note_launch();
+  return err;
+}
+cudaError_t launch_a2a(const A2ATable32& a, bool shift, cudaStream_t s) {
+  cudaError_t err = launch_params(a, shift, s);
+  if (err == cudaSuccess && a.tile0[a.ndest] != 0) note_launch();
+  return err;
+}
+cudaError_t launch_a2a(const A2ATable64& a, bool shift, cudaStream_t s) {
+  cudaError_t err = launch_params(a, shift, s);
+  if (err == cudaSuccess && a.tile0[a.ndest] != 0) note_launch();
   return err;
 }
 

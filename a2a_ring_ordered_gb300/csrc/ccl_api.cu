@@ -39,6 +39,34 @@ int current_sm_count() {
   return sms;
 }
 
+int first_wave_ctas(const void* kernel) {
+  struct Entry {
+    const void* kernel;
+    int dev, ctas;
+  };
+  constexpr int kEntries = 64;
+  static thread_local Entry cache[kEntries];
+  static thread_local int used = 0, next = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  for (int i = 0; i < used; ++i)
+    if (cache[i].kernel == kernel && cache[i].dev == dev) return cache[i].ctas;
+  int per_sm = 0;
+  // every kernel launched through launch_kernel runs 256 threads per CTA
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess) {
+    (void)cudaGetLastError();  // not sticky; prefetch is then simply off
+    per_sm = 0;
+  }
+  const Entry e{kernel, dev, per_sm * current_sm_count()};
+  if (used < kEntries) {
+    cache[used++] = e;
+  } else {
+    cache[next] = e;
+    next = (next + 1) % kEntries;
+  }
+  return e.ctas;
+}
+
 namespace {
 
 thread_local char t_error[512];
@@ -918,6 +946,101 @@ extern "C" ccl_status_t ccl_all_to_all_heads(const void* const* send, void* cons
 }
 
 // ============================================================== all-to-allv
+namespace {
+
+// Destination tiles of one launch: tile0[c] = tiles before destination
+// j0 + c; returns the launch's total.
+template <class P>
+uint64_t fill_tiles(P& a, void* const* recv, const uint64_t* out_bytes) {
+  uint64_t total = 0;
+  for (int c = 0; c < a.ndest; ++c) {
+    a.tile0[c] = total;
+    total += a2a_tiles_for(static_cast<const char*>(recv[a.j0 + c]), out_bytes[a.j0 + c]);
+  }
+  a.tile0[a.ndest] = total;
+  return total;
+}
+
+template <class P>
+void fill_pointers(P& a, const void* const* send, void* const* recv, int p) {
+  for (int r = 0; r < p; ++r) {
+    a.send[r] = static_cast<const char*>(send[r]);
+    a.recv[r] = static_cast<char*>(recv[r]);
+  }
+}
+
+// The all-to-allv through row-prefix tables, as many destinations per launch
+// as the parameter block holds (all of them for p <= 85).
+template <class P>
+ccl_status_t a2a_table_launches(P& a, const void* const* send, void* const* recv, const size_t* counts,
+                                int p, uint64_t row_bytes, size_t e, const uint64_t* out_bytes,
+                                bool shift, cudaStream_t s) {
+  const int per_launch = P::kTableCap / p - 1;
+  for (int j0 = 0; j0 < p; j0 += per_launch) {
+    memset(static_cast<void*>(&a), 0, sizeof(a));
+    fill_pointers(a, send, recv, p);
+    a.p = p;
+    a.j0 = j0;
+    a.ndest = (p - j0 < per_launch) ? p - j0 : per_launch;
+    a.plain = 0;
+    a.row_bytes = row_bytes;
+    a.elem = static_cast<int>(e);
+    const int stride = a.ndest + 1;
+    for (int i = 0; i < p; ++i) {
+      uint64_t rows = 0;
+      for (int d = 0; d < j0; ++d) rows += counts[static_cast<size_t>(i) * p + d];
+      for (int c = 0; c <= a.ndest; ++c) {
+        a.table[i * stride + c] = static_cast<typename P::Entry>(rows);
+        if (j0 + c < p) rows += counts[static_cast<size_t>(i) * p + j0 + c];
+      }
+    }
+    if (fill_tiles(a, recv, out_bytes) == 0) continue;
+    cudaError_t err = launch_a2a(a, shift, s);
+    if (err != cudaSuccess) return cuda_fail(err, "all-to-all kernel launch");
+  }
+  return CCL_OK;
+}
+
+ccl_status_t a2a_table(const void* const* send, const size_t* counts, void* const* recv, int p,
+                       uint64_t row_bytes, size_t e, const uint64_t* in_rows, cudaStream_t s) {
+  uint64_t out_bytes[CCL_MAX_RANKS] = {0};
+  uint64_t max_rows = 0;
+  for (int i = 0; i < p; ++i) {
+    max_rows = in_rows[i] > max_rows ? in_rows[i] : max_rows;
+    for (int d = 0; d < p; ++d) out_bytes[d] += counts[static_cast<size_t>(i) * p + d] * row_bytes;
+  }
+  // some block's source and destination differ in 16-byte phase
+  bool shift = false;
+  uint64_t col[CCL_MAX_RANKS] = {0};  // rows of destination d before source i's block
+  for (int i = 0; i < p && !shift; ++i) {
+    uint64_t row = 0;
+    for (int d = 0; d < p; ++d) {
+      const uint64_t c = counts[static_cast<size_t>(i) * p + d];
+      if (c != 0) {
+        const uintptr_t src = reinterpret_cast<uintptr_t>(send[i]) + row * row_bytes;
+        const uintptr_t dst = reinterpret_cast<uintptr_t>(recv[d]) + col[d] * row_bytes;
+        shift = shift || ((src - dst) & 15) != 0;
+      }
+      row += c;
+      col[d] += c;
+    }
+  }
+  // uint32 table entries hold every row prefix only while each source has
+  // fewer than 2^32 rows
+  if (max_rows >= (1ull << 32)) {
+    static thread_local A2ATable64 a;  // 32 KB: kept off the stack
+    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, s);
+  }
+  if (p <= A2ASmall::kCap) {
+    static thread_local A2ASmall a;
+    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, s);
+  }
+  static thread_local A2ATable32 a;
+  return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, s);
+}
+
+}  // namespace
+
 extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts,
                                         void* const* recv, int p, size_t row_elems,
                                         ccl_dtype_t dt, void* stream) {
@@ -955,34 +1078,7 @@ extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* c
   if ((st = check_aliasing(in, out, nullptr, p)) != CCL_OK) return st;
   if (row_bytes == 0) return CCL_OK;
 
-  // exclusive prefix sums: source s's block for d, destination d's block from s
-  uint64_t recv_row[CCL_MAX_RANKS] = {0};  // next free row of each destination
-  static thread_local A2AArgs a;             // 32 KB: kept off the stack
-  memset(&a, 0, sizeof(a));
-  for (int s = 0; s < p; ++s) {
-    uint64_t send_row = 0;
-    for (int d = 0; d < p; ++d) {
-      const uint64_t rows = counts[s * p + d];
-      if (rows != 0) {
-        A2ADesc& desc = a.d[a.ndesc];
-        desc.src = static_cast<const char*>(send[s]) + send_row * row_bytes;
-        desc.dst = static_cast<char*>(recv[d]) + recv_row[d] * row_bytes;
-        desc.bytes = rows * row_bytes;
-        desc.tile0 = a.total_tiles;
-        a.total_tiles += a2a_tiles_for(desc.dst, desc.bytes);
-        if (++a.ndesc == kA2AMaxDesc) {
-          cudaError_t err = launch_a2av(a, as_stream(stream));
-          if (err != cudaSuccess) return cuda_fail(err, "all-to-allv kernel launch");
-          memset(&a, 0, sizeof(a));
-        }
-      }
-      send_row += rows;
-      recv_row[d] += rows;
-    }
-  }
-  cudaError_t err = launch_a2av(a, as_stream(stream));
-  if (err != cudaSuccess) return cuda_fail(err, "all-to-allv kernel launch");
-  return CCL_OK;
+  return a2a_table(send, counts, recv, p, row_bytes, e, in_rows, as_stream(stream));
 }
 
 extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* recv, int p, size_t n,
@@ -991,16 +1087,56 @@ extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* rec
   clear_error();
   ccl_status_t st = check_p(p);
   if (st != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (send == nullptr || recv == nullptr) return fail(CCL_ERR_INVALID_ARG, "send or recv is NULL");
   if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
-  // block d of every source is chunk d (the chunk rule): counts[s][d] = len(d)
-  // elements, so destination d receives p blocks of len(d) in source order
-  static thread_local size_t counts[CCL_MAX_RANKS * CCL_MAX_RANKS];
-  for (int d = 0; d < p; ++d) {
-    uint64_t off, len;
-    chunk(p, n, d, &off, &len);
-    for (int src = 0; src < p; ++src) counts[static_cast<size_t>(src) * p + d] = len;
+  // block d of every source is chunk d (the chunk rule): destination d
+  // receives p blocks of len(d) elements in source order
+  uint64_t in_bytes[CCL_MAX_RANKS], out_bytes[CCL_MAX_RANKS], off[CCL_MAX_RANKS], len[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    chunk(p, n, r, &off[r], &len[r]);
+    in_bytes[r] = n * e;
+    out_bytes[r] = static_cast<uint64_t>(p) * len[r] * e;
+    in[r] = span(send[r], in_bytes[r]);
+    out[r] = span(recv[r], out_bytes[r]);
   }
-  return ccl_all_to_allv(send, counts, recv, p, 1, dt, stream);
+  if ((st = check_buffers("send", send, p, in_bytes, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", const_cast<const void* const*>(recv), p, out_bytes, e)) != CCL_OK) return st;
+  if ((st = check_aliasing(in, out, nullptr, p)) != CCL_OK) return st;
+  if (n == 0) return CCL_OK;
+  bool shift = false;  // some block's source and destination differ in 16-byte phase
+  for (int d = 0; d < p && !shift; ++d) {
+    if (len[d] == 0) continue;
+    for (int i = 0; i < p && !shift; ++i) {
+      const uintptr_t src = reinterpret_cast<uintptr_t>(send[i]) + off[d] * e;
+      const uintptr_t dst = reinterpret_cast<uintptr_t>(recv[d]) + static_cast<uint64_t>(i) * len[d] * e;
+      shift = ((src - dst) & 15) != 0;
+    }
+  }
+  auto fill = [&](auto& a) -> ccl_status_t {
+    memset(static_cast<void*>(&a), 0, sizeof(a));
+    fill_pointers(a, send, recv, p);
+    a.p = p;
+    a.j0 = 0;
+    a.ndest = p;
+    a.plain = 1;
+    a.row_bytes = e;
+    a.elem = static_cast<int>(e);
+    a.q = n / static_cast<uint64_t>(p);
+    a.rem = n % static_cast<uint64_t>(p);
+    if (fill_tiles(a, recv, out_bytes) == 0) return CCL_OK;
+    cudaError_t err = launch_a2a(a, shift, as_stream(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "all-to-all kernel launch");
+    return CCL_OK;
+  };
+  if (p <= A2ASmall::kCap) {
+    A2ASmall a;
+    return fill(a);
+  }
+  A2APlain a;
+  return fill(a);
 }
 
 // ====================================================== literal ring engine

@@ -20,6 +20,9 @@ enum FoldMode : int {
   kModeReduce = 3          // fold, write the result only to recv[0] (the root's buffer)
 };
 
+// pf_ctas (set by launch_kernel): CTAs of the launch's first wave, the ones
+// that prefetch their first inputs into L2 before waiting on the previous
+// grid (0: none).
 struct FoldArgs {
   const void* send[CCL_MAX_RANKS];
   void* recv[CCL_MAX_RANKS];
@@ -27,6 +30,7 @@ struct FoldArgs {
   uint64_t rem;  // n mod p
   int p;
   float scale;   // bucket mode only
+  uint32_t pf_ctas;
 };
 
 // `vec`: every pointer is 16-byte aligned, so 16-byte vectors may be used.
@@ -57,6 +61,7 @@ struct GatherArgs {
   void* recv[CCL_MAX_RANKS];        // full n-element outputs
   uint64_t q, rem;
   int p;
+  uint32_t pf_ctas;                 // as in FoldArgs
 };
 cudaError_t launch_gather(int dt, bool vec, const GatherArgs& a, cudaStream_t s);
 // Fan-out through bulk copies: chunk c (chunk_bytes from send[c], or from
@@ -78,33 +83,49 @@ cudaError_t launch_bounded_wait_probe(cudaStream_t s);
 cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, cudaStream_t s);
 
 // ------------------------------------------------------------- all-to-allv
-// One contiguous byte block src -> dst.  Blocks are cut into tiles of
-// kA2ATileBytes measured from dst rounded down to 16 bytes; tile0 is the
-// index of the block's first tile in the launch.
-struct A2ADesc {
-  const char* src;
-  char* dst;
-  uint64_t bytes;
-  uint64_t tile0;
-};
-// Descriptors per launch: up to 112 travel in a parameter block under the
-// classic 4 KB limit; a call with more blocks (p > 10) uses the 32 KB
-// parameter space of CUDA 12.1+ drivers (1016 descriptors), so even p = 128
-// (16,384 blocks) takes 17 launches instead of 147.
-constexpr int kA2ASmallDesc = 112;
-constexpr int kA2AMaxDesc = 1016;  // 1016 * 32 B + header < 32,764 bytes
+// Destination j's buffer holds one block per source i in source order; work
+// is cut into kA2ATileBytes tiles of destination space (boundaries on 512
+// bytes of the destination's address), tile0[c] = first tile of destination
+// j0 + c in this launch, tile0[ndest] = the launch's tiles.
+//  plain = 1: the all-to-all of the chunk rule, one element per row:
+//    block i of destination j has len(j) rows and starts at row off(j) of
+//    send[i] (n = q * p + rem elements per rank).
+//  plain = 0: table[i * (ndest + 1) + c] = rows of send[i] before its block
+//    for destination j0 + c (c = 0..ndest; c = ndest gives the next
+//    destination's start, or source i's total rows when j0 + ndest = p).
 constexpr uint64_t kA2ATileBytes = 32768;
-template <int CAP>
-struct A2AArgsT {
-  uint64_t total_tiles;
-  int ndesc;
-  A2ADesc d[CAP];
+template <int CAP, int TCAP, typename TT>
+struct A2AParamsT {
+  static constexpr int kCap = CAP;
+  static constexpr int kTableCap = TCAP;
+  using Entry = TT;
+  const char* send[CAP];
+  char* recv[CAP];
+  uint64_t tile0[CAP + 1];
+  uint64_t row_bytes;  // bytes per row (a multiple of elem)
+  uint64_t q, rem;     // plain: the chunk rule of n
+  int p, j0, ndest, plain;
+  int elem;            // element bytes (2 or 4)
+  TT table[TCAP];
 };
-using A2AArgs = A2AArgsT<kA2AMaxDesc>;
-static_assert(sizeof(A2AArgsT<kA2ASmallDesc>) <= 4096, "all-to-allv parameters exceed 4 KB");
-static_assert(sizeof(A2AArgs) <= 32764, "all-to-allv parameters exceed 32,764 bytes");
+// p <= 16, any geometry (a table of 16 x 17 entries): under the classic 4 KB
+using A2ASmall = A2AParamsT<16, 16 * 17, uint32_t>;
+// plain all-to-all, any p
+using A2APlain = A2AParamsT<128, 1, uint32_t>;
+// tables in the 32 KB parameter space of CUDA 12.1+ drivers: p * (ndest + 1)
+// entries per launch (uint32 while every row prefix fits in 32 bits)
+using A2ATable32 = A2AParamsT<128, 7408, uint32_t>;
+using A2ATable64 = A2AParamsT<128, 3704, uint64_t>;
+static_assert(sizeof(A2ASmall) <= 4096, "all-to-allv parameters exceed 4 KB");
+static_assert(sizeof(A2APlain) <= 4096, "all-to-all parameters exceed 4 KB");
+static_assert(sizeof(A2ATable32) <= 32764, "all-to-allv parameters exceed 32,764 bytes");
+static_assert(sizeof(A2ATable64) <= 32764, "all-to-allv parameters exceed 32,764 bytes");
 uint64_t a2a_tiles_for(const char* dst, uint64_t bytes);
-cudaError_t launch_a2av(const A2AArgs& a, cudaStream_t s);
+// shift: some block's source and destination differ in 16-byte phase
+cudaError_t launch_a2a(const A2ASmall& a, bool shift, cudaStream_t s);
+cudaError_t launch_a2a(const A2APlain& a, bool shift, cudaStream_t s);
+cudaError_t launch_a2a(const A2ATable32& a, bool shift, cudaStream_t s);
+cudaError_t launch_a2a(const A2ATable64& a, bool shift, cudaStream_t s);
 
 // ------------------------------------------------- literal ring engine steps
 // One launch moves p independent transfers, transfer r: src[r] -> dst[r],
@@ -183,5 +204,10 @@ void note_launch();
 
 // Streaming multiprocessors of the current device (0 if unknown).
 int current_sm_count();
+
+// CTAs of `kernel` (kThreads threads each) resident on the current device at
+// once -- a launch's first wave -- cached per host thread, kernel and device
+// (0 if unknown).
+int first_wave_ctas(const void* kernel);
 
 }  // namespace ccl

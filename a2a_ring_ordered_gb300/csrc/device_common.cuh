@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <type_traits>
+#include <utility>
 
 #include "ccl_internal.h"
 
@@ -184,6 +185,40 @@ __device__ __forceinline__ void store_one(void* base, uint64_t i, const uint32_t
   }
 }
 
+// ------------------------------------------------------- early L2 prefetch
+// A kernel may prefetch its first inputs into L2 before pdl_enter(): while
+// the previous grid in the stream drains, the lines are already on their way,
+// which hides the first loads' DRAM latency of back-to-back calls.  This is
+// only a hint: a prefetch returns no data, and L2 is the device's point of
+// coherence, so a line the previous grid writes afterwards is updated in L2
+// and the loads after pdl_enter() see the written value (they bypass or miss
+// L1, which the prefetch does not fill).  Prefetched lines hold at least one
+// byte of a buffer the kernel reads, so they lie in mapped pages.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// The byte spans [base[r] + off, base[r] + off + len), r < nspans, prefetched
+// into L2 by the CTA's threads together, one prefetch per 128-byte line, at
+// most kPrefetchCtaBytes in all (the spans cut short evenly).
+constexpr uint64_t kPrefetchCtaBytes = 65536;
+__device__ __forceinline__ void prefetch_spans_l2(const void* const* base, int nspans, uint64_t off,
+                                                  uint64_t len) {
+  if (len == 0) return;
+  {
+    const uint64_t cap = kPrefetchCtaBytes / static_cast<uint64_t>(nspans);
+    len = len < cap ? len : (cap > 128 ? cap : 128);
+  }
+  const uint64_t lines = (len + 127) / 128 + 1;  // lines a span of len bytes can touch
+  const uint64_t total = lines * static_cast<uint64_t>(nspans);
+  for (uint64_t k = threadIdx.x; k < total; k += blockDim.x) {
+    const uint64_t r = k / lines, l = k - r * lines;
+    const uintptr_t first = reinterpret_cast<uintptr_t>(base[r]) + off;
+    const uintptr_t line = (first & ~static_cast<uintptr_t>(127)) + 128 * l;
+    if (line < first + len) prefetch_l2(reinterpret_cast<const void*>(line));
+  }
+}
+
 // ------------------------------------------- programmatic dependent launch
 // Kernels are launched with programmatic stream serialisation, so a kernel
 // may be scheduled while the previous kernel in the stream is still draining.
@@ -201,9 +236,23 @@ __device__ __forceinline__ void pdl_enter() {
 #endif
 }
 
+template <typename T, typename = void>
+struct HasPfCtas : std::false_type {};
+template <typename T>
+struct HasPfCtas<T, std::void_t<decltype(std::declval<T&>().pf_ctas)>> : std::true_type {};
+
+// The CTA's place in launch order (x fastest, then y).
+__device__ __forceinline__ uint64_t cta_rank() {
+  return static_cast<uint64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+}
+
 template <typename Args>
 cudaError_t launch_kernel(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t s,
-                          const Args& args) {
+                          const Args& args_in) {
+  // arguments with a pf_ctas field get the kernel's first wave there
+  Args args = args_in;
+  if constexpr (HasPfCtas<Args>::value)
+    args.pf_ctas = static_cast<uint32_t>(first_wave_ctas(reinterpret_cast<const void*>(kernel)));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;

@@ -97,7 +97,6 @@ __device__ __forceinline__ void emit(const FoldArgs& a, int p, int c, const Chun
 template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE, bool REALIGN>
 __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ FoldArgs a) {
   using Acc = typename Elem<DT_IN>::Acc;
-  pdl_enter();
   const int p = a.p;
   const int c = blockIdx.y;
   const Chunk ch = chunk_of(c, a.q, a.rem);
@@ -105,6 +104,16 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ 
   const uint64_t v_lo = (ch.off + VEC - 1) / VEC;  // first whole vector inside chunk c
   const uint64_t v_hi = end / VEC;                 // one past the last
   const int first = (c + 1 == p) ? 0 : c + 1;      // the rank that starts chunk c
+  if (VEC > 1 && cta_rank() < a.pf_ctas) {  // this CTA's first vectors of every rank, before waiting on the previous grid
+    uint64_t b0 = ((MODE == kModeReduceScatter) ? v_lo : (v_lo & ~static_cast<uint64_t>(31))) +
+                  static_cast<uint64_t>(blockIdx.x) * kThreads;
+    uint64_t e0 = b0 + kThreads;
+    b0 = b0 > v_lo ? b0 : v_lo;
+    e0 = e0 < v_hi ? e0 : v_hi;
+    if (b0 < e0)
+      prefetch_spans_l2(a.send, p, b0 * VEC * Elem<DT_IN>::kBytes, (e0 - b0) * VEC * Elem<DT_IN>::kBytes);
+  }
+  pdl_enter();
 
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   if (MODE == kModeReduceScatter && REALIGN && VEC > 1 && (ch.off % VEC) != 0) {
@@ -203,7 +212,6 @@ __device__ __forceinline__ void fold_vectors(const FoldArgs& a, int p, int first
 template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE, int BATCH, int U>
 __global__ void __launch_bounds__(kThreads) fold_unrolled_kernel(const __grid_constant__ FoldArgs a) {
   using Acc = typename Elem<DT_IN>::Acc;
-  pdl_enter();
   const int p = a.p;
   const int c = blockIdx.y;
   const Chunk ch = chunk_of(c, a.q, a.rem);
@@ -216,6 +224,15 @@ __global__ void __launch_bounds__(kThreads) fold_unrolled_kernel(const __grid_co
   // in fold_kernel); lanes before v_lo stay idle
   const uint64_t v_start = v_lo & ~static_cast<uint64_t>(31);
   constexpr uint64_t kSpan = static_cast<uint64_t>(kThreads) * U;
+  if (cta_rank() < a.pf_ctas) {  // this CTA's first kSpan vectors of every rank, before waiting on the previous grid
+    uint64_t b0 = v_start + static_cast<uint64_t>(blockIdx.x) * kSpan;
+    uint64_t e0 = b0 + kSpan;
+    b0 = b0 > v_lo ? b0 : v_lo;
+    e0 = e0 < v_hi ? e0 : v_hi;
+    if (b0 < e0)
+      prefetch_spans_l2(a.send, p, b0 * VEC * Elem<DT_IN>::kBytes, (e0 - b0) * VEC * Elem<DT_IN>::kBytes);
+  }
+  pdl_enter();
   for (uint64_t base = v_start + static_cast<uint64_t>(blockIdx.x) * kSpan; base < v_hi;
        base += static_cast<uint64_t>(gridDim.x) * kSpan) {
     Acc acc[U][VEC];

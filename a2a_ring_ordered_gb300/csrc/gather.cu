@@ -36,7 +36,6 @@ __device__ __forceinline__ void load_elems(const void* base, uint64_t i, uint32_
 template <int DT, int VEC, int U, bool REALIGN>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherArgs a) {
   constexpr int W = (VEC * Elem<DT>::kBytes + 3) / 4;
-  pdl_enter();
   const int p = a.p;
   const int k = blockIdx.y;
   const Chunk ch = chunk_of(k, a.q, a.rem);
@@ -44,6 +43,18 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
   const uint64_t v_lo = (ch.off + VEC - 1) / VEC;
   const uint64_t v_hi = end / VEC;
   const void* src = a.send[k];
+  if (VEC > 1 && cta_rank() < a.pf_ctas) {  // this CTA's first source bytes, before waiting on the previous grid
+    constexpr uint64_t kSpan0 = static_cast<uint64_t>(kThreads) * U;
+    uint64_t b0 = (REALIGN ? (v_lo & ~static_cast<uint64_t>(31)) : v_lo) + static_cast<uint64_t>(blockIdx.x) * kSpan0;
+    uint64_t e0 = b0 + kSpan0;
+    b0 = b0 > v_lo ? b0 : v_lo;
+    e0 = e0 < v_hi ? e0 : v_hi;
+    if (b0 < e0) {
+      constexpr uint64_t B = Elem<DT>::kBytes;
+      prefetch_spans_l2(&src, 1, (b0 * VEC - ch.off) * B, (e0 - b0) * VEC * B);
+    }
+  }
+  pdl_enter();
   const bool src_aligned = (ch.off % VEC) == 0;
   // Block k unaligned in the outputs (off(k) not a multiple of VEC): output
   // vector v takes the source bytes [((v - q) * VEC - s) * B, + 16), i.e.

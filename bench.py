@@ -1376,7 +1376,172 @@ def run_ours(a, wl: Workload, rank: int, world: int, local: int) -> dict | None:
         out["overlap"] = wl.overlap_report()
     if world == 1 and not a.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl)
+    if world == 1 and a.workload == "bucket" and not a.no_configs:
+        t_cfg = time.time()
+        out["configs"] = config_records(lib, torch, device, peak)
+        out["configs"]["wall_s"] = round(time.time() - t_cfg, 1)
     return out
+
+
+# ----------------------------------------------- points and their oracle check
+def _bits(t) -> np.ndarray:
+    """A device tensor on the host as numpy (bf16 as its uint16 bits)."""
+    import torch
+    h = t.detach().cpu()
+    return h.view(torch.int16).numpy().view(np.uint16) if h.dtype == torch.bfloat16 else h.numpy()
+
+
+def _sample_positions(n: int, count: int, seed: int, edges=()) -> np.ndarray:
+    """count random positions in [0, n) plus the given edge positions and both ends."""
+    rng = np.random.default_rng(seed)
+    idx = [rng.integers(0, n, size=min(count, n)), np.array([0, n - 1]), np.asarray(list(edges), np.int64)]
+    idx = np.unique(np.concatenate(idx).astype(np.int64))
+    return idx[(idx >= 0) & (idx < n)]
+
+
+def _chunk_edges(lib, p: int, n: int) -> list[int]:
+    out = []
+    for k in range(p):
+        off, ln = lib.ccl_chunk_bounds(p, n, k)
+        out += [off - 1, off, off + ln - 1, off + ln]
+    return out
+
+
+def _mismatches(got: np.ndarray, want: np.ndarray) -> int:
+    """Elements whose bits differ (NaN payloads and signed zeros included)."""
+    g, w = np.ascontiguousarray(got), np.ascontiguousarray(want)
+    if g.dtype.itemsize != w.dtype.itemsize or g.size != w.size:
+        return max(g.size, w.size)
+    return int((g.view(np.uint8).reshape(g.size, -1) != w.view(np.uint8).reshape(w.size, -1)).any(axis=1).sum())
+
+
+def _gather_from(snd, src: np.ndarray, pos: np.ndarray, dev) -> np.ndarray:
+    """Elements snd[src[i]][pos[i]] on the host."""
+    import torch
+    out = None
+    for s_ in np.unique(src):
+        sel = src == s_
+        v = _bits(snd[int(s_)][torch.from_numpy(pos[sel]).to(dev)])
+        if out is None:
+            out = np.empty(src.size, dtype=v.dtype)
+        out[sel] = v
+    return out
+
+
+def oracle_check_leg(lib, kind: str, dt: str, p: int, n: int, snd, rcv, count: int = 4096, seed: int = 0) -> dict:
+    """The CPU-baseline leg's parity check of a measured point (after its timed
+    region): the oracle's per-element forms, on the host, at a bounded sample
+    of positions -- random ones plus every chunk edge and both ends -- timed,
+    and compared bit for bit with the kernel's output there.  all-reduce /
+    reduce-scatter: the ring fold ("Networks and Collective Communication"
+    section 5.1); all-gather and all-to-all: the placement of section 4.1."""
+    import torch
+    from oracle import pointwise
+    dev = snd[0].device
+    mism, nsamp = 0, 0
+    t0 = time.perf_counter()
+    ranks = sorted({0, p // 2, p - 1})
+    if kind in ("allreduce", "reduce_scatter", "all_gather"):
+        idx = _sample_positions(n, count, seed, _chunk_edges(lib, p, n))
+        it = torch.from_numpy(idx).to(dev)
+        k, pos = pointwise.all_gather_source(p, n, idx)  # chunk of each position
+        nsamp = idx.size
+        if kind == "all_gather":
+            want = _gather_from(snd, k, pos, dev)
+        else:
+            want = pointwise.allreduce_at_columns([_bits(x[it]) for x in snd], idx, n, dt)
+        if kind == "reduce_scatter":  # position off(k) + t is element t of rank k's shard
+            mism += _mismatches(_gather_from(rcv, k, pos, dev), want)
+        else:
+            for r in ranks:
+                mism += _mismatches(_bits(rcv[r][it]), want)
+    elif kind == "all_to_all":
+        for j in ranks:
+            m = rcv[j].numel()
+            if m == 0:
+                continue
+            ln = m // p
+            edges = [i * ln + d for i in range(p) for d in (-1, 0, ln - 1)]
+            idx = _sample_positions(m, count, seed + j, edges)
+            src, spos = pointwise.all_to_all_source(p, n, j, idx)
+            mism += _mismatches(_bits(rcv[j][torch.from_numpy(idx).to(dev)]), _gather_from(snd, src, spos, dev))
+            nsamp += idx.size
+    else:
+        raise ValueError(kind)
+    return {"checked": mism == 0, "samples": int(nsamp), "mismatches": int(mism),
+            "oracle_s": round(time.perf_counter() - t0, 3),
+            "how": f"oracle.pointwise at random positions plus every chunk edge; output ranks {ranks}"}
+
+
+def _collective(lib, kind):
+    return {"allreduce": lib.ccl_allreduce, "reduce_scatter": lib.ccl_reduce_scatter,
+            "all_gather": lib.ccl_all_gather, "all_to_all": lib.ccl_all_to_all}[kind]
+
+
+def measure_point(lib, torch, device, stream, kind: str, dt: str, p: int, n: int, gen, peak: float,
+                  init=None, max_calls: int = 4000, target_us: float = 20000.0):
+    """Time one collective call of p ranks x n elements: K calls captured in a
+    CUDA graph and replayed under CUDA events on ``stream``, rotating over
+    enough buffer sets that the rotated footprint is at least twice the L2
+    (where memory allows), every rank buffer on a 256-byte boundary.  Returns
+    (record, views of the buffer sets).  ``init(j, inputs)`` may overwrite the
+    inputs of set j (the default is U(-1, 1) from ``gen``)."""
+    e = 4 if dt == "f32" else 2
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    lens = [lib.ccl_chunk_bounds(p, n, k)[1] for k in range(p)]
+    in_sizes = lens if kind == "all_gather" else [n] * p
+    out_sizes = (lens if kind == "reduce_scatter" else
+                 [p * ln for ln in lens] if kind == "all_to_all" else [n] * p)
+    pad = 256 // e
+    rnd = lambda m: -(-m // pad) * pad
+    n_in, n_out = sum(rnd(m) for m in in_sizes), sum(rnd(m) for m in out_sizes)
+    foot = (sum(in_sizes) + sum(out_sizes)) * e  # the primitive's minimum bytes
+    sets = int(min(64, max(1, -(-2 * L2_BYTES // foot))))
+    arena_in = (torch.rand(sets * n_in, generator=gen, device=device) * 2 - 1).to(tdt)
+    arena_out = torch.empty(sets * n_out, dtype=tdt, device=device)
+
+    def split(t, sizes):
+        out, off = [], 0
+        for m in sizes:
+            out.append(t[off:off + m])
+            off += rnd(m)
+        return out
+
+    views = [(split(arena_in[j * n_in:(j + 1) * n_in], in_sizes),
+              split(arena_out[j * n_out:(j + 1) * n_out], out_sizes)) for j in range(sets)]
+    if init is not None:
+        for j in range(sets):
+            init(j, views[j][0])
+    call = _collective(lib, kind)
+    est_us = max(2.0, foot / (peak * 1e3))
+    k = int(min(max_calls, max(2 * sets, target_us / est_us)))
+    with torch.cuda.stream(stream):
+        for j in range(min(sets, 3)):  # warm-up outside capture
+            call(views[j][0], views[j][1], stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(k):
+            snd, rcv = views[i % sets]
+            call(snd, rcv, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / (reps * k)
+    del g
+    # the last replay left every set's outputs computed from its own inputs
+    gbs = foot / (ms * 1e-3) / 1e9
+    rec = {"collective": kind, "dtype": dt, "p": p, "n_per_rank": n, "bytes_per_rank": n * e,
+           "us_per_call": round(ms * 1e3, 3), "effective_gbs": round(gbs, 1),
+           "frac_of_hbm": round(gbs / peak, 4), "algorithmic_bytes_per_call": foot,
+           "buffer_sets": sets, "calls_per_graph": k}
+    return rec, views
 
 
 def run_sweep(a) -> int:
@@ -1388,10 +1553,10 @@ def run_sweep(a) -> int:
     all-gather n in and p*n out (the primitive's minimum bytes).  Per point,
     K calls are captured in a CUDA graph (small messages are launch-bound, and
     host-side call overhead would otherwise leave the GPU idle between
-    kernels) and the graph is replayed under CUDA events on the replay stream.
-    The calls rotate over enough buffer sets that the rotated footprint is at
-    least twice the L2 where memory allows, so mid-size messages are not
-    served from L2 left by the previous call.
+    kernels) and the graph is replayed under CUDA events on the replay stream
+    (``measure_point``).  After the timed region the CPU-baseline leg checks
+    the point's output against the oracle at sampled positions
+    (``oracle_check_leg``); the line carries ``checked``.
     """
     import torch
     from a2a_ring_ordered_gb300 import ccl as lib
@@ -1405,74 +1570,188 @@ def run_sweep(a) -> int:
     gen = torch.Generator(device=device)
     gen.manual_seed(4)
     s = torch.cuda.Stream(device)
-    call = {"allreduce": lib.ccl_allreduce, "reduce_scatter": lib.ccl_reduce_scatter,
-            "all_gather": lib.ccl_all_gather, "all_to_all": lib.ccl_all_to_all}[kind]
     for dt in dtypes:
         e = 4 if dt == "f32" else 2
-        tdt = torch.float32 if dt == "f32" else torch.bfloat16
         for p in ps:
             top = 28 if p == 72 else 30  # p=72 up to 256 MiB per rank, else 1 GiB
-            for lg in range(max(10, a.sweep_lo), min(top, a.sweep_hi) + 1, a.sweep_stride):
+            lgs = ([int(x) for x in a.sweep_sizes.split(",")] if a.sweep_sizes else
+                   range(max(10, a.sweep_lo), min(top, a.sweep_hi) + 1, a.sweep_stride))
+            for lg in lgs:
+                if lg > top:
+                    continue
                 nbytes_rank = 1 << lg
                 n = nbytes_rank // e
-                lens = [lib.ccl_chunk_bounds(p, n, k)[1] for k in range(p)]
-                in_sizes = lens if kind == "all_gather" else [n] * p
-                out_sizes = (lens if kind == "reduce_scatter" else
-                             [p * ln for ln in lens] if kind == "all_to_all" else [n] * p)
-                # every rank buffer starts on a 256-byte boundary of its arena,
-                # as separately allocated buffers would
-                pad = 256 // e
-                rnd = lambda m: -(-m // pad) * pad
-                n_in, n_out = sum(rnd(m) for m in in_sizes), sum(rnd(m) for m in out_sizes)
-                foot = (sum(in_sizes) + sum(out_sizes)) * e  # the primitive's minimum bytes
-                sets = int(min(64, max(1, -(-2 * L2_BYTES // foot))))
-                arena_in = (torch.rand(sets * n_in, generator=gen, device=device) * 2 - 1).to(tdt)
-                arena_out = torch.empty(sets * n_out, dtype=tdt, device=device)
-
-                def split(t, sizes):
-                    out, off = [], 0
-                    for m in sizes:
-                        out.append(t[off:off + m])
-                        off += rnd(m)
-                    return out
-
-                views = [(split(arena_in[j * n_in:(j + 1) * n_in], in_sizes),
-                          split(arena_out[j * n_out:(j + 1) * n_out], out_sizes)) for j in range(sets)]
-                est_us = max(2.0, foot / (peak * 1e3))
-                k = int(min(4000, max(2 * sets, 20000.0 / est_us)))
-                with torch.cuda.stream(s):
-                    for j in range(min(sets, 3)):  # warm-up outside capture
-                        call(views[j][0], views[j][1], stream=s)
-                s.synchronize()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=s):
-                    for i in range(k):
-                        snd, rcv = views[i % sets]
-                        call(snd, rcv, stream=s)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                reps = 3
-                with torch.cuda.stream(s):  # replay() launches on the current stream
-                    g.replay()
-                    e0.record(s)
-                    for _ in range(reps):
-                        g.replay()
-                    e1.record(s)
-                torch.cuda.synchronize(device)
-                ms = e0.elapsed_time(e1) / (reps * k)
-                algo = foot
-                gbs = algo / (ms * 1e-3) / 1e9
+                rec, views = measure_point(lib, torch, device, s, kind, dt, p, n, gen, peak)
+                chk = oracle_check_leg(lib, kind, dt, p, n, views[0][0], views[0][1], seed=lg)
+                ms = rec["us_per_call"] * 1e-3
                 bus = {"allreduce": 2 * (p - 1) / p}.get(kind, (p - 1) / p)
                 print(json.dumps({
                     "sweep": kind, "dtype": dt, "p": p, "bytes_per_rank": nbytes_rank,
-                    "us_per_call": round(ms * 1e3, 3), "effective_gbs": round(gbs, 1),
-                    "frac_of_hbm": round(gbs / peak, 4), "peak": peak, "peak_source": peak_src,
+                    "us_per_call": rec["us_per_call"], "effective_gbs": rec["effective_gbs"],
+                    "frac_of_hbm": rec["frac_of_hbm"], "peak": peak, "peak_source": peak_src,
                     "algbw_gbs": round(nbytes_rank / (ms * 1e-3) / 1e9, 2),
                     "busbw_gbs": round(nbytes_rank / (ms * 1e-3) / 1e9 * bus, 2),
-                    "buffer_sets": sets, "rotated_footprint_mb": round(sets * foot / 1e6, 1),
-                    "calls_per_graph": k}), flush=True)
-                del g, views, arena_in, arena_out
+                    "buffer_sets": rec["buffer_sets"],
+                    "rotated_footprint_mb": round(rec["buffer_sets"] * rec["algorithmic_bytes_per_call"] / 1e6, 1),
+                    "calls_per_graph": rec["calls_per_graph"], "checked": chk["checked"],
+                    "oracle_check": chk}), flush=True)
+                del views
                 torch.cuda.empty_cache()
     return 0
+
+
+def config_records(lib, torch, device, peak: float) -> dict:
+    """One record per configuration beside the headline's (run after its timed
+    region): the worked-example / p=4 fp32 collectives, the ZeRO chain, the
+    MoE all-to-allv and the all-reduce sweep at 8 MiB, 64 MiB and 1 GiB per
+    rank for p = 2, 16 and 72.  Each entry: effective GB/s and the fraction
+    of the measured copy bandwidth per call (CUDA graph of back-to-back calls,
+    ``measure_point``), the kernel's per-launch time, and the CPU-baseline
+    leg's oracle check."""
+    from a2a_ring_ordered_gb300 import workloads
+    out: dict = {}
+    s = torch.cuda.Stream(device)
+    gen = torch.Generator(device=device)
+    kernel = {"allreduce": "fold", "reduce_scatter": "fold", "all_gather": "gather", "all_to_all": "a2av"}
+
+    def point(kind, dt, p, n, init=None, seed=0, count=4096):
+        rec, views = measure_point(lib, torch, device, s, kind, dt, p, n, gen, peak, init=init)
+        rec["kernel"] = kernel[kind]
+        rec["ms_per_launch"] = round(rec["us_per_call"] * 1e-3, 6)
+        rec["oracle_check"] = oracle_check_leg(lib, kind, dt, p, n, views[0][0], views[0][1], count=count,
+                                               seed=seed)
+        rec["checked"] = rec["oracle_check"]["checked"]
+        del views
+        torch.cuda.empty_cache()
+        return rec
+
+    # (1) p=4 fp32, n=1,048,576 per rank ~ N(0,1) from seed 0 (set 0 holds
+    # exactly those inputs; the other rotation sets U(-1,1))
+    p, n = 4, 1_048_576
+    x = workloads.normal(p, n, 1.0, seed=0)
+    blocks = [x[k][off:off + ln] for k, (off, ln) in
+              ((k, lib.ccl_chunk_bounds(p, n, k)) for k in range(p))]
+
+    def init_full(j, ins):
+        if j == 0:
+            for r, t in enumerate(ins):
+                t.copy_(torch.from_numpy(x[r]))
+
+    def init_blocks(j, ins):
+        if j == 0:
+            for r, t in enumerate(ins):
+                t.copy_(torch.from_numpy(blocks[r]))
+    gen.manual_seed(0)
+    out["1_p4_f32_n1048576"] = {
+        "workload": "p=4 fp32, n=1,048,576 per rank ~ N(0,1) seed 0 (4 MiB per rank)",
+        "allreduce": point("allreduce", "f32", p, n, init_full, count=1 << 16),
+        "reduce_scatter": point("reduce_scatter", "f32", p, n, init_full, count=1 << 16),
+        "all_gather": point("all_gather", "f32", p, n, init_blocks, count=1 << 16),
+        "all_to_all": point("all_to_all", "f32", p, n, init_full, count=1 << 16)}
+
+    # (3) ZeRO: p=16 x 100,663,296 bf16 ~ N(0, 1e-2), seed 2: RS then AG
+    z = Zero()
+    z.setup(lib, torch, device)
+    zrec = {"workload": "ZeRO reduce-scatter then all-gather, p=16 x 192 MiB bf16, N(0, 1e-2) seed 2"}
+    for name, nb, fn in z.parts():
+        zrec[("reduce_scatter" if name == "fold" else "all_gather")] = _time_part(torch, device, s, fn, nb, peak, name)
+    chain = zrec["reduce_scatter"]["ms_per_launch"] + zrec["all_gather"]["ms_per_launch"]
+    zrec["chain"] = {"ms": round(chain, 5), "effective_gbs": round(z.bytes_per_step() / (chain * 1e-3) / 1e9, 1),
+                     "frac_of_hbm": round(z.bytes_per_step() / (chain * 1e-3) / 1e9 / peak, 4)}
+    chk_rs = oracle_check_leg(lib, "reduce_scatter", "bf16", z.p, z.n, z.send, z.shards, count=1 << 16, seed=3)
+    chk_ar = oracle_check_leg(lib, "allreduce", "bf16", z.p, z.n, z.send, z.recv, count=1 << 16, seed=4)
+    zrec["oracle_check"] = {"reduce_scatter": chk_rs, "all_gather_of_shards_equals_allreduce": chk_ar}
+    zrec["checked"] = chk_rs["checked"] and chk_ar["checked"]
+    out["3_zero_p16_bf16_192MiB"] = zrec
+    del z
+    torch.cuda.empty_cache()
+
+    # (4) MoE all-to-allv dispatch + combine, p=8, Zipf(1.2) counts, seed 3
+    m = Moe()
+    m.setup(lib, torch, device)
+    mrec = {"workload": "MoE all-to-allv dispatch + combine: p=8, 16,384 tokens x 4096 bf16 per rank, "
+                        "Zipf(1.2) counts seed 3"}
+    for (name, nb, fn), what in zip(m.parts(), ("dispatch", "combine")):
+        mrec[what] = _time_part(torch, device, s, fn, nb, peak, name)
+    m.step(s)
+    torch.cuda.synchronize(device)
+    mrec["oracle_check"] = moe_check_leg(m)
+    mrec["checked"] = mrec["oracle_check"]["checked"]
+    out["4_moe_p8_zipf"] = mrec
+    del m
+    torch.cuda.empty_cache()
+
+    # (5) all-reduce at 8 MiB, 64 MiB and 1 GiB per rank (p=72: 256 MiB), U(-1,1) seed 4
+    gen.manual_seed(4)
+    pts = []
+    for dt in ("f32", "bf16"):
+        e = 4 if dt == "f32" else 2
+        for p in (2, 16, 72):
+            for mib in (8, 64, 256 if p == 72 else 1024):
+                pts.append(point("allreduce", dt, p, (mib << 20) // e, seed=mib))
+    out["5_allreduce_sweep"] = pts
+    return out
+
+
+def _time_part(torch, device, stream, fn, nbytes: int, peak: float, kernel: str, calls: int = 20) -> dict:
+    """K back-to-back launches of one part in a CUDA graph, CUDA events."""
+    for _ in range(2):
+        fn(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            fn(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / calls
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": kernel, "ms_per_launch": round(ms, 5), "algorithmic_bytes_per_launch": nbytes,
+            "effective_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
+
+
+def moe_check_leg(m, rows_per_dest: int = 512, seed: int = 3) -> dict:
+    """The CPU-baseline leg's check of the MoE exchange: sampled received rows
+    of every destination (random rows plus the first and last row of every
+    source's block) against the oracle's all-to-allv placement, and the
+    combine's rows against the sender's (combine of dispatch = identity)."""
+    import torch
+    from oracle import pointwise
+    t0 = time.perf_counter()
+    rng = np.random.default_rng(seed)
+    mism, nrows = 0, 0
+    h = m.hidden
+    dev = m.send[0].device
+    for d in range(m.p):
+        total = int(m.counts[:, d].sum())
+        if total == 0:
+            continue
+        starts = np.concatenate([[0], np.cumsum(m.counts[:, d])])
+        edges = np.concatenate([starts[:-1], starts[1:] - 1])
+        rows = np.unique(np.concatenate([rng.integers(0, total, rows_per_dest), edges]))
+        rows = rows[(rows >= 0) & (rows < total)]
+        src, srow = pointwise.all_to_allv_source(m.counts, d, rows)
+        got = _bits(m.mid[d].view(-1, h)[torch.from_numpy(rows).to(dev)])
+        want = np.empty_like(got)
+        for a_ in np.unique(src):
+            sel = src == a_
+            want[sel] = _bits(m.send[int(a_)].view(-1, h)[torch.from_numpy(srow[sel]).to(dev)])
+        mism += int((got != want).any(axis=1).sum())
+        nrows += rows.size
+    for s_ in range(m.p):
+        total = int(m.counts[s_].sum())
+        rows = np.unique(np.concatenate([rng.integers(0, total, rows_per_dest), [0, total - 1]]))
+        it = torch.from_numpy(rows).to(dev)
+        got, want = _bits(m.back[s_].view(-1, h)[it]), _bits(m.send[s_].view(-1, h)[it])
+        mism += int((got != want).any(axis=1).sum())
+        nrows += rows.size
+    return {"checked": mism == 0, "rows_checked": int(nrows), "mismatching_rows": int(mism),
+            "oracle_s": round(time.perf_counter() - t0, 3),
+            "how": "oracle.pointwise.all_to_allv_source for sampled received rows; combine rows vs sent rows"}
 
 
 def main(argv=None) -> int:
@@ -1480,7 +1759,7 @@ def main(argv=None) -> int:
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=0,
                     help="timed steps (default: enough for ~1 s of device time, so the "
-                         "200 ms clock sampler sees the timed region)")
+                         "clock record holds hundreds of samples)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bucket",
@@ -1500,6 +1779,8 @@ def main(argv=None) -> int:
     ap.add_argument("--group", type=int, default=8,
                     help="ranks per group of --schedule hierarchical (groups of consecutive ranks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration records that follow the default bench line")
     ap.add_argument("--eager", action="store_true",
                     help="issue every timed step from Python instead of replaying a CUDA graph")
     ap.add_argument("--sweep", action="store_true",
@@ -1508,6 +1789,8 @@ def main(argv=None) -> int:
     ap.add_argument("--sweep-dtype-only", action="store_true", help="sweep only --dtype")
     ap.add_argument("--sweep-lo", type=int, default=10, help="log2 of the smallest per-rank message (bytes)")
     ap.add_argument("--sweep-hi", type=int, default=30, help="log2 of the largest per-rank message (bytes)")
+    ap.add_argument("--sweep-sizes", default="",
+                    help="comma-separated log2 per-rank message sizes (bytes), in place of --sweep-lo/hi/stride")
     ap.add_argument("--sweep-collective", default="allreduce",
                     choices=["allreduce", "reduce_scatter", "all_gather", "all_to_all"],
                     help="collective of --sweep")

@@ -253,8 +253,9 @@ ccl_status_t ccl_bucket_allreduce_scale_cast(const float* const* grads, void* co
 /* All-to-all ("Networks and Collective Communication" 4.1: device i's block j
  * goes to device j, a transpose).  send[i]: n elements cut into p blocks by
  * the chunk rule; recv[j]: p * len(j) elements, block j of every source in
- * source order.  ccl_all_to_allv with counts[s][d] = len(d) and one-element
- * rows; applying it twice restores the inputs when p divides n. */
+ * source order (the all-to-allv with counts[s][d] = len(d) and one-element
+ * rows); applying it twice restores the inputs when p divides n.  The block
+ * geometry follows from p and n, so every call is one kernel launch. */
 ccl_status_t ccl_all_to_all(const void* const* send, void* const* recv, int p, size_t n, ccl_dtype_t dt,
                             void* stream);
 
@@ -268,8 +269,12 @@ ccl_status_t ccl_all_to_all(const void* const* send, void* const* recv, int p, s
  *   recv[d]    sum_s counts[s][d] rows; the block from s lands at row
  *              sum_{s' < s} counts[s'][d].
  * Combine is the same call on the received buffers with counts transposed.
- * Buffers must not overlap.  Bit-exact copy for every dtype.  One kernel
- * launch per 1016 non-empty blocks (one launch up to p = 31). */
+ * Buffers must not overlap.  Bit-exact copy for every dtype.  The counts
+ * travel to the kernel as a table of row prefixes inside its parameter
+ * block (nothing is allocated): one launch for p <= 85, else one launch per
+ * group of destinations that fits (p = 128: three).  While some source has
+ * 2^32 rows or more the table takes 64-bit entries and half as many
+ * destinations per launch. */
 ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts, void* const* recv,
                              int p, size_t row_elems, ccl_dtype_t dt, void* stream);
 

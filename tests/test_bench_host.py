@@ -8,6 +8,7 @@ import socket
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -133,3 +134,40 @@ def test_cpu_rank_sample_times_the_same_workload():
     dt1, nb1, _ = wl.oracle_sample(0.01)
     assert nb == nb1 and dt > 0 and dt1 > 0
     assert 1 <= threads <= wl.p and f"{threads} threads" in desc
+
+
+@pytest.mark.parametrize("kind", ["allreduce", "reduce_scatter", "all_gather", "all_to_all"])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_oracle_check_leg_accepts_the_oracle_and_catches_one_wrong_element(kind, dt):
+    """The bench's sampled check (host logic, CPU tensors): outputs written by
+    the oracle pass; one element changed at a chunk edge is caught."""
+    import torch
+
+    from a2a_ring_ordered_gb300 import ccl as lib
+    from a2a_ring_ordered_gb300 import workloads
+    from oracle import collectives, ring
+
+    p, n = 5, 1003
+    x = workloads.normal(p, n, 1.0, seed=7, dtype=dt)
+    t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == "bf16" else torch.from_numpy(a)
+    bounds = ring.chunk_bounds(p, n)
+    if kind == "all_gather":
+        snd = [x[k][off:off + ln] for k, (off, ln) in enumerate(bounds)]
+        rcv = collectives.all_gather(snd)
+    elif kind == "all_to_all":
+        snd, rcv = x, collectives.all_to_all(x)
+    elif kind == "allreduce":
+        snd, rcv = x, ring.ring_allreduce(x, dt, "sum")[0]
+    else:
+        snd, rcv = x, ring.ring_reduce_scatter(x, dt, "sum")[0]
+    snd_t = [t(np.ascontiguousarray(v)) for v in snd]
+    rcv_t = [t(np.ascontiguousarray(v).copy()) for v in rcv]
+    ok = bench.oracle_check_leg(lib, kind, dt, p, n, snd_t, rcv_t, count=64)
+    assert ok["checked"] and ok["mismatches"] == 0 and ok["samples"] > 64
+    # corrupt one sampled element: a chunk edge of rank 0's output (rank 0's
+    # shard start for the reduce-scatter)
+    pos = 0 if kind in ("reduce_scatter", "all_to_all") else bounds[1][0]
+    v = rcv_t[0].view(torch.int16) if dt == "bf16" else rcv_t[0].view(torch.int32)
+    v[pos] ^= 1
+    bad = bench.oracle_check_leg(lib, kind, dt, p, n, snd_t, rcv_t, count=64)
+    assert not bad["checked"] and bad["mismatches"] == 1

@@ -83,3 +83,41 @@ def test_all_to_all_past_4_gib_offsets(lib):
         assert_equal(to_host(recv[j][torch.from_numpy(pos).cuda()]), want, "f32", f"A2A rank {j}")
     del send, recv
     _free()
+
+
+def test_all_to_allv_row_prefixes_past_32_bits(lib):
+    """A source with more than 2^32 rows: the row-prefix table takes 64-bit
+    entries.  p = 2, one-element bf16 rows, source 0 sends 2^31 + 5 rows to
+    destination 0 and 2^31 + 7 to destination 1 (8.6 GB), source 1 three and
+    two rows.  Sampled received rows (every block edge included) against the
+    oracle's placement (oracle.pointwise.all_to_allv_source), and every
+    block equal to its source slice on the device."""
+    from oracle import pointwise
+    p = 2
+    counts = np.array([[(1 << 31) + 5, (1 << 31) + 7], [3, 2]], dtype=np.int64)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(34)
+    send = [(torch.rand(int(counts[s].sum()), generator=gen, device="cuda") * 2 - 1).to(torch.bfloat16)
+            for s in range(p)]
+    recv = [torch.empty(int(counts[:, d].sum()), dtype=torch.bfloat16, device="cuda") for d in range(p)]
+    lib.ccl_all_to_allv(send, counts, recv, 1)
+    rng = np.random.default_rng(35)
+    for d in range(p):
+        total = int(counts[:, d].sum())
+        starts = np.concatenate([[0], np.cumsum(counts[:, d])])
+        rows = np.unique(np.concatenate([rng.integers(0, total, size=1 << 16), starts[:-1], starts[1:] - 1]))
+        rows = rows[rows < total]
+        src, srow = pointwise.all_to_allv_source(counts, d, rows)
+        want = np.empty(rows.size, dtype=np.uint16)
+        for s in range(p):
+            sel = src == s
+            want[sel] = to_host(send[s][torch.from_numpy(srow[sel]).cuda()])
+        assert_equal(to_host(recv[d][torch.from_numpy(rows).cuda()]), want, "bf16", f"a2av rank {d}")
+    # whole blocks on the device
+    a, b = int(counts[0, 0]), int(counts[0, 1])
+    assert torch.equal(recv[0][:a].view(torch.int16), send[0][:a].view(torch.int16))
+    assert torch.equal(recv[0][a:].view(torch.int16), send[1][:3].view(torch.int16))
+    assert torch.equal(recv[1][:b].view(torch.int16), send[0][a:].view(torch.int16))
+    assert torch.equal(recv[1][b:].view(torch.int16), send[1][3:].view(torch.int16))
+    del send, recv
+    _free()

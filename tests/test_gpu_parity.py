@@ -343,12 +343,22 @@ def test_all_to_all_equal_blocks(lib, dtype, p, n):
             assert_equal(to_host(back[j]), x[j], dtype, f"A2A twice rank {j}")
 
 
-@pytest.mark.parametrize("p,row,hi", [(16, 64, 40), (48, 3, 6), (128, 8, 2)])
+def a2av_launches(p: int) -> int:
+    """Launches of an all-to-allv: the row-prefix table of p sources x
+    (destinations + 1) columns travels in the parameter block, 16 x 17
+    entries in the 4 KB form, 7408 in the 32 KB form (uint32 entries)."""
+    if p <= 16:
+        return 1
+    per = 7408 // p - 1
+    return -(-p // per)
+
+
+@pytest.mark.parametrize("p,row,hi", [(16, 64, 40), (48, 3, 6), (85, 1, 3), (86, 2, 3), (128, 8, 2)])
 def test_all_to_allv_many_blocks(lib, p, row, hi):
-    """More blocks than a 4 KB parameter block holds: p=16 (256 blocks, one
-    launch with the large parameter block), p=48 with 3-element rows (about
-    1900 blocks, two launches, shuffle realignment), p=128 (about 8200 blocks
-    of 0-1 rows, nine launches)."""
+    """Many blocks: p=16 (256 blocks, the 4 KB parameter block), p=48 with
+    3-element rows (about 1900 blocks, phase-shifted, one launch), p=85 with
+    one-element rows (the largest p whose table fits one launch), p=86 (two
+    launches), p=128 (about 8200 blocks of 0-1 rows, three launches)."""
     rng = np.random.default_rng(5 + p)
     counts = rng.integers(0 if p > 16 else 1, hi, size=(p, p))
     x = [workloads.normal(1, max(int(counts[s].sum()), 1) * row, 1.0, seed=s, dtype="bf16")[0][: int(counts[s].sum()) * row]
@@ -359,9 +369,52 @@ def test_all_to_allv_many_blocks(lib, p, row, hi):
     blocks = int((counts > 0).sum())
     n0 = lib.ccl_kernel_launch_count()
     lib.ccl_all_to_allv([to_dev(v, "bf16") for v in x], counts, recv, row)
-    assert lib.ccl_kernel_launch_count() - n0 == -(-blocks // 1016)
+    assert blocks > 0
+    assert lib.ccl_kernel_launch_count() - n0 == a2av_launches(p)
     for d in range(p):
         assert_equal(to_host(recv[d]), want[d], "bf16", f"rank {d}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("p,n", [(72, 256), (72, 512), (128, 1000), (72, 72 * 301 + 5), (100, 37)])
+def test_all_to_all_small_blocks_one_launch(lib, dtype, p, n):
+    """The plain all-to-all is one launch for any p (its blocks follow the
+    chunk rule, nothing travels in a table): 1 KiB and 2 KiB per rank at
+    p = 72 (blocks of 3-4 and 7-8 elements, no block holding a whole 16-byte
+    unit), p = 128, p = 100 with n < p (empty blocks), and mid-size blocks
+    off the 16-byte grid; every element against the oracle, guard bands."""
+    x = make_inputs(dtype, p, n, seed=p + n)
+    want = collectives.all_to_all(x)
+    outs = [Guarded(len(want[j]), dtype, offset=GUARD + j % 5) for j in range(p)]
+    send = [to_dev(v, dtype) for v in x]
+    n0 = lib.ccl_kernel_launch_count()
+    lib.ccl_all_to_all(send, [o.view for o in outs])
+    assert lib.ccl_kernel_launch_count() - n0 == 1
+    for j in range(p):
+        assert_equal(to_host(outs[j].view), want[j], dtype, f"A2A {dtype} p={p} n={n} rank {j}")
+        assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("row_elems,dtype", [(1, "bf16"), (1, "f32"), (3, "bf16"), (5, "f32")])
+def test_all_to_allv_tiny_rows_straddle_units(lib, row_elems, dtype):
+    """Rows far smaller than a 16-byte unit with many empty blocks: every
+    destination unit holds elements of several blocks and is assembled
+    element by element; p = 24, counts 0-3 rows."""
+    p = 24
+    rng = np.random.default_rng(row_elems * 31 + len(dtype))
+    counts = rng.integers(0, 4, size=(p, p))
+    counts[rng.random((p, p)) < 0.3] = 0
+    send_np = [make_inputs(dtype, 1, max(1, int(counts[s].sum()) * row_elems), seed=s)[0][: int(counts[s].sum()) * row_elems]
+               for s in range(p)]
+    want = collectives.all_to_allv(send_np, counts, row_elems)
+    send = [to_dev(np.ascontiguousarray(v), dtype) for v in send_np]
+    outs = [Guarded(int(counts[:, d].sum()) * row_elems, dtype, offset=GUARD + d % 7) for d in range(p)]
+    n0 = lib.ccl_kernel_launch_count()
+    lib.ccl_all_to_allv(send, counts, [o.view for o in outs], row_elems)
+    assert lib.ccl_kernel_launch_count() - n0 == 1
+    for d in range(p):
+        assert_equal(to_host(outs[d].view), want[d], dtype, f"a2av rank {d}")
+        assert outs[d].guards_intact()
 
 
 # ------------------------------------------- bulk-copy fan-out (TMA bulk)
