@@ -162,18 +162,26 @@ cudaError_t launch_typed(bool vec, const GatherArgs& a, cudaStream_t s) {
   // 8 vectors (128 bytes) of loads in flight per thread before its p x 8
   // stores: at p = 16 that is 0.977 -> 1.022 of the copy bandwidth over 4
   // vectors, 8 outrunning 2 and 4 and matching 32-byte stores.  Mid-size
-  // calls whose grid would be under 8 CTAs per SM take 2 vectors per thread
-  // (4x the CTAs) instead, as the fold kernels do: measured on GB300 for
-  // bf16, p = 16 at 8 / 16 MiB per rank 0.74 -> 0.82 / 0.75 -> 0.98 of the
-  // copy bandwidth, p = 2 at 8 MiB 0.59 -> 0.75.  (The broadcast, tried the
-  // same way, went up at p = 4 and down at p = 16, and keeps 8.)
+  // calls whose grid would be under 8 CTAs per SM take fewer vectors per
+  // thread, as the fold kernels do: 1 while that grid stays within 20 CTAs
+  // per SM (2.5 waves of this 32-register kernel), else 2.  Measured on
+  // GB300 (fp32, fraction of the copy bandwidth, 2 vectors -> 1): p = 2 at
+  // 4 / 8 MiB per rank 0.66 -> 0.72 / 0.75 -> 0.82, p = 8 at 4 / 8 MiB
+  // 0.64 -> 0.90 / 0.84 -> 0.88, p = 16 at 8 MiB 0.83 -> 0.91; at 16 MiB
+  // (about 3.4 waves with 1) 2 vectors stay ahead (p = 2: 0.94 against
+  // 0.91).  Before that rule, 2 vectors against 8: bf16 p = 16 at 8 / 16 MiB
+  // 0.74 -> 0.82 / 0.75 -> 0.98.  (The broadcast, tried the same way, went
+  // up at p = 4 and down at p = 16, and keeps 8.)
   if (!vec) return launch_one<DT, 1, 1>(a, s);
   constexpr int VEC = 16 / Elem<DT>::kBytes;
   const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
   const int sms = current_sm_count();
-  const uint64_t want_ctas = 8ull * static_cast<uint64_t>(sms > 0 ? sms : 1);
-  if ((per_chunk + kThreads * 8 - 1) / (kThreads * 8) * static_cast<uint64_t>(a.p) < want_ctas)
+  const uint64_t sm_count = static_cast<uint64_t>(sms > 0 ? sms : 1);
+  auto ctas = [&](uint64_t u) { return (per_chunk + kThreads * u - 1) / (kThreads * u) * static_cast<uint64_t>(a.p); };
+  if (ctas(8) < 8 * sm_count) {
+    if (ctas(1) <= 20 * sm_count) return launch_one<DT, VEC, 1>(a, s);
     return launch_one<DT, VEC, 2>(a, s);
+  }
   return launch_one<DT, VEC, 8>(a, s);
 }
 

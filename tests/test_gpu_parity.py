@@ -128,6 +128,22 @@ def test_all_gather_matches_oracle(lib, dtype, p, n):
         assert outs[r].guards_intact()
 
 
+# vectors per thread of the all-gather (the host picks them by grid size):
+# mid-size calls take 1 (grids up to 20 CTAs per SM) or 2, larger ones 8;
+# blocks on the 16-byte grid or off it (p = 72, p = 3)
+AG_SIZE_CLASSES = [("f32", 2, 2 * 1048576), ("bf16", 8, 8 * 262144 + 8), ("bf16", 72, 72 * 41000 + 5),
+                   ("f32", 2, 4 * 1048576), ("bf16", 3, 3 * 4194304 + 1), ("f32", 2, 16 * 1048576 + 4),
+                   ("f32", 3, 3 * 3400000 + 1)]
+
+
+@pytest.mark.parametrize("dtype,p,n", AG_SIZE_CLASSES)
+def test_all_gather_size_classes_match_oracle(lib, dtype, p, n):
+    """Every element of every output against the literal ring all-gather,
+    at sizes that select 1, 2 and 8 vectors per thread, aligned and
+    realigned blocks, guard bands."""
+    test_all_gather_matches_oracle(lib, dtype, p, n)
+
+
 # -------------------------------------------- alignment and in-place forms
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("p,n", [(4, 1027), (8, 4096), (3, 50001)])
