@@ -32,8 +32,6 @@
 namespace ccl {
 namespace {
 
-constexpr int kUnitsPerTile = static_cast<int>(kA2ATileBytes / 16);  // 2048
-constexpr int kUnitsPerThread = kUnitsPerTile / kThreads;             // 8
 
 // Bounds of destination j's blocks, in bytes: block i covers destination
 // bytes [dst0 + cs[i], dst0 + cs[i+1]) and its first byte comes from src[i].
@@ -88,7 +86,7 @@ __device__ __noinline__ void unit_by_elements(const uint64_t* cs, const char* co
 // SHIFT: some block's source and destination differ in 16-byte phase (the
 // host checks); without it each thread keeps 8 units' loads in flight,
 // with it 4 units' two granules.  64 registers, 4 CTAs per SM.
-template <class P, bool SHIFT>
+template <class P, bool SHIFT, uint32_t TILE>
 __global__ void __launch_bounds__(kThreads, 4) a2a_kernel(const __grid_constant__ P a) {
   __shared__ uint64_t s_cs[P::kCap + 1];
   __shared__ const char* s_src[P::kCap];
@@ -96,6 +94,15 @@ __global__ void __launch_bounds__(kThreads, 4) a2a_kernel(const __grid_constant_
   const int p = a.p;
   const uint64_t rb = a.row_bytes;
   const uint64_t total_tiles = a.tile0[a.ndest];
+  // Tile size and 16-byte units per thread (8 for 32 KB tiles, 1 for 4 KB
+  // ones).  The phase-shifting kernels take it from the template (one
+  // instantiation per tile size), the others from the parameters: measured
+  // on GB300, the other way round cost up to 10 % (the template form of the
+  // unshifted kernel spilled 16 bytes: p = 8 all-to-all at 8 MiB per rank
+  // 1.01 -> 0.91 of the copy bandwidth; the parameter form of the shifted
+  // one ran p = 72 at 0.98 instead of 1.01).
+  const uint32_t tile = SHIFT ? TILE : a.tile_bytes;
+  const int units_per_thread = static_cast<int>(tile / 16 / kThreads);
   for (uint64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
     // this tile's destination (uniform over the CTA)
     int c = 0;
@@ -145,9 +152,9 @@ __global__ void __launch_bounds__(kThreads, 4) a2a_kernel(const __grid_constant_
 
     Blocks b{s_cs, s_src, reinterpret_cast<uintptr_t>(a.recv[j]), p};
     const uintptr_t vlo0 = b.dst0, vhi0 = b.dst0 + s_cs[p];
-    const uintptr_t tlo = (b.dst0 & ~static_cast<uintptr_t>(511)) + (t - a.tile0[c]) * kA2ATileBytes;
+    const uintptr_t tlo = (b.dst0 & ~static_cast<uintptr_t>(511)) + (t - a.tile0[c]) * tile;
     const uintptr_t vlo = tlo > vlo0 ? tlo : vlo0;
-    const uintptr_t vhi = tlo + kA2ATileBytes < vhi0 ? tlo + kA2ATileBytes : vhi0;
+    const uintptr_t vhi = tlo + tile < vhi0 ? tlo + tile : vhi0;
     // the blocks this tile touches
     const int ia = block_of(b, vlo - b.dst0, 0, p - 1);
     const int ib = block_of(b, vhi - 1 - b.dst0, ia, p - 1);
@@ -179,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 4) a2a_kernel(const __grid_constant_
     // issued together
     constexpr int U = SHIFT ? 4 : 8;
 #pragma unroll 1
-    for (int w0 = 0; w0 < kUnitsPerThread; w0 += U) {
+    for (int w0 = 0; w0 < units_per_thread; w0 += U) {
       uint4 g0[U], g1[U];
       // per unit: -1 outside the tile's bytes, else (block << 5) | (whole << 4) | phase
       int code[U];
@@ -233,16 +240,18 @@ cudaError_t launch_params(const P& a, bool shift, cudaStream_t s) {
   if (tiles == 0) return cudaSuccess;
   const uint64_t g = tiles < (1ull << 31) - 1 ? tiles : (1ull << 31) - 1;
   const dim3 grid(static_cast<unsigned>(g));
-  return shift ? launch_kernel(a2a_kernel<P, true>, grid, dim3(kThreads), s, a)
-               : launch_kernel(a2a_kernel<P, false>, grid, dim3(kThreads), s, a);
+  constexpr uint32_t kBig = static_cast<uint32_t>(kA2ATileBytes), kSmall = static_cast<uint32_t>(kA2ASmallTileBytes);
+  if (!shift) return launch_kernel(a2a_kernel<P, false, kBig>, grid, dim3(kThreads), s, a);  // tile size at run time
+  if (a.tile_bytes == kSmall) return launch_kernel(a2a_kernel<P, true, kSmall>, grid, dim3(kThreads), s, a);
+  return launch_kernel(a2a_kernel<P, true, kBig>, grid, dim3(kThreads), s, a);
 }
 
 }  // namespace
 
-uint64_t a2a_tiles_for(const char* dst, uint64_t bytes) {
+uint64_t a2a_tiles_for(const char* dst, uint64_t bytes, uint64_t tile_bytes) {
   if (bytes == 0) return 0;
   const uint64_t lead = reinterpret_cast<uintptr_t>(dst) & 511;  // tiles start on 512-byte boundaries
-  return (lead + bytes + kA2ATileBytes - 1) / kA2ATileBytes;
+  return (lead + bytes + tile_bytes - 1) / tile_bytes;
 }
 
 cudaError_t launch_a2a(const A2ASmall& a, bool shift, cudaStream_t s) {

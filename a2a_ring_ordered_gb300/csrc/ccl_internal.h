@@ -84,7 +84,8 @@ cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, 
 
 // ------------------------------------------------------------- all-to-allv
 // Destination j's buffer holds one block per source i in source order; work
-// is cut into kA2ATileBytes tiles of destination space (boundaries on 512
+// is cut into tiles of tile_bytes of destination space (kA2ATileBytes, or
+// kA2ASmallTileBytes for calls too small to fill the GPU; boundaries on 512
 // bytes of the destination's address), tile0[c] = first tile of destination
 // j0 + c in this launch, tile0[ndest] = the launch's tiles.
 //  plain = 1: the all-to-all of the chunk rule, one element per row:
@@ -94,6 +95,7 @@ cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, 
 //    for destination j0 + c (c = 0..ndest; c = ndest gives the next
 //    destination's start, or source i's total rows when j0 + ndest = p).
 constexpr uint64_t kA2ATileBytes = 32768;
+constexpr uint64_t kA2ASmallTileBytes = 4096;
 template <int CAP, int TCAP, typename TT>
 struct A2AParamsT {
   static constexpr int kCap = CAP;
@@ -106,6 +108,7 @@ struct A2AParamsT {
   uint64_t q, rem;     // plain: the chunk rule of n
   int p, j0, ndest, plain;
   int elem;            // element bytes (2 or 4)
+  uint32_t tile_bytes; // kA2ATileBytes or kA2ASmallTileBytes
   TT table[TCAP];
 };
 // p <= 16, any geometry (a table of 16 x 17 entries): under the classic 4 KB
@@ -120,7 +123,7 @@ static_assert(sizeof(A2ASmall) <= 4096, "all-to-allv parameters exceed 4 KB");
 static_assert(sizeof(A2APlain) <= 4096, "all-to-all parameters exceed 4 KB");
 static_assert(sizeof(A2ATable32) <= 32764, "all-to-allv parameters exceed 32,764 bytes");
 static_assert(sizeof(A2ATable64) <= 32764, "all-to-allv parameters exceed 32,764 bytes");
-uint64_t a2a_tiles_for(const char* dst, uint64_t bytes);
+uint64_t a2a_tiles_for(const char* dst, uint64_t bytes, uint64_t tile_bytes);
 // shift: some block's source and destination differ in 16-byte phase
 cudaError_t launch_a2a(const A2ASmall& a, bool shift, cudaStream_t s);
 cudaError_t launch_a2a(const A2APlain& a, bool shift, cudaStream_t s);

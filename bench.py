@@ -9,9 +9,14 @@ the all-gather and the all-reduce of that bucket in one kernel.
 
 Metric: effective GB/s = the primitive's minimum HBM bytes per step / the
 device time of a step (CUDA events on the launching stream), and the fraction
-of the measured HBM copy bandwidth.  Other workloads (``--workload``) cover the
-ZeRO chain, MoE dispatch/combine, plain all-reduce sweep points and the
-literal ring engine.
+of the measured HBM copy bandwidth.  After the default line's timed region
+it also carries ``configs``: the other configurations of the workload set
+(the p=4 fp32 collectives, the ZeRO chain, the MoE all-to-allv, the
+all-reduce at 8 MiB / 64 MiB / 1 GiB per rank for p = 2, 16, 72), each timed
+and checked against the oracle at sampled positions.  Other workloads
+(``--workload``) cover the ZeRO chain, MoE dispatch/combine, plain
+all-reduce points, the other fold orders and the literal ring engine;
+``--sweep`` runs a message-size sweep of one collective.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload bucket|allreduce|reduce_scatter|all_gather|zero|moe|literal]
