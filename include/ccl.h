@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
   CCL_OK = 0,
   CCL_ERR_INVALID_ARG = 1, /* bad p, pointer, size, alignment or aliasing */
-  CCL_ERR_UNSUPPORTED = 2, /* valid arguments this build does not implement */
+  CCL_ERR_UNSUPPORTED = 2, /* valid arguments this library does not implement */
   CCL_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
   CCL_ERR_TIMEOUT = 4      /* a bounded device-side wait ran out (kernels run asynchronously,
                               so ccl_stream_check reports it); no kernel of this library waits
