@@ -986,7 +986,7 @@ void fill_pointers(P& a, const void* const* send, void* const* recv, int p) {
 template <class P>
 ccl_status_t a2a_table_launches(P& a, const void* const* send, void* const* recv, const size_t* counts,
                                 int p, uint64_t row_bytes, size_t e, const uint64_t* out_bytes,
-                                bool shift, cudaStream_t s) {
+                                bool shift, bool stage, cudaStream_t s) {
   const int per_launch = P::kTableCap / p - 1;
   for (int j0 = 0; j0 < p; j0 += per_launch) {
     memset(static_cast<void*>(&a), 0, sizeof(a));
@@ -1007,7 +1007,7 @@ ccl_status_t a2a_table_launches(P& a, const void* const* send, void* const* recv
       }
     }
     if (fill_tiles(a, recv, out_bytes) == 0) continue;
-    cudaError_t err = launch_a2a(a, shift, s);
+    cudaError_t err = launch_a2a(a, shift, stage, s);
     if (err != cudaSuccess) return cuda_fail(err, "all-to-all kernel launch");
   }
   return CCL_OK;
@@ -1037,18 +1037,36 @@ ccl_status_t a2a_table(const void* const* send, const size_t* counts, void* cons
       col[d] += c;
     }
   }
+  // the small-block stage: some block edge or destination end off the
+  // 16-byte grid, and blocks of kA2AStageMaxBlockBytes or less on average
+  bool off_grid = false;
+  uint64_t blocks = 0, total = 0;
+  for (int d = 0; d < p; ++d) {
+    if (out_bytes[d] == 0) continue;
+    const uintptr_t dst = reinterpret_cast<uintptr_t>(recv[d]);
+    uint64_t rows = 0;
+    for (int i = 0; i < p; ++i) {
+      const uint64_t c = counts[static_cast<size_t>(i) * p + d];
+      off_grid = off_grid || ((dst + rows * row_bytes) & 15) != 0;
+      blocks += c != 0 ? 1 : 0;
+      rows += c;
+    }
+    off_grid = off_grid || ((dst + out_bytes[d]) & 15) != 0;
+    total += out_bytes[d];
+  }
+  const bool stage = off_grid && total <= kA2AStageMaxBlockBytes * blocks;
   // uint32 table entries hold every row prefix only while each source has
   // fewer than 2^32 rows
   if (max_rows >= (1ull << 32)) {
     static thread_local A2ATable64 a;  // 32 KB: kept off the stack
-    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, s);
+    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, stage, s);
   }
   if (p <= A2ASmall::kCap) {
     static thread_local A2ASmall a;
-    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, s);
+    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, stage, s);
   }
   static thread_local A2ATable32 a;
-  return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, s);
+  return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, stage, s);
 }
 
 }  // namespace
@@ -1127,6 +1145,15 @@ extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* rec
       shift = ((src - dst) & 15) != 0;
     }
   }
+  // the small-block stage: some block edge or destination end off the
+  // 16-byte grid, and blocks of kA2AStageMaxBlockBytes or less on average
+  bool off_grid = false;
+  for (int d = 0; d < p && !off_grid; ++d) {
+    if (len[d] == 0) continue;
+    for (int i = 0; i <= p && !off_grid; ++i)
+      off_grid = ((reinterpret_cast<uintptr_t>(recv[d]) + static_cast<uint64_t>(i) * len[d] * e) & 15) != 0;
+  }
+  const bool stage = off_grid && n * e <= kA2AStageMaxBlockBytes * static_cast<uint64_t>(p);
   auto fill = [&](auto& a) -> ccl_status_t {
     memset(static_cast<void*>(&a), 0, sizeof(a));
     fill_pointers(a, send, recv, p);
@@ -1139,7 +1166,7 @@ extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* rec
     a.q = n / static_cast<uint64_t>(p);
     a.rem = n % static_cast<uint64_t>(p);
     if (fill_tiles(a, recv, out_bytes) == 0) return CCL_OK;
-    cudaError_t err = launch_a2a(a, shift, as_stream(stream));
+    cudaError_t err = launch_a2a(a, shift, stage, as_stream(stream));
     if (err != cudaSuccess) return cuda_fail(err, "all-to-all kernel launch");
     return CCL_OK;
   };

@@ -96,6 +96,10 @@ cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, 
 //    destination's start, or source i's total rows when j0 + ndest = p).
 constexpr uint64_t kA2ATileBytes = 32768;
 constexpr uint64_t kA2ASmallTileBytes = 4096;
+// Calls with a block edge off the 16-byte grid take the small-block stage
+// while their blocks average at most this many bytes (larger blocks leave a
+// tile one edge or none, which the element path handles at less cost).
+constexpr uint64_t kA2AStageMaxBlockBytes = 8192;
 template <int CAP, int TCAP, typename TT>
 struct A2AParamsT {
   static constexpr int kCap = CAP;
@@ -124,11 +128,12 @@ static_assert(sizeof(A2APlain) <= 4096, "all-to-all parameters exceed 4 KB");
 static_assert(sizeof(A2ATable32) <= 32764, "all-to-allv parameters exceed 32,764 bytes");
 static_assert(sizeof(A2ATable64) <= 32764, "all-to-allv parameters exceed 32,764 bytes");
 uint64_t a2a_tiles_for(const char* dst, uint64_t bytes, uint64_t tile_bytes);
-// shift: some block's source and destination differ in 16-byte phase
-cudaError_t launch_a2a(const A2ASmall& a, bool shift, cudaStream_t s);
-cudaError_t launch_a2a(const A2APlain& a, bool shift, cudaStream_t s);
-cudaError_t launch_a2a(const A2ATable32& a, bool shift, cudaStream_t s);
-cudaError_t launch_a2a(const A2ATable64& a, bool shift, cudaStream_t s);
+// shift: some block's source and destination differ in 16-byte phase;
+// stage: the units that straddle blocks go through the small-block stage
+cudaError_t launch_a2a(const A2ASmall& a, bool shift, bool stage, cudaStream_t s);
+cudaError_t launch_a2a(const A2APlain& a, bool shift, bool stage, cudaStream_t s);
+cudaError_t launch_a2a(const A2ATable32& a, bool shift, bool stage, cudaStream_t s);
+cudaError_t launch_a2a(const A2ATable64& a, bool shift, bool stage, cudaStream_t s);
 
 // ------------------------------------------------- literal ring engine steps
 // One launch moves p independent transfers, transfer r: src[r] -> dst[r],

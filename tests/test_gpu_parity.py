@@ -433,6 +433,34 @@ def test_all_to_allv_tiny_rows_straddle_units(lib, row_elems, dtype):
         assert outs[d].guards_intact()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "i32", "bf16"])
+@pytest.mark.parametrize("scale", [0, 1, 9000])
+def test_all_to_allv_block_edges_off_grid_same_phase(lib, dtype, scale):
+    """Block edges off the 16-byte grid while every block's source and
+    destination share the 16-byte phase (so no realignment is needed):
+    p = 2, one-element rows, counts chosen so that block (1, 1) starts
+    6 or 4 bytes into a unit on both sides and destination 0 ends off the
+    grid.  The units holding those edges go through the small-block stage;
+    scale 9000 spreads each destination over a hundred tiles or more."""
+    u = 16 // (2 if dtype == "bf16" else 4)  # elements per 16-byte unit
+    a, b, c, d = (scale, 2 * scale + 1, 3 * scale + 2, scale + 3)
+    if dtype == "bf16":
+        counts = np.array([[8 + u * a, 3 + u * b], [3 + u * c, 5 + u * d]])
+    else:
+        counts = np.array([[4 + u * a, 1 + u * b], [1 + u * c, 3 + u * d]])
+    p = 2
+    send_np = [make_inputs(dtype, 1, int(counts[s].sum()), seed=40 + s)[0] for s in range(p)]
+    want = collectives.all_to_allv(send_np, counts, 1)
+    send = [to_dev(v, dtype) for v in send_np]
+    outs = [Guarded(int(counts[:, j].sum()), dtype) for j in range(p)]
+    n0 = lib.ccl_kernel_launch_count()
+    lib.ccl_all_to_allv(send, counts, [o.view for o in outs], 1)
+    assert lib.ccl_kernel_launch_count() - n0 == 1
+    for j in range(p):
+        assert_equal(to_host(outs[j].view), want[j], dtype, f"a2av {dtype} scale {scale} rank {j}")
+        assert outs[j].guards_intact()
+
+
 # ------------------------------------------- bulk-copy fan-out (TMA bulk)
 # with CCL_FORCE_VARIANT=tma, all-gather / broadcast calls with blocks >= 1 MiB,
 # p | n and aligned device buffers run on the bulk-copy engine: whole tiles, a
