@@ -214,16 +214,21 @@ def ccl_chunk_bounds(p: int, n: int, c: int) -> tuple[int, int]:
     return off.value, ln.value
 
 
-def ccl_fold_plan(p: int, n: int, dtype: str = "f32", op: str = "sum", bucket: bool = False,
+FOLD_KINDS = {"allreduce": 0, "reduce_scatter": 1, "bucket": 2, "reduce": 3}  # ccl_fold_kind_t
+
+
+def ccl_fold_plan(p: int, n: int, dtype: str = "f32", op: str = "sum", kind: str = "allreduce",
                   aligned: bool = True, sm_count: int = 0) -> tuple[int, int]:
     """(ranks per load batch, vectors per thread) of the fused fold kernel a
-    call of p ranks x n elements takes; (0, 0) is the general kernel.
-    sm_count <= 0 asks the current device."""
+    call of the given kind with p ranks x n elements takes; (0, 0) is the
+    general kernel.  sm_count <= 0 asks the current device."""
     codes = {"f32": CCL_F32, "bf16": CCL_BF16, "i32": CCL_I32}
     if dtype not in codes:
         raise ValueError(f"dtype must be one of {sorted(codes)}")
+    if kind not in FOLD_KINDS:
+        raise ValueError(f"kind must be one of {sorted(FOLD_KINDS)}")
     b, v = ctypes.c_int(), ctypes.c_int()
-    _check(LIB.ccl_fold_plan(1 if bucket else 0, codes[dtype], _op_code(op), p, n, 1 if aligned else 0,
+    _check(LIB.ccl_fold_plan(FOLD_KINDS[kind], codes[dtype], _op_code(op), p, n, 1 if aligned else 0,
                              sm_count, ctypes.byref(b), ctypes.byref(v)), "ccl_fold_plan")
     return b.value, v.value
 

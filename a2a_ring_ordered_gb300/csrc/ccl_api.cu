@@ -292,18 +292,27 @@ extern "C" ccl_status_t ccl_chunk_bounds(int p, size_t n, int c, size_t* off, si
   return CCL_OK;
 }
 
-extern "C" ccl_status_t ccl_fold_plan(int bucket, ccl_dtype_t dt, ccl_op_t op, int p, size_t n,
+extern "C" ccl_status_t ccl_fold_plan(ccl_fold_kind_t kind, ccl_dtype_t dt, ccl_op_t op, int p, size_t n,
                                       int aligned, int sm_count, int* batch, int* vectors) {
   clear_error();
   ccl_status_t st = check_p(p);
   if (st != CCL_OK) return st;
   if (elem_bytes(dt) == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
   if (!valid_op(op)) return fail(CCL_ERR_INVALID_ARG, "unknown op %d", op);
+  int mode = 0;
+  switch (kind) {
+    case CCL_FOLD_ALLREDUCE: mode = kModeAllReduce; break;
+    case CCL_FOLD_REDUCE_SCATTER: mode = kModeReduceScatter; break;
+    case CCL_FOLD_BUCKET: mode = kModeBucket; break;
+    case CCL_FOLD_REDUCE: mode = kModeReduce; break;
+    default: return fail(CCL_ERR_INVALID_ARG, "unknown call kind %d", kind);
+  }
+  const bool bucket = mode == kModeBucket;
   if (bucket && (dt != CCL_F32 || op != CCL_SUM))
     return fail(CCL_ERR_INVALID_ARG, "the bucket call folds fp32 sums only");
   if (batch == nullptr || vectors == nullptr) return fail(CCL_ERR_INVALID_ARG, "NULL output pointer");
   const int sms = sm_count > 0 ? sm_count : current_sm_count();
-  const FoldPlan pl = fold_plan(dt, bucket ? CCL_BF16 : dt, op, p, n / static_cast<uint64_t>(p),
+  const FoldPlan pl = fold_plan(dt, bucket ? CCL_BF16 : dt, op, mode, p, n / static_cast<uint64_t>(p),
                                 aligned != 0, sms);
   *batch = pl.batch;
   *vectors = pl.vectors;

@@ -39,11 +39,12 @@ cudaError_t launch_fold(int mode, int dt, int op, bool vec, const FoldArgs& a, c
 // The fold kernel a call takes: fold_unrolled_kernel with `batch` ranks'
 // loads issued together and `vectors` vectors per thread, or fold_kernel
 // when batch == 0.  dt_in / dt_out: element types (kF32 -> kBF16 is the
-// bucket); q = floor(n / p); sms = the device's SM count.
+// bucket); mode: the call kind (kMode*); q = floor(n / p); sms = the
+// device's SM count.
 struct FoldPlan {
   int batch, vectors;
 };
-FoldPlan fold_plan(int dt_in, int dt_out, int op, int p, uint64_t q, bool vec, int sms);
+FoldPlan fold_plan(int dt_in, int dt_out, int op, int mode, int p, uint64_t q, bool vec, int sms);
 
 // Fold in another schedule's order (schedule_fold.cu): `linear` = the naive
 // root's rank-order fold; otherwise the pairwise tree over ranks in identity

@@ -323,20 +323,21 @@ cudaError_t launch_typed(bool vec, const FoldArgs& a, cudaStream_t s) {
   constexpr int VEC = vec_width<DT_IN, DT_OUT>();
   if constexpr (OP == CCL_SUM) {
     constexpr bool kHalve = VEC > 4;
-    const FoldPlan pl = fold_plan(DT_IN, DT_OUT, OP, a.p, a.q, true, current_sm_count());
+    const FoldPlan pl = fold_plan(DT_IN, DT_OUT, OP, MODE, a.p, a.q, true, current_sm_count());
 #define CCL_UNROLLED(B, U) \
   if (pl.batch == B && pl.vectors == U) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, B, U>(a, s);
     CCL_UNROLLED(2, 2)
     CCL_UNROLLED(4, 1)
-    if constexpr (kHalve) {
+    CCL_UNROLLED(4, 2)
+    if constexpr (MODE == kModeBucket) {
       CCL_UNROLLED(2, 4)
-      CCL_UNROLLED(4, 2)
     } else {
-      CCL_UNROLLED(2, 8)
-      CCL_UNROLLED(4, 4)
-    }
-    if constexpr (!kHalve || DT_IN == kBF16) {
-      CCL_UNROLLED(8, 2)
+      CCL_UNROLLED(8, 1)
+      if constexpr (MODE == kModeAllReduce) {
+        CCL_UNROLLED(2, 1)
+      } else if constexpr (!kHalve) {
+        CCL_UNROLLED(2, 8)
+      }
     }
 #undef CCL_UNROLLED
     if (pl.batch != 0) return cudaErrorInvalidConfiguration;  // a plan with no instantiation
@@ -364,38 +365,60 @@ cudaError_t launch_mode(int dt, int op, bool vec, const FoldArgs& a, cudaStream_
 }  // namespace
 
 // Small p (sums only) goes to fold_unrolled_kernel with (ranks per batch,
-// vectors per thread) = (2, 8), (4, 4) or (8, 2) for 16-byte fp32 / int32
-// vectors.  A bf16 vector widens to 8 fp32 accumulators and a bucket vector
-// is 32 bytes, so those use (2, 4) and (4, 2) (at most 32 accumulators per
-// thread); bf16 takes (8, 2) for p = 5..8 as well, the bucket leaves p > 4
-// to fold_kernel.
-//
-// Mid-size messages: with many vectors per thread the grid can be only one
-// or two CTAs per SM, and the SMs that got two finish last.  Below about 8
-// CTAs per SM take fewer vectors per thread instead (2 at p <= 2 for every
-// type: measured on GB300, bf16 at 8 MiB per rank 0.74 -> 0.77 of the copy
-// bandwidth against 1, fp32 at 1-4 MiB 10-20 % slower with 4).
-//
-// p <= 8 with 16-byte vectors of 4 words (fp32, int32, and bf16 in and out):
-// 8 ranks x 2 vectors.  Measured for bf16 on GB300 against the general
-// kernel: all-reduce p = 6 0.92 -> 1.03 and p = 8 1.03 -> 1.05,
-// reduce-scatter p = 8 0.94 -> 1.07 of the copy bandwidth at 256 MiB - 1 GiB
-// per rank.  (The bucket's 32-byte fp32 vectors would need 128 registers of
-// loads: it stays on fold_kernel.)
-FoldPlan fold_plan(int dt_in, int dt_out, int op, int p, uint64_t q, bool vec, int sms) {
+// vectors per thread): a thread issues the loads of all its ranks' vectors
+// before folding any.  The choice, measured on GB300 per call kind over
+// 1 MiB - 256 MiB per rank (fractions of the copy bandwidth):
+//  * Calls whose one-vector grid fits one wave (the one-vector kernels hold
+//    4 CTAs per SM) take one vector per thread: all-reduce p = 2 at 2 MiB
+//    0.57 -> 0.63 against two.  Above that, the reduce-scatter (and the
+//    reduce to the root: the same bytes read and written) wants more loads in
+//    flight than the all-reduce, which also stores every vector p times:
+//  * p <= 2: all-reduce 2 x 2 (2 x 8 fp32 / 2 x 4 bf16 at 20 MiB and up ran
+//    0.7-0.9 % slower); reduce-scatter 2 x 2, fp32 / int32 2 x 8 once that
+//    grid has 8 CTAs per SM (bf16 2 x 4 there: 1.00 against 1.05 at 256 MiB).
+//  * p = 3..4: 4 x 2 (reduce-scatter p = 3 fp32 at 8 MiB 0.75 -> 0.88 and at
+//    16 MiB 0.84 -> 1.01 against 4 x 1, p = 4 0.94 -> 0.99; all-reduce p = 3
+//    bf16 at 8 MiB 0.88 -> 0.93), except the all-reduce at p = 4, which
+//    keeps 4 x 1 (0.93 against 0.87 at 8 MiB, 1.05 against 1.04 at 256 MiB).
+//  * p = 5..8: 8 x 1 at every size (57 registers, 4 CTAs per SM: the loads
+//    in flight per SM of 8 x 2 at 2 CTAs, in twice the CTAs): reduce-scatter
+//    fp32 p = 5 0.90 -> 1.03 at 256 MiB and 0.75 -> 0.95 at 8 MiB, p = 6
+//    0.82 -> 1.00 and p = 8 0.95 -> 1.09 at 8 MiB; all-reduce bf16 p = 5
+//    0.87 -> 0.93 at 8 MiB; 1 KiB calls 1.7-2.4 -> 1.3-1.9 us.  8 x 2 had
+//    replaced the general kernel for bf16 (all-reduce p = 6 0.92 -> 1.03,
+//    reduce-scatter p = 8 0.94 -> 1.07 at 256 MiB - 1 GiB).
+//  * The DDP bucket (fp32 in, 32-byte vectors of 8 accumulators): 2 x 4 at
+//    p <= 2 and 4 x 2 at p <= 4 once that grid has 8 CTAs per SM, else 2 x 2
+//    and 4 x 1; p > 4 stays on fold_kernel (8 ranks of 32-byte vectors
+//    would need twice the registers).
+// The general kernel ran 0.3-0.8 for p <= 4 at these sizes.
+FoldPlan fold_plan(int dt_in, int dt_out, int op, int mode, int p, uint64_t q, bool vec, int sms) {
   if (!vec || op != CCL_SUM || p < 1) return FoldPlan{0, 0};
   const int in_bytes = (dt_in == kBF16) ? 2 : 4;
   const int v = (dt_in == kF32 && dt_out == kBF16) ? 8 : 16 / in_bytes;  // vec_width
   const bool halve = v > 4;
   const uint64_t per_chunk = (q + 1 + v - 1) / v;
-  const uint64_t want_ctas = 8ull * static_cast<uint64_t>(sms > 0 ? sms : 1);
+  const uint64_t n_sms = static_cast<uint64_t>(sms > 0 ? sms : 1);
+  const uint64_t want_ctas = 8 * n_sms;
   auto ctas = [&](int u) {
     return (per_chunk + static_cast<uint64_t>(kThreads) * u - 1) / (static_cast<uint64_t>(kThreads) * u) *
            static_cast<uint64_t>(p);
   };
-  if (p <= 2) return ctas(halve ? 4 : 8) >= want_ctas ? FoldPlan{2, halve ? 4 : 8} : FoldPlan{2, 2};
-  if (p <= 4) return ctas(halve ? 2 : 4) >= want_ctas ? FoldPlan{4, halve ? 2 : 4} : FoldPlan{4, 1};
-  if (p <= 8 && (!halve || dt_in == kBF16)) return FoldPlan{8, 2};
+  if (mode == kModeBucket) {
+    if (p <= 2) return ctas(4) >= want_ctas ? FoldPlan{2, 4} : FoldPlan{2, 2};
+    if (p <= 4) return ctas(2) >= want_ctas ? FoldPlan{4, 2} : FoldPlan{4, 1};
+    return FoldPlan{0, 0};
+  }
+  const bool one_wave = ctas(1) <= 4 * n_sms;
+  if (p <= 2) {
+    if (mode == kModeAllReduce) return one_wave ? FoldPlan{2, 1} : FoldPlan{2, 2};
+    return (!halve && ctas(8) >= want_ctas) ? FoldPlan{2, 8} : FoldPlan{2, 2};
+  }
+  if (p <= 4) {
+    if (mode == kModeAllReduce && p == 4) return FoldPlan{4, 1};
+    return one_wave ? FoldPlan{4, 1} : FoldPlan{4, 2};
+  }
+  if (p <= 8) return FoldPlan{8, 1};
   return FoldPlan{0, 0};
 }
 

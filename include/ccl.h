@@ -122,17 +122,23 @@ ccl_status_t ccl_selftest_bounded_wait(void* stream);
 ccl_status_t ccl_chunk_bounds(int p, size_t n, int c, size_t* off, size_t* len);
 
 /* Diagnostic (no counterpart on the pages): which fused fold kernel a call of
- * p ranks x n elements launches.  bucket = 0 for ccl_allreduce,
- * ccl_reduce_scatter and ccl_reduce with element type dt and reduction op;
- * bucket = 1 for ccl_bucket_allreduce_scale_cast (dt must be CCL_F32, op
- * CCL_SUM).  aligned != 0: every pointer of the call is 16-byte aligned.
- * sm_count: the device's SM count, or <= 0 for the current device's.
- * Returns *batch = ranks whose loads one thread issues together and *vectors
- * = 16-byte vectors per thread of the small-p kernel, both 0 for the general
- * kernel (large p, MAX / MIN, unaligned buffers).  Host only; it enqueues
- * nothing.  Errors: p outside 1..CCL_MAX_RANKS, an unknown dt / op, a bucket
+ * p ranks x n elements launches.  kind: the call (ccl_allreduce,
+ * ccl_reduce_scatter, ccl_reduce with element type dt and reduction op, or
+ * ccl_bucket_allreduce_scale_cast, whose dt must be CCL_F32 and op CCL_SUM).
+ * aligned != 0: every pointer of the call is 16-byte aligned.  sm_count: the
+ * device's SM count, or <= 0 for the current device's.  Returns *batch =
+ * ranks whose loads one thread issues together and *vectors = 16-byte
+ * vectors per thread of the small-p kernel, both 0 for the general kernel
+ * (large p, MAX / MIN, unaligned buffers).  Host only; it enqueues nothing.
+ * Errors: p outside 1..CCL_MAX_RANKS, an unknown kind / dt / op, a bucket
  * plan for another dt / op, NULL outputs -> CCL_ERR_INVALID_ARG. */
-ccl_status_t ccl_fold_plan(int bucket, ccl_dtype_t dt, ccl_op_t op, int p, size_t n, int aligned,
+typedef enum {
+  CCL_FOLD_ALLREDUCE = 0,
+  CCL_FOLD_REDUCE_SCATTER = 1,
+  CCL_FOLD_BUCKET = 2,
+  CCL_FOLD_REDUCE = 3
+} ccl_fold_kind_t;
+ccl_status_t ccl_fold_plan(ccl_fold_kind_t kind, ccl_dtype_t dt, ccl_op_t op, int p, size_t n, int aligned,
                            int sm_count, int* batch, int* vectors);
 
 /* -------------------------------------------------- fused single-pass kernels

@@ -32,12 +32,12 @@ def _sizes():
     return sorted(out)
 
 
-def _reachable(lib, dtype, bucket):
+def _reachable(lib, dtype, kind):
     seen = set()
     for p in range(1, 17):
         for n in _sizes():
             for sms in SM_COUNTS:
-                seen.add(lib.ccl_fold_plan(p, n, dtype, "sum", bucket=bucket, sm_count=sms))
+                seen.add(lib.ccl_fold_plan(p, n, dtype, "sum", kind=kind, sm_count=sms))
     return seen
 
 
@@ -46,7 +46,7 @@ def test_every_reachable_fold_variant_has_a_gpu_case(kind):
     lib = _lib()
     dtypes = ("f32",) if kind == "bucket" else ("f32", "bf16", "i32")
     for dt in dtypes:
-        reach = _reachable(lib, dt, kind == "bucket")
+        reach = _reachable(lib, dt, kind)
         covered = {plan for (k, d, _, _, plan) in fold_variants.CASES if k == kind and d == dt}
         missing = reach - covered
         assert not missing, f"{kind} {dt}: variants {sorted(missing)} have no GPU parity case"
@@ -56,7 +56,7 @@ def test_every_reachable_fold_variant_has_a_gpu_case(kind):
 def test_gpu_cases_select_their_variant_on_a_152_sm_device(case):
     kind, dt, p, n, plan = case
     lib = _lib()
-    assert lib.ccl_fold_plan(p, n, dt, "sum", bucket=kind == "bucket", sm_count=152) == plan
+    assert lib.ccl_fold_plan(p, n, dt, "sum", kind=kind, sm_count=152) == plan
     assert n % p != 0 or p == 1, "cases keep ragged chunk edges"
 
 
@@ -76,6 +76,8 @@ def test_fold_plan_rejects_bad_arguments():
     with pytest.raises(lib.CclError):
         lib.ccl_fold_plan(129, 10)
     with pytest.raises(lib.CclError):
-        lib.ccl_fold_plan(4, 10, "bf16", bucket=True)
+        lib.ccl_fold_plan(4, 10, "bf16", kind="bucket")
     with pytest.raises(lib.CclError):
-        lib.ccl_fold_plan(4, 10, "f32", "max", bucket=True)
+        lib.ccl_fold_plan(4, 10, "f32", "max", kind="bucket")
+    with pytest.raises(ValueError):
+        lib.ccl_fold_plan(4, 10, "f32", kind="gather")
