@@ -161,28 +161,38 @@ template <int DT>
 cudaError_t launch_typed(bool vec, const GatherArgs& a, cudaStream_t s) {
   // 8 vectors (128 bytes) of loads in flight per thread before its p x 8
   // stores: at p = 16 that is 0.977 -> 1.022 of the copy bandwidth over 4
-  // vectors, 8 outrunning 2 and 4 and matching 32-byte stores.  Mid-size
-  // calls whose grid would be under 8 CTAs per SM take fewer vectors per
-  // thread, as the fold kernels do: 1 while that grid stays within 20 CTAs
-  // per SM (2.5 waves of this 32-register kernel), else 2.  Measured on
-  // GB300 (fp32, fraction of the copy bandwidth, 2 vectors -> 1): p = 2 at
-  // 4 / 8 MiB per rank 0.66 -> 0.72 / 0.75 -> 0.82, p = 8 at 4 / 8 MiB
-  // 0.64 -> 0.90 / 0.84 -> 0.88, p = 16 at 8 MiB 0.83 -> 0.91; at 16 MiB
-  // (about 3.4 waves with 1) 2 vectors stay ahead (p = 2: 0.94 against
-  // 0.91).  Before that rule, 2 vectors against 8: bf16 p = 16 at 8 / 16 MiB
-  // 0.74 -> 0.82 / 0.75 -> 0.98.  (The broadcast, tried the same way, went
-  // up at p = 4 and down at p = 16, and keeps 8.)
+  // vectors, 8 outrunning 2 and 4 and matching 32-byte stores.  Two
+  // exceptions, measured on GB300 (fraction of the copy bandwidth):
+  //  * Mid-size calls whose grid would be under 8 CTAs per SM take fewer
+  //    vectors per thread, as the fold kernels do: 1 while that grid stays
+  //    within 20 CTAs per SM (2.5 waves of this 32-register kernel), else 2
+  //    (2 vectors -> 1: p = 2 at 4 / 8 MiB per rank 0.66 -> 0.72 / 0.75 ->
+  //    0.82, p = 8 at 4 / 8 MiB 0.64 -> 0.90 / 0.84 -> 0.88; at 16 MiB p = 2
+  //    keeps 2, 0.94 against 0.91).  From p = 8 on, where every loaded
+  //    vector is stored 8 times or more, 1 at any mid size (16 MiB, 2
+  //    vectors -> 1: p = 8 0.91-0.93 -> 0.94, p = 16 0.93-0.95 -> 0.96,
+  //    p = 32 0.96 -> 0.99, p = 72 0.95 -> 1.00).
+  //  * From p = 8 on, blocks off the output vectors (the realigning kernel,
+  //    whose two granules per vector cost registers) take 1 vector at every
+  //    size: p = 72 at 64 / 256 MiB 0.98 / 0.98 -> 1.01 / 1.03, p = 48 0.98
+  //    / 0.96 -> 1.01 / 1.02 against 8.  Aligned blocks keep 8 (p = 32 at
+  //    64 MiB 1.06 against 0.99-1.01 with 1).
   if (!vec) return launch_one<DT, 1, 1>(a, s);
   constexpr int VEC = 16 / Elem<DT>::kBytes;
   const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC;
   const int sms = current_sm_count();
   const uint64_t sm_count = static_cast<uint64_t>(sms > 0 ? sms : 1);
   auto ctas = [&](uint64_t u) { return (per_chunk + kThreads * u - 1) / (kThreads * u) * static_cast<uint64_t>(a.p); };
-  if (ctas(8) < 8 * sm_count) {
-    if (ctas(1) <= 20 * sm_count) return launch_one<DT, VEC, 1>(a, s);
-    return launch_one<DT, VEC, 2>(a, s);
+  const bool many = a.p >= 8;
+  if (ctas(8) >= 8 * sm_count) {
+    bool realign = false;  // some block starts inside a vector of the outputs
+    for (uint64_t k = 0; k < static_cast<uint64_t>(a.p) && !realign; ++k)
+      realign = (k * a.q + (k < a.rem ? k : a.rem)) % VEC != 0;  // off(k), the chunk rule
+    if (many && realign) return launch_one<DT, VEC, 1>(a, s);
+    return launch_one<DT, VEC, 8>(a, s);
   }
-  return launch_one<DT, VEC, 8>(a, s);
+  if (many || ctas(1) <= 20 * sm_count) return launch_one<DT, VEC, 1>(a, s);
+  return launch_one<DT, VEC, 2>(a, s);
 }
 
 // Broadcast: one 1-D pass over the root's buffer (send[0]); each of a

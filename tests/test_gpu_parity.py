@@ -128,12 +128,13 @@ def test_all_gather_matches_oracle(lib, dtype, p, n):
         assert outs[r].guards_intact()
 
 
-# vectors per thread of the all-gather (the host picks them by grid size):
-# mid-size calls take 1 (grids up to 20 CTAs per SM) or 2, larger ones 8;
-# blocks on the 16-byte grid or off it (p = 72, p = 3)
+# vectors per thread of the all-gather (the host picks them by grid size
+# and p): mid-size calls take 1 (grids up to 20 CTAs per SM, or p >= 8) or 2,
+# larger ones 8, or 1 from p = 8 on when blocks are off the output vectors;
+# blocks on the 16-byte grid or off it (p = 72, p = 8, p = 3)
 AG_SIZE_CLASSES = [("f32", 2, 2 * 1048576), ("bf16", 8, 8 * 262144 + 8), ("bf16", 72, 72 * 41000 + 5),
                    ("f32", 2, 4 * 1048576), ("bf16", 3, 3 * 4194304 + 1), ("f32", 2, 16 * 1048576 + 4),
-                   ("f32", 3, 3 * 3400000 + 1)]
+                   ("f32", 3, 3 * 3400000 + 1), ("f32", 8, 8 * 2097152 + 3), ("bf16", 16, 16 * 1048576 + 16)]
 
 
 @pytest.mark.parametrize("dtype,p,n", AG_SIZE_CLASSES)
