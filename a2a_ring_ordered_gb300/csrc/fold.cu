@@ -34,12 +34,13 @@ __host__ __device__ constexpr int vec_width() {
 __host__ __device__ constexpr int words_for(int vec, int bytes) { return (vec * bytes + 3) / 4; }
 
 // Fold VEC elements starting at element i, in ring order from rank `first`.
-template <int DT_IN, int VEC, int OP>
+// BATCH_IN: ranks whose loads are issued together before any of them is
+// folded (0: 16, or 8 for 32-byte vectors).
+template <int DT_IN, int VEC, int OP, int BATCH_IN = 0>
 __device__ __forceinline__ void fold_elements(const FoldArgs& a, int p, int first, uint64_t i,
                                               typename Elem<DT_IN>::Acc* acc) {
   constexpr int WI = words_for(VEC, Elem<DT_IN>::kBytes);
-  // ranks whose loads are issued together before any of them is folded
-  constexpr int BATCH = (WI >= 8) ? 8 : 16;
+  constexpr int BATCH = BATCH_IN > 0 ? BATCH_IN : ((WI >= 8) ? 8 : 16);
   int r = first;
   for (int j0 = 0; j0 < p; j0 += BATCH) {
     uint32_t raw[BATCH][WI];
@@ -94,7 +95,7 @@ __device__ __forceinline__ void emit(const FoldArgs& a, int p, int c, const Chun
 // off the vector grid; the host picks it only when some chunk is, so that
 // the aligned kernel keeps its registers (128 against 109 for bf16, which
 // cost the p = 16 reduce-scatter 1 %).
-template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE, bool REALIGN>
+template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE, bool REALIGN, int BATCH = 0>
 __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ FoldArgs a) {
   using Acc = typename Elem<DT_IN>::Acc;
   const int p = a.p;
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ 
          vb += stride) {
       const uint64_t v = vb + lane;
       Acc acc[VEC] = {};
-      if (v < v_hi) fold_elements<DT_IN, VEC, OP>(a, p, first, v * VEC, acc);
+      if (v < v_hi) fold_elements<DT_IN, VEC, OP, BATCH>(a, p, first, v * VEC, acc);
       uint32_t w[words_for(VEC, Elem<DT_OUT>::kBytes)];
       pack_out<DT_OUT, VEC>(acc, w);
       if constexpr (VEC * Elem<DT_OUT>::kBytes == 16)
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ 
          v += stride) {
       if (v < v_lo) continue;
       Acc acc[VEC];
-      fold_elements<DT_IN, VEC, OP>(a, p, first, v * VEC, acc);
+      fold_elements<DT_IN, VEC, OP, BATCH>(a, p, first, v * VEC, acc);
       emit<DT_OUT, VEC, MODE>(a, p, c, ch, v * VEC, acc);
     }
   }
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const __grid_constant__ 
     for (uint64_t t = threadIdx.x; t < n_edge; t += kThreads) {
       const uint64_t i = (t < n_head) ? ch.off + t : tail_begin + (t - n_head);
       Acc acc[1];
-      fold_elements<DT_IN, 1, OP>(a, p, first, i, acc);
+      fold_elements<DT_IN, 1, OP, BATCH>(a, p, first, i, acc);
       emit<DT_OUT, 1, MODE>(a, p, c, ch, i, acc);
     }
   }
@@ -294,6 +295,20 @@ constexpr int kVectorsPerThread = 2;
 // p = 72 at 256 KiB 0.36 -> 0.47; taking one vector also when its grid
 // spills into a second wave lost at 2 MiB (reduce-scatter p = 72 0.97 ->
 // 0.88).
+//
+// The reduce-scatter with 9..32 ranks and chunks of 128 KiB or more loads 8
+// ranks per batch instead of 16 (about 60 registers instead of 91-107: 4
+// CTAs per SM instead of 2, each thread two dependent rounds of loads).
+// Measured on GB300 against 16 (fraction of the copy bandwidth): p = 9 bf16
+// at 8 / 64 / 256 MiB per rank 0.73 / 0.84 / 0.87 -> 0.85 / 0.98 / 0.98,
+// p = 12 fp32 0.79 / 0.84 / 0.84 -> 0.91 / 1.02 / 1.03, p = 24 bf16 0.86 /
+// 0.94 / 0.94 -> 0.99 / 1.05 / 1.04; p = 16 at 8 MiB 0.98 / 0.93 -> 1.08 /
+// 1.07 (fp32 / bf16), p = 32 at 4 MiB 1.03 / 0.97 -> 1.06 / 1.05.  Smaller
+// chunks lost (p = 16 at 1 MiB 0.83 -> 0.62: the second round of loads is
+// latency there), p = 72 came out even, and the all-reduce, which stores
+// every vector p times, lost 1-2 % at p = 16 - 72.
+constexpr uint64_t kBatch8MinChunkBytes = 128 * 1024;
+
 template <int DT_IN, int DT_OUT, int VEC, int OP, int MODE>
 cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
   auto kernel = fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, false>;
@@ -301,7 +316,14 @@ cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
     bool realign = false;  // some chunk starts off the vector grid (off(c), the chunk rule)
     for (uint64_t c = 0; c < static_cast<uint64_t>(a.p) && !realign; ++c)
       realign = (c * a.q + (c < a.rem ? c : a.rem)) % VEC != 0;
-    if (realign) kernel = fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, true>;
+    constexpr bool kWide = words_for(VEC, Elem<DT_IN>::kBytes) >= 8;  // 32-byte vectors batch 8 already
+    const bool batch8 = !kWide && a.p >= 9 && a.p <= 32 && a.q * Elem<DT_IN>::kBytes >= kBatch8MinChunkBytes;
+    if (batch8) {
+      kernel = realign ? fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, true, 8>
+                       : fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, false, 8>;
+    } else if (realign) {
+      kernel = fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, true>;
+    }
   }
   const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC + 31;  // + the lanes before v_lo
   auto grid_x = [&](uint64_t vpt) { return (per_chunk + kThreads * vpt - 1) / (kThreads * vpt); };

@@ -145,6 +145,29 @@ def test_all_gather_size_classes_match_oracle(lib, dtype, p, n):
     test_all_gather_matches_oracle(lib, dtype, p, n)
 
 
+# the reduce-scatter with 9..32 ranks and chunks of at least 128 KiB loads 8
+# ranks per batch (the general kernel otherwise 16): chunks off the vector
+# grid (p = 9, 32) and on it (p = 16), every op, and the boundaries of the
+# rule (p = 8 and 33 keep their kernels)
+RS_BATCH8 = [(dt, op, 9, 9 * 40000 + 5) for dt in ("f32", "bf16", "i32") for op in ("sum", "max", "min")]
+RS_BATCH8 += [(dt, "sum", p, n) for dt in ("f32", "bf16", "i32")
+              for p, n in ((16, 16 * 65536), (32, 32 * 40000 + 17), (33, 33 * 40000 + 1))]
+
+
+@pytest.mark.parametrize("dtype,op,p,n", RS_BATCH8)
+def test_reduce_scatter_eight_rank_batches_match_oracle(lib, dtype, op, p, n):
+    """Every element of every shard against the literal ring reduce-scatter,
+    guard bands around each shard."""
+    x = make_inputs(dtype, p, n, seed=p * 31 + n % 1000)
+    want, _ = ring.ring_reduce_scatter(x, dtype, op)
+    send = [to_dev(v, dtype) for v in x]
+    shards = guarded_outputs(p, [ln for _, ln in ring.chunk_bounds(p, n)], dtype)
+    lib.ccl_reduce_scatter(send, [s.view for s in shards], op=op)
+    for k in range(p):
+        assert_equal(to_host(shards[k].view), want[k], dtype, f"RS {dtype} {op} p={p} n={n} rank {k}")
+        assert shards[k].guards_intact()
+
+
 # -------------------------------------------- alignment and in-place forms
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("p,n", [(4, 1027), (8, 4096), (3, 50001)])
