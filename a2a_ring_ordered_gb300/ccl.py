@@ -33,6 +33,12 @@ _DTYPES = {torch.float32: CCL_F32, torch.bfloat16: CCL_BF16, torch.int32: CCL_I3
 _OPS = {"sum": CCL_SUM, "max": CCL_MAX, "min": CCL_MIN}
 
 
+class A2APlan(ctypes.Structure):
+    """ccl_a2a_plan_t."""
+    _fields_ = [("form", ctypes.c_int), ("shift", ctypes.c_int), ("stage", ctypes.c_int),
+                ("launches", ctypes.c_int), ("tile_bytes", ctypes.c_uint)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -66,6 +72,8 @@ def _load() -> ctypes.CDLL:
         "ccl_gather": (st, [pp, vp, i32, sz, i32, i32, vp]),
         "ccl_bucket_allreduce_scale_cast": (st, [pp, pp, i32, sz, ctypes.c_float, vp]),
         "ccl_all_to_allv": (st, [pp, ctypes.POINTER(sz), pp, i32, sz, i32, vp]),
+        "ccl_all_to_all_plan": (st, [pp, pp, i32, sz, i32, i32, ctypes.POINTER(A2APlan)]),
+        "ccl_all_to_allv_plan": (st, [pp, ctypes.POINTER(sz), pp, i32, sz, i32, i32, ctypes.POINTER(A2APlan)]),
         "ccl_ring_literal_workspace_bytes": (sz, [i32, i32, sz, i32]),
         "ccl_moe_route": (st, [pp, i32, sz, i32, i32, vp, pp, vp]),
         "ccl_all_to_all_heads": (st, [pp, pp, i32, sz, sz, sz, i32, i32, vp]),
@@ -447,6 +455,41 @@ def ccl_all_to_allv(send, counts, recv, row_elems: int, stream=None) -> None:
                                _ptr_array([t.data_ptr() for t in recv]), p, row_elems,
                                _dtype_code(send[0]), _stream(stream, send[0].device)),
            "ccl_all_to_allv")
+
+
+A2A_FORMS = ("small", "plain", "table32", "table64")  # ccl_a2a_form_t
+
+
+def _addresses(bufs) -> list[int]:
+    return [b if isinstance(b, int) else b.data_ptr() for b in bufs]
+
+
+def _plan_tuple(pl) -> tuple:
+    return (A2A_FORMS[pl.form], bool(pl.shift), bool(pl.stage), pl.launches, pl.tile_bytes)
+
+
+def ccl_all_to_all_plan(send, recv, n: int, dtype: str = "f32", sm_count: int = 0) -> tuple:
+    """(form, shift, stage, launches, tile_bytes) of the kernel ccl_all_to_all
+    launches for these buffers (tensors, or their addresses as ints: only the
+    addresses matter) with n elements per rank; sm_count <= 0 asks the
+    current device."""
+    codes = {"f32": CCL_F32, "bf16": CCL_BF16, "i32": CCL_I32}
+    pl = A2APlan()
+    _check(LIB.ccl_all_to_all_plan(_ptr_array(_addresses(send)), _ptr_array(_addresses(recv)), len(send), n,
+                                   codes[dtype], sm_count, ctypes.byref(pl)), "ccl_all_to_all_plan")
+    return _plan_tuple(pl)
+
+
+def ccl_all_to_allv_plan(send, counts, recv, row_elems: int, dtype: str = "f32", sm_count: int = 0) -> tuple:
+    """(form, shift, stage, launches, tile_bytes) of the kernel ccl_all_to_allv
+    launches for these buffers (tensors or addresses) and counts."""
+    codes = {"f32": CCL_F32, "bf16": CCL_BF16, "i32": CCL_I32}
+    p = len(send)
+    flat = (ctypes.c_size_t * (p * p))(*[int(counts[s][d]) for s in range(p) for d in range(p)])
+    pl = A2APlan()
+    _check(LIB.ccl_all_to_allv_plan(_ptr_array(_addresses(send)), flat, _ptr_array(_addresses(recv)), p,
+                                    row_elems, codes[dtype], sm_count, ctypes.byref(pl)), "ccl_all_to_allv_plan")
+    return _plan_tuple(pl)
 
 
 # ------------------------------------------------------- literal ring engine

@@ -19,16 +19,18 @@
 //  * a unit inside one block is one aligned 16-byte source load when source
 //    and destination share the 16-byte phase, else two aligned source
 //    granules whose bytes are funnel-shifted into place;
-//  * a unit that straddles blocks (small blocks, block edges off the
-//    16-byte grid) goes through the tile's small-block stage: before the
-//    aligned units, the whole CTA issues asynchronous copies of the
-//    elements of all such units at once (each element's aligned source
-//    word, from the block holding it) into shared memory; after them, each
-//    unit is assembled from the stage and stored whole.  A unit not inside
+//  * a unit that straddles blocks (block edges off the 16-byte grid) is
+//    assembled from its elements and stored whole.  When blocks are small
+//    (the host's choice: STAGE) this goes through the tile's small-block
+//    stage: before the aligned units, the whole CTA issues asynchronous
+//    copies of the elements of all such units at once (each element's
+//    aligned source word, from the block holding it) into shared memory;
+//    after them, each unit is assembled from the stage.  A unit not inside
 //    one block holds one of the destination's p + 1 block edges, so the
-//    stage holds at most p + 1 units;
+//    stage holds at most p + 1 units.  With large blocks a tile holds one
+//    such unit or none, and the thread that meets it loads its elements;
 //  * only the units at the ends of the destination buffer, partly outside
-//    it, are stored element by element (from the stage).
+//    it, are stored element by element.
 // Every load touches only aligned granules (16 bytes, or the 4-byte words
 // of the stage) that hold at least one byte of a block.  HBM traffic: one
 // read and one write of every moved byte.

@@ -965,7 +965,7 @@ namespace {
 // 16 KiB 9.05 -> 4.49 us; with the 4 KB grid past one wave it lost (p = 8
 // at 1 MiB, 2,048 CTAs: 3.9 -> 8.6 us).
 template <class P>
-uint64_t fill_tiles(P& a, void* const* recv, const uint64_t* out_bytes) {
+uint64_t fill_tiles(P& a, void* const* recv, const uint64_t* out_bytes, int sms) {
   auto fill = [&](uint64_t tile) {
     a.tile_bytes = static_cast<uint32_t>(tile);
     uint64_t total = 0;
@@ -976,11 +976,17 @@ uint64_t fill_tiles(P& a, void* const* recv, const uint64_t* out_bytes) {
     a.tile0[a.ndest] = total;
     return total;
   };
-  const int sms = current_sm_count();
   if (fill(kA2ASmallTileBytes) <= 4ull * static_cast<uint64_t>(sms > 0 ? sms : 1))
     return a.tile0[a.ndest];
   return fill(kA2ATileBytes);
 }
+
+// What an all-to-all(v) call launches (ccl_a2a_plan_t): filled instead of
+// launching when a plan is asked for.
+struct A2APlanOut {
+  int form = 0, shift = 0, stage = 0, launches = 0;
+  uint32_t tile_bytes = 0;
+};
 
 template <class P>
 void fill_pointers(P& a, const void* const* send, void* const* recv, int p) {
@@ -995,7 +1001,7 @@ void fill_pointers(P& a, const void* const* send, void* const* recv, int p) {
 template <class P>
 ccl_status_t a2a_table_launches(P& a, const void* const* send, void* const* recv, const size_t* counts,
                                 int p, uint64_t row_bytes, size_t e, const uint64_t* out_bytes,
-                                bool shift, bool stage, cudaStream_t s) {
+                                bool shift, bool stage, cudaStream_t s, int sms, A2APlanOut* plan) {
   const int per_launch = P::kTableCap / p - 1;
   for (int j0 = 0; j0 < p; j0 += per_launch) {
     memset(static_cast<void*>(&a), 0, sizeof(a));
@@ -1015,7 +1021,11 @@ ccl_status_t a2a_table_launches(P& a, const void* const* send, void* const* recv
         if (j0 + c < p) rows += counts[static_cast<size_t>(i) * p + j0 + c];
       }
     }
-    if (fill_tiles(a, recv, out_bytes) == 0) continue;
+    if (fill_tiles(a, recv, out_bytes, sms) == 0) continue;
+    if (plan != nullptr) {
+      if (plan->launches++ == 0) plan->tile_bytes = a.tile_bytes;
+      continue;
+    }
     cudaError_t err = launch_a2a(a, shift, stage, s);
     if (err != cudaSuccess) return cuda_fail(err, "all-to-all kernel launch");
   }
@@ -1023,7 +1033,8 @@ ccl_status_t a2a_table_launches(P& a, const void* const* send, void* const* recv
 }
 
 ccl_status_t a2a_table(const void* const* send, const size_t* counts, void* const* recv, int p,
-                       uint64_t row_bytes, size_t e, const uint64_t* in_rows, cudaStream_t s) {
+                       uint64_t row_bytes, size_t e, const uint64_t* in_rows, cudaStream_t s, int sms,
+                       A2APlanOut* plan) {
   uint64_t out_bytes[CCL_MAX_RANKS] = {0};
   uint64_t max_rows = 0;
   for (int i = 0; i < p; ++i) {
@@ -1064,18 +1075,43 @@ ccl_status_t a2a_table(const void* const* send, const size_t* counts, void* cons
     total += out_bytes[d];
   }
   const bool stage = off_grid && total <= kA2AStageMaxBlockBytes * blocks;
+  if (plan != nullptr) {
+    plan->shift = shift;
+    plan->stage = stage;
+  }
   // uint32 table entries hold every row prefix only while each source has
   // fewer than 2^32 rows
   if (max_rows >= (1ull << 32)) {
     static thread_local A2ATable64 a;  // 32 KB: kept off the stack
-    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, stage, s);
+    if (plan != nullptr) plan->form = CCL_A2A_TABLE64;
+    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, stage, s, sms, plan);
   }
   if (p <= A2ASmall::kCap) {
     static thread_local A2ASmall a;
-    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, stage, s);
+    if (plan != nullptr) plan->form = CCL_A2A_SMALL;
+    return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, stage, s, sms, plan);
   }
   static thread_local A2ATable32 a;
-  return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, stage, s);
+  if (plan != nullptr) plan->form = CCL_A2A_TABLE32;
+  return a2a_table_launches(a, send, recv, counts, p, row_bytes, e, out_bytes, shift, stage, s, sms, plan);
+}
+
+// Rows each rank sends and receives, with the size checks of an
+// all-to-allv (CCL_OK, or the failure already recorded).
+ccl_status_t a2av_rows(const size_t* counts, int p, uint64_t row_bytes, uint64_t* in_rows, uint64_t* out_rows) {
+  for (int r = 0; r < p; ++r) in_rows[r] = out_rows[r] = 0;
+  for (int s = 0; s < p; ++s) {
+    for (int d = 0; d < p; ++d) {
+      const uint64_t c = counts[s * p + d];
+      if (c > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "counts[%d][%d] too large", s, d);
+      in_rows[s] += c;
+      out_rows[d] += c;
+    }
+  }
+  for (int r = 0; r < p; ++r)
+    if (row_bytes != 0 && (in_rows[r] > kMaxElems / row_bytes || out_rows[r] > kMaxElems / row_bytes))
+      return fail(CCL_ERR_INVALID_ARG, "rank %d buffer too large", r);
+  return CCL_OK;
 }
 
 }  // namespace
@@ -1093,20 +1129,11 @@ extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* c
     return fail(CCL_ERR_INVALID_ARG, "send, recv or counts is NULL");
   if (row_elems > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "row_elems=%zu too large", row_elems);
   const uint64_t row_bytes = row_elems * e;
-  uint64_t in_rows[CCL_MAX_RANKS] = {0}, out_rows[CCL_MAX_RANKS] = {0};
-  for (int s = 0; s < p; ++s) {
-    for (int d = 0; d < p; ++d) {
-      const uint64_t c = counts[s * p + d];
-      if (c > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "counts[%d][%d] too large", s, d);
-      in_rows[s] += c;
-      out_rows[d] += c;
-    }
-  }
+  uint64_t in_rows[CCL_MAX_RANKS], out_rows[CCL_MAX_RANKS];
+  if ((st = a2av_rows(counts, p, row_bytes, in_rows, out_rows)) != CCL_OK) return st;
   uint64_t in_bytes[CCL_MAX_RANKS], out_bytes[CCL_MAX_RANKS];
   Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
   for (int r = 0; r < p; ++r) {
-    if (row_bytes != 0 && (in_rows[r] > kMaxElems / row_bytes || out_rows[r] > kMaxElems / row_bytes))
-      return fail(CCL_ERR_INVALID_ARG, "rank %d buffer too large", r);
     in_bytes[r] = in_rows[r] * row_bytes;
     out_bytes[r] = out_rows[r] * row_bytes;
     in[r] = span(send[r], in_bytes[r]);
@@ -1117,34 +1144,21 @@ extern "C" ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* c
   if ((st = check_aliasing(in, out, nullptr, p)) != CCL_OK) return st;
   if (row_bytes == 0) return CCL_OK;
 
-  return a2a_table(send, counts, recv, p, row_bytes, e, in_rows, as_stream(stream));
+  return a2a_table(send, counts, recv, p, row_bytes, e, in_rows, as_stream(stream), current_sm_count(), nullptr);
 }
 
-extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* recv, int p, size_t n,
-                                       ccl_dtype_t dt, void* stream) {
-  CCL_TRACE();
-  clear_error();
-  ccl_status_t st = check_p(p);
-  if (st != CCL_OK) return st;
-  const size_t e = elem_bytes(dt);
-  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
-  if (send == nullptr || recv == nullptr) return fail(CCL_ERR_INVALID_ARG, "send or recv is NULL");
-  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
-  // block d of every source is chunk d (the chunk rule): destination d
-  // receives p blocks of len(d) elements in source order
-  uint64_t in_bytes[CCL_MAX_RANKS], out_bytes[CCL_MAX_RANKS], off[CCL_MAX_RANKS], len[CCL_MAX_RANKS];
-  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+namespace {
+
+// The plain all-to-all of n elements per rank (block d of every source is
+// chunk d, the chunk rule): its kernel choice, and its launch unless a plan
+// is asked for.
+ccl_status_t a2a_plain(const void* const* send, void* const* recv, int p, uint64_t n, size_t e,
+                       cudaStream_t s, int sms, A2APlanOut* plan) {
+  uint64_t out_bytes[CCL_MAX_RANKS], off[CCL_MAX_RANKS], len[CCL_MAX_RANKS];
   for (int r = 0; r < p; ++r) {
     chunk(p, n, r, &off[r], &len[r]);
-    in_bytes[r] = n * e;
     out_bytes[r] = static_cast<uint64_t>(p) * len[r] * e;
-    in[r] = span(send[r], in_bytes[r]);
-    out[r] = span(recv[r], out_bytes[r]);
   }
-  if ((st = check_buffers("send", send, p, in_bytes, e)) != CCL_OK) return st;
-  if ((st = check_buffers("recv", const_cast<const void* const*>(recv), p, out_bytes, e)) != CCL_OK) return st;
-  if ((st = check_aliasing(in, out, nullptr, p)) != CCL_OK) return st;
-  if (n == 0) return CCL_OK;
   bool shift = false;  // some block's source and destination differ in 16-byte phase
   for (int d = 0; d < p && !shift; ++d) {
     if (len[d] == 0) continue;
@@ -1163,6 +1177,11 @@ extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* rec
       off_grid = ((reinterpret_cast<uintptr_t>(recv[d]) + static_cast<uint64_t>(i) * len[d] * e) & 15) != 0;
   }
   const bool stage = off_grid && n * e <= kA2AStageMaxBlockBytes * static_cast<uint64_t>(p);
+  if (plan != nullptr) {
+    plan->form = p <= A2ASmall::kCap ? CCL_A2A_SMALL : CCL_A2A_PLAIN;
+    plan->shift = shift;
+    plan->stage = stage;
+  }
   auto fill = [&](auto& a) -> ccl_status_t {
     memset(static_cast<void*>(&a), 0, sizeof(a));
     fill_pointers(a, send, recv, p);
@@ -1174,8 +1193,13 @@ extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* rec
     a.elem = static_cast<int>(e);
     a.q = n / static_cast<uint64_t>(p);
     a.rem = n % static_cast<uint64_t>(p);
-    if (fill_tiles(a, recv, out_bytes) == 0) return CCL_OK;
-    cudaError_t err = launch_a2a(a, shift, stage, as_stream(stream));
+    if (fill_tiles(a, recv, out_bytes, sms) == 0) return CCL_OK;
+    if (plan != nullptr) {
+      plan->launches = 1;
+      plan->tile_bytes = a.tile_bytes;
+      return CCL_OK;
+    }
+    cudaError_t err = launch_a2a(a, shift, stage, s);
     if (err != cudaSuccess) return cuda_fail(err, "all-to-all kernel launch");
     return CCL_OK;
   };
@@ -1185,6 +1209,86 @@ extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* rec
   }
   A2APlain a;
   return fill(a);
+}
+
+ccl_status_t put_plan(const A2APlanOut& pl, ccl_a2a_plan_t* plan) {
+  plan->form = static_cast<ccl_a2a_form_t>(pl.form);
+  plan->shift = pl.shift;
+  plan->stage = pl.stage;
+  plan->launches = pl.launches;
+  plan->tile_bytes = pl.tile_bytes;
+  return CCL_OK;
+}
+
+}  // namespace
+
+extern "C" ccl_status_t ccl_all_to_all(const void* const* send, void* const* recv, int p, size_t n,
+                                       ccl_dtype_t dt, void* stream) {
+  CCL_TRACE();
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (send == nullptr || recv == nullptr) return fail(CCL_ERR_INVALID_ARG, "send or recv is NULL");
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  // destination d receives p blocks of len(d) elements in source order
+  uint64_t in_bytes[CCL_MAX_RANKS], out_bytes[CCL_MAX_RANKS];
+  Span in[CCL_MAX_RANKS], out[CCL_MAX_RANKS];
+  for (int r = 0; r < p; ++r) {
+    uint64_t off, len;
+    chunk(p, n, r, &off, &len);
+    in_bytes[r] = n * e;
+    out_bytes[r] = static_cast<uint64_t>(p) * len * e;
+    in[r] = span(send[r], in_bytes[r]);
+    out[r] = span(recv[r], out_bytes[r]);
+  }
+  if ((st = check_buffers("send", send, p, in_bytes, e)) != CCL_OK) return st;
+  if ((st = check_buffers("recv", const_cast<const void* const*>(recv), p, out_bytes, e)) != CCL_OK) return st;
+  if ((st = check_aliasing(in, out, nullptr, p)) != CCL_OK) return st;
+  if (n == 0) return CCL_OK;
+  return a2a_plain(send, recv, p, n, e, as_stream(stream), current_sm_count(), nullptr);
+}
+
+extern "C" ccl_status_t ccl_all_to_all_plan(const void* const* send, void* const* recv, int p, size_t n,
+                                            ccl_dtype_t dt, int sm_count, ccl_a2a_plan_t* plan) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (send == nullptr || recv == nullptr || plan == nullptr)
+    return fail(CCL_ERR_INVALID_ARG, "send, recv or plan is NULL");
+  if (n > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
+  A2APlanOut pl;
+  if (n != 0) {
+    st = a2a_plain(send, recv, p, n, e, nullptr, sm_count > 0 ? sm_count : current_sm_count(), &pl);
+    if (st != CCL_OK) return st;
+  }
+  return put_plan(pl, plan);
+}
+
+extern "C" ccl_status_t ccl_all_to_allv_plan(const void* const* send, const size_t* counts, void* const* recv,
+                                             int p, size_t row_elems, ccl_dtype_t dt, int sm_count,
+                                             ccl_a2a_plan_t* plan) {
+  clear_error();
+  ccl_status_t st = check_p(p);
+  if (st != CCL_OK) return st;
+  const size_t e = elem_bytes(dt);
+  if (e == 0) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", dt);
+  if (send == nullptr || recv == nullptr || counts == nullptr || plan == nullptr)
+    return fail(CCL_ERR_INVALID_ARG, "send, recv, counts or plan is NULL");
+  if (row_elems > kMaxElems) return fail(CCL_ERR_INVALID_ARG, "row_elems=%zu too large", row_elems);
+  const uint64_t row_bytes = row_elems * e;
+  uint64_t in_rows[CCL_MAX_RANKS], out_rows[CCL_MAX_RANKS];
+  if ((st = a2av_rows(counts, p, row_bytes, in_rows, out_rows)) != CCL_OK) return st;
+  A2APlanOut pl;
+  if (row_bytes != 0) {
+    st = a2a_table(send, counts, recv, p, row_bytes, e, in_rows, nullptr,
+                   sm_count > 0 ? sm_count : current_sm_count(), &pl);
+    if (st != CCL_OK) return st;
+  }
+  return put_plan(pl, plan);
 }
 
 // ====================================================== literal ring engine

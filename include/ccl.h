@@ -284,6 +284,35 @@ ccl_status_t ccl_all_to_all(const void* const* send, void* const* recv, int p, s
 ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts, void* const* recv,
                              int p, size_t row_elems, ccl_dtype_t dt, void* stream);
 
+/* Diagnostic (no counterpart on the pages): which all-to-all kernel a call
+ * of ccl_all_to_all / ccl_all_to_allv with the same arguments launches.
+ * The pointers are only read as addresses (their 16-byte phases decide);
+ * nothing is dereferenced, checked against the device or enqueued.
+ * sm_count: the device's SM count, or <= 0 for the current device's.
+ *   form        where the block bounds come from: CCL_A2A_SMALL (p <= 16,
+ *               4 KB parameter block), CCL_A2A_PLAIN (the chunk rule, p > 16),
+ *               CCL_A2A_TABLE32 / CCL_A2A_TABLE64 (row-prefix tables of
+ *               32- / 64-bit entries, p > 16 or a source of 2^32 rows or more)
+ *   shift       some block's source and destination differ in 16-byte phase
+ *   stage       the units that straddle blocks go through the small-block
+ *               stage in shared memory
+ *   launches    kernel launches of the call (0: nothing to move)
+ *   tile_bytes  destination tile of the first launch (4096 or 32768)
+ * Errors: as the call's own argument checks (p, dt, NULL pointers, sizes)
+ * -> CCL_ERR_INVALID_ARG. */
+typedef enum { CCL_A2A_SMALL = 0, CCL_A2A_PLAIN = 1, CCL_A2A_TABLE32 = 2, CCL_A2A_TABLE64 = 3 } ccl_a2a_form_t;
+typedef struct {
+  ccl_a2a_form_t form;
+  int shift;
+  int stage;
+  int launches;
+  unsigned tile_bytes;
+} ccl_a2a_plan_t;
+ccl_status_t ccl_all_to_all_plan(const void* const* send, void* const* recv, int p, size_t n, ccl_dtype_t dt,
+                                 int sm_count, ccl_a2a_plan_t* plan);
+ccl_status_t ccl_all_to_allv_plan(const void* const* send, const size_t* counts, void* const* recv, int p,
+                                  size_t row_elems, ccl_dtype_t dt, int sm_count, ccl_a2a_plan_t* plan);
+
 /* DDP gradient bucketing ("dist_train", Communication-Computation Overlap:
  * with bucket_cap_mb = 25 the gradients are cut into buckets in the order
  * backprop produces them, and a bucket is all-reduced as soon as all of its
