@@ -284,6 +284,82 @@ cudaError_t launch_unrolled(const FoldArgs& a, cudaStream_t s) {
                        dim3(kThreads), s, a);
 }
 
+// Small chunks at large p: a CTA loads all p ranks' elements of a segment
+// of chunk c at once (one round of loads, whatever p is) into shared
+// memory, folds each element there in ring order from rank c + 1 (the same
+// operations in the same order as fold_elements) and stores the results
+// with all its threads.  The vector kernels load 16 ranks per round, p / 16
+// dependent rounds.  Segments hold kSmallMaxItems / p elements; grid x =
+// segments, grid y = chunks.
+constexpr int kSmallMaxItems = 4096;  // p x segment held in shared memory
+constexpr int kSmallMaxLen = 256;     // chunks this kernel takes
+
+template <int DT_IN, int DT_OUT, int OP, int MODE>
+__global__ void __launch_bounds__(kThreads) fold_small_kernel(const __grid_constant__ FoldArgs a) {
+  using Acc = typename Elem<DT_IN>::Acc;
+  __shared__ Acc s_in[kSmallMaxItems];  // ring position j, element e at j * len + e
+  __shared__ Acc s_out[kSmallMaxItems / 17 + 1];
+  const int p = a.p;
+  const int c = blockIdx.y;
+  const Chunk ch = chunk_of(c, a.q, a.rem);
+  const int seg = kSmallMaxItems / p;
+  const int e0 = static_cast<int>(blockIdx.x) * seg;
+  const int len = static_cast<int>(ch.len) - e0 < seg ? static_cast<int>(ch.len) - e0 : seg;
+  const uint64_t off = ch.off + static_cast<uint64_t>(e0);
+  const int first = (c + 1 == p) ? 0 : c + 1;
+  pdl_enter();
+  if (len <= 0) return;  // (uniform over the CTA)
+  for (int t = threadIdx.x; t < p * len; t += kThreads) {
+    const int j = t / len, e = t - j * len;
+    const int r = first + j < p ? first + j : first + j - p;
+    uint32_t w[1];
+    load_raw<DT_IN, 1>(a.send[r], off + static_cast<uint64_t>(e), w);
+    s_in[t] = widen<DT_IN>(w, 0);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < len; e += kThreads) {
+    Acc acc = s_in[e];
+    for (int j = 1; j < p; ++j) acc = combine<OP>(acc, s_in[j * len + e]);
+    if constexpr (MODE == kModeBucket) acc = __fmul_rn(acc, a.scale);
+    s_out[e] = acc;
+  }
+  __syncthreads();
+  const int outputs = (MODE == kModeAllReduce || MODE == kModeBucket) ? p : 1;
+  for (int t = threadIdx.x; t < outputs * len; t += kThreads) {
+    const int r = t / len, e = t - r * len;
+    Acc v = s_out[e];
+    uint32_t w[1];
+    pack_out<DT_OUT, 1>(&v, w);
+    if constexpr (MODE == kModeReduceScatter) {
+      store_raw<DT_OUT, 1>(a.recv[c], static_cast<uint64_t>(e0 + e), w);
+    } else if constexpr (MODE == kModeReduce) {
+      store_raw<DT_OUT, 1>(a.recv[0], off + static_cast<uint64_t>(e), w);
+    } else {
+      store_raw<DT_OUT, 1>(a.recv[r], off + static_cast<uint64_t>(e), w);
+    }
+  }
+}
+
+// Whether a call takes fold_small_kernel: more than 16 ranks (the vector
+// kernels' one round of loads) and chunks of at most kSmallMaxLen elements;
+// up to 32 ranks (two rounds) only while a chunk holds at most 2048 of the
+// ranks' elements.  Measured on GB300 against the vector kernels (us per
+// call, one call after another): all-reduce fp32 p = 72 at 1 / 4 / 16 / 64
+// KiB per rank 4.9 / 7.8 / 9.1 / 10.1 -> 2.2 / 2.9 / 5.6 / 6.8, p = 128 at
+// 1 / 64 KiB 6.1 / 10.6 -> 2.7 / 9.5, p = 17 at 1 KiB 3.3 -> 1.7;
+// reduce-scatter fp32 p = 72 at 1 / 16 KiB 3.7 / 8.0 -> 2.0 / 4.6.  At
+// p = 17 - 32 with chunks of 128 - 240 fp32 (16 KiB per rank) it lost
+// (p = 32 all-reduce 2.8 -> 4.0 us).
+bool fold_small(int p, uint64_t q) {
+  if (p <= 16 || q + 1 > static_cast<uint64_t>(kSmallMaxLen)) return false;
+  return p > 32 || static_cast<uint64_t>(p) * (q + 1) <= 2048;
+}
+
+unsigned fold_small_segments(int p, uint64_t q) {
+  const uint64_t seg = static_cast<uint64_t>(kSmallMaxItems / p);
+  return static_cast<unsigned>((q + 1 + seg - 1) / seg);
+}
+
 constexpr int kVectorsPerThread = 2;
 
 // fold_kernel strides over a chunk's vectors, about kVectorsPerThread per
@@ -341,11 +417,14 @@ cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
 // them is fold_plan's (below), so that one host function states it.
 template <int DT_IN, int DT_OUT, int OP, int MODE>
 cudaError_t launch_typed(bool vec, const FoldArgs& a, cudaStream_t s) {
+  const FoldPlan pl = fold_plan(DT_IN, DT_OUT, OP, MODE, a.p, a.q, vec, current_sm_count());
+  if (pl.batch < 0)
+    return launch_kernel(fold_small_kernel<DT_IN, DT_OUT, OP, MODE>,
+                         dim3(fold_small_segments(a.p, a.q), static_cast<unsigned>(a.p)), dim3(kThreads), s, a);
   if (!vec) return launch_one<DT_IN, DT_OUT, 1, OP, MODE>(a, s);
   constexpr int VEC = vec_width<DT_IN, DT_OUT>();
   if constexpr (OP == CCL_SUM) {
     constexpr bool kHalve = VEC > 4;
-    const FoldPlan pl = fold_plan(DT_IN, DT_OUT, OP, MODE, a.p, a.q, true, current_sm_count());
 #define CCL_UNROLLED(B, U) \
   if (pl.batch == B && pl.vectors == U) return launch_unrolled<DT_IN, DT_OUT, VEC, OP, MODE, B, U>(a, s);
     CCL_UNROLLED(2, 2)
@@ -413,9 +492,13 @@ cudaError_t launch_mode(int dt, int op, bool vec, const FoldArgs& a, cudaStream_
 //    p <= 2 and 4 x 2 at p <= 4 once that grid has 8 CTAs per SM, else 2 x 2
 //    and 4 x 1; p > 4 stays on fold_kernel (8 ranks of 32-byte vectors
 //    would need twice the registers).
-// The general kernel ran 0.3-0.8 for p <= 4 at these sizes.
+// The general kernel ran 0.3-0.8 for p <= 4 at these sizes.  Calls of
+// more than 16 ranks whose chunks fit shared memory (fold_small) take
+// fold_small_kernel, whatever the op and alignment: (-1, 0).
 FoldPlan fold_plan(int dt_in, int dt_out, int op, int mode, int p, uint64_t q, bool vec, int sms) {
-  if (!vec || op != CCL_SUM || p < 1) return FoldPlan{0, 0};
+  if (p < 1) return FoldPlan{0, 0};
+  if (fold_small(p, q)) return FoldPlan{-1, 0};  // fold_small_kernel, any op and alignment
+  if (!vec || op != CCL_SUM) return FoldPlan{0, 0};
   const int in_bytes = (dt_in == kBF16) ? 2 : 4;
   const int v = (dt_in == kF32 && dt_out == kBF16) ? 8 : 16 / in_bytes;  // vec_width
   const bool halve = v > 4;

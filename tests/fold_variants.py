@@ -1,8 +1,8 @@
 """The fused fold kernel's variants and the GPU cases that reach each one.
 
 ``ccl_fold_plan`` names the kernel a sum of p ranks x n elements takes: the
-small-p kernel with (ranks per load batch, vectors per thread), or (0, 0) for
-the general kernel.  Each variant is a separate instantiation per call kind
+small-p kernel with (ranks per load batch, vectors per thread), (0, 0) for
+the general kernel, or (-1, 0) for the kernel of small chunks at p > 16.  Each variant is a separate instantiation per call kind
 (all-reduce, reduce-scatter, reduce to the root, DDP bucket), so each
 (kind, dtype, variant) needs a GPU parity case at a size that selects it.
 ``CASES`` lists them; ``tests/test_fold_plan.py`` checks on the CPU that
@@ -28,17 +28,20 @@ _SUM_CASES = {
     "f32": [(1, 12 * M, (2, 2), (2, 8)), (2, 12 * M + 3, (2, 2), (2, 8)), (3, 6 * M + 1, (4, 2), (4, 2)),
             (4, 6 * M + 2, (4, 1), (4, 2)), (2, 100_003, (2, 1), (2, 2)), (1, 4099, (2, 1), (2, 2)),
             (3, 300_007, (4, 1), (4, 1)), (4, 65_537, (4, 1), (4, 1)), (5, 200_003, (8, 1), (8, 1)),
-            (8, 1_000_003, (8, 1), (8, 1)), (9, 100_003, (0, 0), (0, 0)), (16, 50_021, (0, 0), (0, 0))],
+            (8, 1_000_003, (8, 1), (8, 1)), (9, 100_003, (0, 0), (0, 0)), (16, 50_021, (0, 0), (0, 0)),
+            (72, 1_000, (-1, 0), (-1, 0)), (17, 1_999, (-1, 0), (-1, 0)), (72, 14_405, (-1, 0), (-1, 0))],
     "i32": [(2, 12 * M + 1, (2, 2), (2, 8)), (3, 6 * M + 2, (4, 2), (4, 2)), (4, 6 * M + 1, (4, 1), (4, 2)),
             (2, 100_001, (2, 1), (2, 2)), (4, 65_539, (4, 1), (4, 1)), (7, 200_005, (8, 1), (8, 1)),
-            (12, 40_009, (0, 0), (0, 0))],
+            (12, 40_009, (0, 0), (0, 0)), (100, 3_999, (-1, 0), (-1, 0))],
     "bf16": [(1, 12 * M + 6, (2, 2), (2, 2)), (2, 12 * M + 1, (2, 2), (2, 2)), (3, 6 * M + 1, (4, 2), (4, 2)),
              (4, 6 * M + 3, (4, 1), (4, 2)), (2, 100_003, (2, 1), (2, 2)), (3, 300_001, (4, 1), (4, 1)),
              (6, 200_003, (8, 1), (8, 1)), (8, 500_009, (8, 1), (8, 1)), (9, 100_003, (0, 0), (0, 0)),
-             (16, 50_021, (0, 0), (0, 0))],
+             (16, 50_021, (0, 0), (0, 0)), (72, 1_001, (-1, 0), (-1, 0)), (33, 3_999, (-1, 0), (-1, 0)),
+             (128, 32_767, (-1, 0), (-1, 0))],
 }
 _BUCKET_CASES = [(1, 12 * M, (2, 4)), (2, 12 * M + 1, (2, 4)), (3, 6 * M + 2, (4, 2)), (4, 6 * M + 3, (4, 2)),
-                 (2, 100_003, (2, 2)), (4, 65_539, (4, 1)), (5, 200_003, (0, 0)), (8, 300_007, (0, 0))]
+                 (2, 100_003, (2, 2)), (4, 65_539, (4, 1)), (5, 200_003, (0, 0)), (8, 300_007, (0, 0)),
+                 (72, 1_003, (-1, 0))]
 
 CASES = [(kind, dt, p, n, ar if kind == "allreduce" else rs) for kind in ("allreduce", "reduce_scatter", "reduce")
          for dt, rows in _SUM_CASES.items() for (p, n, ar, rs) in rows]
