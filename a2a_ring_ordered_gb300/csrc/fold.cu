@@ -372,8 +372,8 @@ constexpr int kVectorsPerThread = 2;
 // spills into a second wave lost at 2 MiB (reduce-scatter p = 72 0.97 ->
 // 0.88).
 //
-// The reduce-scatter with 9..32 ranks and chunks of 128 KiB or more loads 8
-// ranks per batch instead of 16 (about 60 registers instead of 91-107: 4
+// The reduce-scatter (and the reduce to the root) with 9..32 ranks and
+// chunks of 128 KiB or more loads 8 ranks per batch instead of 16 (about 60 registers instead of 91-107: 4
 // CTAs per SM instead of 2, each thread two dependent rounds of loads).
 // Measured on GB300 against 16 (fraction of the copy bandwidth): p = 9 bf16
 // at 8 / 64 / 256 MiB per rank 0.73 / 0.84 / 0.87 -> 0.85 / 0.98 / 0.98,
@@ -400,6 +400,14 @@ cudaError_t launch_one(const FoldArgs& a, cudaStream_t s) {
     } else if (realign) {
       kernel = fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, true>;
     }
+  }
+  if constexpr (MODE == kModeReduce && VEC > 1) {
+    // the reduce to the root reads and writes what the reduce-scatter does
+    // (fp32 p = 9 / 16 / 32 at 16 MiB per rank 0.96 / 1.05 / 1.09 -> 1.00 /
+    // 1.09 / 1.10 of the copy bandwidth, bf16 p = 9 at 64 MiB 0.91 -> 1.03)
+    constexpr bool kWide = words_for(VEC, Elem<DT_IN>::kBytes) >= 8;
+    if (!kWide && a.p >= 9 && a.p <= 32 && a.q * Elem<DT_IN>::kBytes >= kBatch8MinChunkBytes)
+      kernel = fold_kernel<DT_IN, DT_OUT, VEC, OP, MODE, false, 8>;
   }
   const uint64_t per_chunk = (a.q + 1 + VEC - 1) / VEC + 31;  // + the lanes before v_lo
   auto grid_x = [&](uint64_t vpt) { return (per_chunk + kThreads * vpt - 1) / (kThreads * vpt); };

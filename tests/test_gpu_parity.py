@@ -168,6 +168,19 @@ def test_reduce_scatter_eight_rank_batches_match_oracle(lib, dtype, op, p, n):
         assert shards[k].guards_intact()
 
 
+@pytest.mark.parametrize("dtype,op,p,n", RS_BATCH8)
+def test_reduce_eight_rank_batches_match_oracle(lib, dtype, op, p, n):
+    """The reduce to the root takes the same 8-rank batches: the root's
+    buffer against the literal ring all-reduce's bits, guard bands."""
+    x = make_inputs(dtype, p, n, seed=p * 37 + n % 1000)
+    want, _, _ = ring.ring_allreduce(x, dtype, op)
+    root = p - 2
+    out = Guarded(n, dtype)
+    lib.ccl_reduce([to_dev(v, dtype) for v in x], out.view, op=op, root=root)
+    assert_equal(to_host(out.view), want[root], dtype, f"reduce {dtype} {op} p={p} n={n}")
+    assert out.guards_intact()
+
+
 # -------------------------------------------- alignment and in-place forms
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("p,n", [(4, 1027), (8, 4096), (3, 50001)])
