@@ -250,14 +250,31 @@ cudaError_t launch_bcast(const GatherArgs& a, uint64_t n, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, broadcast_kernel<DT, VEC, U>, a, n);
 }
 
+// 8 vectors per thread when that grid has 4 CTAs per SM or more; below it,
+// 1 when the one-vector grid still fills a wave of this kernel (8 CTAs per
+// SM), else 2.  Measured on GB300 (fp32, fraction of the copy bandwidth,
+// 8 vectors -> this rule): p = 4 / 16 / 72 at 2 MiB 0.49 / 0.56 / 0.56 ->
+// 0.76 / 0.96 / 0.94, p = 16 / 72 at 8 MiB 0.96 / 0.97 -> 0.95 / 1.00; from
+// 32 MiB the vector counts came out within 2 % of one another.
+template <int DT, int VEC>
+cudaError_t launch_bcast_vec(const GatherArgs& a, uint64_t n, cudaStream_t s) {
+  const uint64_t nv = n / VEC;
+  const int sms = current_sm_count();
+  const uint64_t sm_count = static_cast<uint64_t>(sms > 0 ? sms : 1);
+  auto ctas = [&](uint64_t u) { return (nv + kThreads * u - 1) / (kThreads * u); };
+  if (ctas(8) >= 4 * sm_count) return launch_bcast<DT, VEC, 8>(a, n, s);
+  if (ctas(1) >= 8 * sm_count) return launch_bcast<DT, VEC, 1>(a, n, s);
+  return launch_bcast<DT, VEC, 2>(a, n, s);
+}
+
 }  // namespace
 
 cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, cudaStream_t s) {
   cudaError_t err = cudaErrorInvalidValue;
   if (dt == kF32 || dt == kI32) {
-    err = vec ? launch_bcast<kF32, 4, 8>(a, n, s) : launch_bcast<kF32, 1, 1>(a, n, s);
+    err = vec ? launch_bcast_vec<kF32, 4>(a, n, s) : launch_bcast<kF32, 1, 1>(a, n, s);
   } else if (dt == kBF16) {
-    err = vec ? launch_bcast<kBF16, 8, 8>(a, n, s) : launch_bcast<kBF16, 1, 1>(a, n, s);
+    err = vec ? launch_bcast_vec<kBF16, 8>(a, n, s) : launch_bcast<kBF16, 1, 1>(a, n, s);
   }
   if (err == cudaSuccess) note_launch();
   return err;

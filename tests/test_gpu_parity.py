@@ -967,6 +967,26 @@ def test_identities_on_gpu(lib, p, n):
         assert torch.equal(a_.view(torch.int32), b_.view(torch.int32))
 
 
+# vectors per thread of the broadcast (the host picks them by grid size):
+# 2 for small calls, 1 once that grid fills a wave, 8 for large ones
+BCAST_SIZE_CLASSES = [("bf16", 16, 100_003), ("f32", 8, 2 * 1048576 + 3), ("bf16", 4, 4 * 1048576 + 1),
+                      ("f32", 4, 6 * 1048576 + 5)]
+
+
+@pytest.mark.parametrize("dtype,p,n", BCAST_SIZE_CLASSES)
+def test_broadcast_size_classes_match_oracle(lib, dtype, p, n):
+    """Every element of every output against the root's buffer, at sizes
+    that select 2, 1 and 8 vectors per thread, guard bands."""
+    x = make_inputs(dtype, p, n, seed=11 * p + n % 1000)
+    root = p - 1
+    outs = guarded_outputs(p, [n] * p, dtype)
+    lib.ccl_broadcast(to_dev(x[root], dtype), [o.view for o in outs], root=root)
+    want = collectives.broadcast(x, root)
+    for r, o in enumerate(outs):
+        assert_equal(to_host(o.view), want[r], dtype, f"bcast {dtype} p={p} n={n} rank {r}")
+        assert o.guards_intact()
+
+
 def test_rooted_in_place_forms(lib):
     p, n = 5, 12345
     x = make_inputs("f32", p, n, seed=9)
