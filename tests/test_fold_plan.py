@@ -81,3 +81,24 @@ def test_fold_plan_rejects_bad_arguments():
         lib.ccl_fold_plan(4, 10, "f32", "max", kind="bucket")
     with pytest.raises(ValueError):
         lib.ccl_fold_plan(4, 10, "f32", kind="gather")
+
+
+def test_small_chunk_kernel_boundaries():
+    """(-1, 0): more than 16 ranks and chunks of at most 256 elements; up to
+    32 ranks only while p x (chunk + 1) stays within 2048 elements.  Any op
+    and alignment."""
+    lib = _lib()
+    for op in ("sum", "max", "min"):
+        for aligned in (True, False):
+            plan = lambda p, n: lib.ccl_fold_plan(p, n, "f32", op, aligned=aligned, sm_count=152)
+            assert plan(16, 16 * 10) != (-1, 0)                 # 16 ranks: one round already
+            assert plan(17, 17 * 119) == (-1, 0)                # 17 x 120 = 2040
+            assert plan(17, 17 * 121) != (-1, 0)                # 17 x 122 = 2074
+            assert plan(32, 32 * 63) == (-1, 0)                 # 32 x 64 = 2048
+            assert plan(32, 32 * 64) != (-1, 0)
+            assert plan(33, 33 * 255) == (-1, 0)                # chunks of 255 (+1)
+            assert plan(33, 33 * 256 + 1) != (-1, 0)            # a chunk of 257
+            assert plan(128, 128 * 255) == (-1, 0)
+            assert plan(128, 128 * 255 + 1) == (-1, 0)          # one chunk of 256: still in
+            assert plan(128, 128 * 256) != (-1, 0)              # chunks of 256 and one of 257
+    assert lib.ccl_fold_plan(72, 1000, "f32", "sum", kind="bucket", sm_count=152) == (-1, 0)
