@@ -110,3 +110,38 @@ def test_plan_rejects_bad_arguments():
     with pytest.raises(lib.CclError):
         lib.ccl_all_to_allv_plan([1 << 30] * 2, np.full((2, 2), 1 << 60), [1 << 31] * 2, 1, "f32", sm_count=152)
     assert lib.ccl_all_to_all_plan([1 << 30] * 4, [1 << 31] * 4, 0, "f32", sm_count=152)[3] == 0
+
+
+def test_stage_follows_the_block_size_and_the_grid():
+    """The small-block stage runs only when some block edge or destination
+    end is off the 16-byte grid and blocks average 8 KB or less; the shift
+    only when some block's source and destination phases differ."""
+    lib = _lib()
+    p = 8
+    s, r = _addresses(p, 0, 4), _addresses(p, 0, 4, base=256)
+    plan = lambda counts, recv, row: lib.ccl_all_to_allv_plan(s, counts, recv, row, "f32", sm_count=152)
+    # blocks of 400 bytes: every edge on the grid, phases equal: neither
+    assert plan(np.full((p, p), 100), r, 1)[1:3] == (False, False)
+    # blocks of 404 bytes: edges off the grid (stage), and a block's source
+    # rows before it differ from its destination's (shift)
+    assert plan(np.full((p, p), 101), r, 1)[1:3] == (True, True)
+    # blocks of 8,188 bytes on average still stage, of 8,196 not
+    assert plan(np.full((p, p), 2047), r, 1)[2] is True
+    assert plan(np.full((p, p), 2049), r, 1)[2] is False
+    # receive buffers 4 bytes off the grid, 16-byte rows: stage and shift
+    assert plan(np.full((p, p), 4), _addresses(p, 1, 4, base=256), 4)[1:3] == (True, True)
+    # the plain all-to-all: n a multiple of 4 p keeps every block on the grid
+    assert lib.ccl_all_to_all_plan(s, r, 4 * p * 100, "f32", sm_count=152)[1:3] == (False, False)
+    assert lib.ccl_all_to_all_plan(s, r, 4 * p * 100 + 1, "f32", sm_count=152)[1:3] == (True, True)
+
+
+def test_small_calls_take_4kb_tiles_while_they_fit_one_wave():
+    lib = _lib()
+    p = 16
+    s, r = _addresses(p, 0, 4), _addresses(p, 0, 4, base=256)
+    # 16 destinations of 64 KB: 256 tiles of 4 KB, within one wave (4 CTAs x 152 SMs)
+    assert lib.ccl_all_to_all_plan(s, r, 16 * 1024, "f32", sm_count=152)[4] == 4096
+    # 16 of 256 KB: 1,024 tiles of 4 KB, past one wave: 32 KB tiles
+    assert lib.ccl_all_to_all_plan(s, r, 16 * 4096, "f32", sm_count=152)[4] == 32768
+    # the same call on a device of twice the SMs keeps 4 KB tiles
+    assert lib.ccl_all_to_all_plan(s, r, 16 * 4096, "f32", sm_count=304)[4] == 4096
