@@ -292,7 +292,7 @@ cudaError_t launch_unrolled(const FoldArgs& a, cudaStream_t s) {
 // dependent rounds.  Segments hold kSmallMaxItems / p elements; grid x =
 // segments, grid y = chunks.
 constexpr int kSmallMaxItems = 4096;  // p x segment held in shared memory
-constexpr int kSmallMaxLen = 256;     // chunks this kernel takes
+constexpr int kSmallMaxLen = 1536;    // chunks this kernel takes at p > 32
 
 template <int DT_IN, int DT_OUT, int OP, int MODE>
 __global__ void __launch_bounds__(kThreads) fold_small_kernel(const __grid_constant__ FoldArgs a) {
@@ -340,24 +340,40 @@ __global__ void __launch_bounds__(kThreads) fold_small_kernel(const __grid_const
   }
 }
 
-// Whether a call takes fold_small_kernel: more than 16 ranks (the vector
-// kernels' one round of loads) and chunks of at most kSmallMaxLen elements;
-// up to 32 ranks (two rounds) only while a chunk holds at most 2048 of the
-// ranks' elements.  Measured on GB300 against the vector kernels (us per
-// call, one call after another): all-reduce fp32 p = 72 at 1 / 4 / 16 / 64
-// KiB per rank 4.9 / 7.8 / 9.1 / 10.1 -> 2.2 / 2.9 / 5.6 / 6.8, p = 128 at
-// 1 / 64 KiB 6.1 / 10.6 -> 2.7 / 9.5, p = 17 at 1 KiB 3.3 -> 1.7;
-// reduce-scatter fp32 p = 72 at 1 / 16 KiB 3.7 / 8.0 -> 2.0 / 4.6.  At
-// p = 17 - 32 with chunks of 128 - 240 fp32 (16 KiB per rank) it lost
-// (p = 32 all-reduce 2.8 -> 4.0 us).
-bool fold_small(int p, uint64_t q) {
-  if (p <= 16 || q + 1 > static_cast<uint64_t>(kSmallMaxLen)) return false;
-  return p > 32 || static_cast<uint64_t>(p) * (q + 1) <= 2048;
-}
-
 unsigned fold_small_segments(int p, uint64_t q) {
   const uint64_t seg = static_cast<uint64_t>(kSmallMaxItems / p);
   return static_cast<unsigned>((q + 1 + seg - 1) / seg);
+}
+
+// Whether a call takes fold_small_kernel.  The vector kernels load 16 ranks
+// per round, ceil(p / 16) dependent rounds; this kernel loads every rank in
+// one round, and its CTAs ran at full speed up to about 4 per SM (p = 48:
+// 480 CTAs 7.6 us, 624 CTAs 11.1 us; p = 72: 504 -> 7.7 us, 648 -> 10.6 us,
+// all-reduce fp32).  So it takes the call when
+//  * 17 - 32 ranks (two rounds): a chunk holds at most 2048 of the ranks'
+//    elements (p = 32 with chunks of 128 - 240 fp32 lost, 2.8 -> 4.0 us);
+//  * more than 32 ranks: chunks of at most kSmallMaxLen elements and at
+//    most 4 CTAs per SM for every two of the vector kernels' rounds.
+// Measured on GB300 against the vector kernels (us per call, one call after
+// another; chunk = elements per chunk):
+//   all-reduce fp32 p = 72 at 1 / 16 / 64 KiB per rank  4.9 / 9.1 / 10.1 -> 2.2 / 5.6 / 6.8
+//   all-reduce p = 72, chunk 300 / 768, fp32            9.9 / 11.5 -> 6.9 / 11.0
+//                                       bf16            12.1 / 12.1 -> 6.5 / 11.2
+//   all-reduce fp32 p = 72, chunk 1024 (1,368 CTAs)     12.5 -> 15.1 (not taken)
+//   all-reduce fp32 p = 128, chunk 300 / 512            18.4 / 20.6 -> 14.2 / 19.4
+//   all-reduce fp32 p = 128, chunk 640 (2,688 CTAs)     22.0 -> 24.6 (not taken)
+//   all-reduce p = 48, chunk 768, fp32 / bf16           7.3 / 7.9 -> 7.6 / 7.3
+//   all-reduce p = 33, chunk 1024, fp32 / bf16          6.6 / 7.1 -> 6.1 / 5.7
+//   reduce-scatter p = 72, chunk 300 / 768, fp32        8.6 / 9.1 -> 5.5 / 8.6
+//                                           bf16        9.4 / 9.6 -> 5.1 / 8.1
+//   reduce-scatter p = 128, chunk 512, fp32 / bf16      14.6 / 15.2 -> 13.3 / 12.9
+bool fold_small(int p, uint64_t q, int sms) {
+  if (p <= 16) return false;
+  if (p <= 32) return static_cast<uint64_t>(p) * (q + 1) <= 2048;
+  if (q + 1 > static_cast<uint64_t>(kSmallMaxLen)) return false;
+  const uint64_t rounds = static_cast<uint64_t>((p + 15) / 16);  // >= 3
+  const uint64_t n_sms = static_cast<uint64_t>(sms > 0 ? sms : 1);
+  return static_cast<uint64_t>(fold_small_segments(p, q)) * static_cast<uint64_t>(p) <= 4 * n_sms * (rounds / 2);
 }
 
 constexpr int kVectorsPerThread = 2;
@@ -505,7 +521,7 @@ cudaError_t launch_mode(int dt, int op, bool vec, const FoldArgs& a, cudaStream_
 // fold_small_kernel, whatever the op and alignment: (-1, 0).
 FoldPlan fold_plan(int dt_in, int dt_out, int op, int mode, int p, uint64_t q, bool vec, int sms) {
   if (p < 1) return FoldPlan{0, 0};
-  if (fold_small(p, q)) return FoldPlan{-1, 0};  // fold_small_kernel, any op and alignment
+  if (fold_small(p, q, sms)) return FoldPlan{-1, 0};  // fold_small_kernel, any op and alignment
   if (!vec || op != CCL_SUM) return FoldPlan{0, 0};
   const int in_bytes = (dt_in == kBF16) ? 2 : 4;
   const int v = (dt_in == kF32 && dt_out == kBF16) ? 8 : 16 / in_bytes;  // vec_width

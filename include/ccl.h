@@ -130,9 +130,12 @@ ccl_status_t ccl_chunk_bounds(int p, size_t n, int c, size_t* off, size_t* len);
  * ranks whose loads one thread issues together and *vectors = 16-byte
  * vectors per thread of the small-p kernel, both 0 for the general kernel
  * (large p, MAX / MIN, unaligned buffers), or *batch = -1 for the kernel of
- * small chunks at p > 16 (chunks of at most 256 elements: every rank's part
- * of a chunk segment loaded in one round into shared memory; any op and
- * alignment).  Host only; it enqueues nothing.
+ * small chunks at p > 16 (every rank's part of a chunk segment loaded in one
+ * round into shared memory; any op and alignment): at p = 17..32 while
+ * p x (chunk + 1) <= 2048 elements, at p > 32 for chunks of at most 1536
+ * elements while its grid (chunk segments of 4096 / p elements x p) holds at
+ * most 4 CTAs per SM for every two of the 16-rank load rounds of the vector
+ * kernels (ceil(p / 16)).  Host only; it enqueues nothing.
  * Errors: p outside 1..CCL_MAX_RANKS, an unknown kind / dt / op, a bucket
  * plan for another dt / op, NULL outputs -> CCL_ERR_INVALID_ARG. */
 typedef enum {

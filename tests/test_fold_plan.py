@@ -84,21 +84,32 @@ def test_fold_plan_rejects_bad_arguments():
 
 
 def test_small_chunk_kernel_boundaries():
-    """(-1, 0): more than 16 ranks and chunks of at most 256 elements; up to
-    32 ranks only while p x (chunk + 1) stays within 2048 elements.  Any op
-    and alignment."""
+    """(-1, 0): 17 - 32 ranks while p x (chunk + 1) stays within 2048
+    elements; more than 32 ranks for chunks of at most 1536 elements while
+    the grid (segments of 4096 // p elements per chunk, x p chunks) holds at
+    most 4 CTAs per SM for every two of the vector kernels' 16-rank rounds.
+    Any op and alignment."""
     lib = _lib()
     for op in ("sum", "max", "min"):
         for aligned in (True, False):
-            plan = lambda p, n: lib.ccl_fold_plan(p, n, "f32", op, aligned=aligned, sm_count=152)
+            plan = lambda p, n, sms=152: lib.ccl_fold_plan(p, n, "f32", op, aligned=aligned, sm_count=sms)
             assert plan(16, 16 * 10) != (-1, 0)                 # 16 ranks: one round already
             assert plan(17, 17 * 119) == (-1, 0)                # 17 x 120 = 2040
             assert plan(17, 17 * 121) != (-1, 0)                # 17 x 122 = 2074
             assert plan(32, 32 * 63) == (-1, 0)                 # 32 x 64 = 2048
             assert plan(32, 32 * 64) != (-1, 0)
-            assert plan(33, 33 * 255) == (-1, 0)                # chunks of 255 (+1)
-            assert plan(33, 33 * 256 + 1) != (-1, 0)            # a chunk of 257
-            assert plan(128, 128 * 255) == (-1, 0)
-            assert plan(128, 128 * 255 + 1) == (-1, 0)          # one chunk of 256: still in
-            assert plan(128, 128 * 256) != (-1, 0)              # chunks of 256 and one of 257
+            # p = 33 (3 rounds): segments of 124, at most 608 CTAs; the 1536 cap binds first
+            assert plan(33, 33 * 1535 + 32) == (-1, 0)          # chunks of 1535 and 1536
+            assert plan(33, 33 * 1536) != (-1, 0)               # q + 1 = 1537
+            # p = 48 (3 rounds): segments of 85, 12 per chunk (576 CTAs) still in, 13 (624) not
+            assert plan(48, 48 * 1019) == (-1, 0)
+            assert plan(48, 48 * 1020) != (-1, 0)
+            # p = 72 (5 rounds, two waves of 4 CTAs per SM): segments of 56, 16 per chunk (1152 CTAs)
+            assert plan(72, 72 * 895) == (-1, 0)
+            assert plan(72, 72 * 896) != (-1, 0)
+            assert plan(72, 72 * 895, sms=132) != (-1, 0)      # 1056 CTAs at most on 132 SMs
+            assert plan(72, 72 * 783, sms=132) == (-1, 0)      # 14 segments, 1008 CTAs
+            # p = 128 (8 rounds, four waves): segments of 32, 19 per chunk (2432 CTAs)
+            assert plan(128, 128 * 607) == (-1, 0)
+            assert plan(128, 128 * 608) != (-1, 0)
     assert lib.ccl_fold_plan(72, 1000, "f32", "sum", kind="bucket", sm_count=152) == (-1, 0)
