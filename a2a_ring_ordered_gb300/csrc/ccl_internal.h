@@ -22,7 +22,7 @@ enum FoldMode : int {
 
 // pf_ctas (set by launch_kernel): CTAs of the launch's first wave, the ones
 // that prefetch their first inputs into L2 before waiting on the previous
-// grid (0: none).
+// grid (0: none); fold_small_kernel compares its grid with it.
 struct FoldArgs {
   const void* send[CCL_MAX_RANKS];
   void* recv[CCL_MAX_RANKS];

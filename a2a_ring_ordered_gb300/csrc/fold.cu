@@ -284,6 +284,20 @@ cudaError_t launch_unrolled(const FoldArgs& a, cudaStream_t s) {
                        dim3(kThreads), s, a);
 }
 
+// Programmatic dependent launch in two halves: wait for the previous grid,
+// and let the next one be scheduled (a CTA that never does the second does
+// it implicitly when it exits).
+__device__ __forceinline__ void pdl_wait() {
+#if CCL_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void pdl_trigger() {
+#if CCL_PDL
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
 // Small chunks at large p: a CTA loads all p ranks' elements of a segment
 // of chunk c at once (one round of loads, whatever p is) into shared
 // memory, folds each element there in ring order from rank c + 1 (the same
@@ -307,7 +321,16 @@ __global__ void __launch_bounds__(kThreads) fold_small_kernel(const __grid_const
   const int len = static_cast<int>(ch.len) - e0 < seg ? static_cast<int>(ch.len) - e0 : seg;
   const uint64_t off = ch.off + static_cast<uint64_t>(e0);
   const int first = (c + 1 == p) ? 0 : c + 1;
-  pdl_enter();
+  // A grid of more than half the device's resident CTAs (a.pf_ctas: one
+  // wave) lets the next grid be scheduled only as its CTAs exit.  Scheduled
+  // at entry, the next grid's CTAs took slots this grid's last CTAs needed:
+  // measured on GB300, back-to-back calls, late against at entry (us per
+  // call): all-reduce p = 72 with chunks of 455 (648 CTAs) 10.6 -> 8.2 fp32,
+  // 11.0 -> 7.8 bf16; reduce-scatter 8.4 -> 6.1 and 8.0 -> 5.7; p = 48 with
+  // chunks of 1024 (624 CTAs) 11.2 -> 8.4.  Grids within half a wave ran the
+  // same either way and keep the early start.
+  pdl_wait();
+  if (static_cast<uint64_t>(gridDim.x) * gridDim.y * 2 <= a.pf_ctas) pdl_trigger();
   if (len <= 0) return;  // (uniform over the CTA)
   for (int t = threadIdx.x; t < p * len; t += kThreads) {
     const int j = t / len, e = t - j * len;
@@ -347,26 +370,27 @@ unsigned fold_small_segments(int p, uint64_t q) {
 
 // Whether a call takes fold_small_kernel.  The vector kernels load 16 ranks
 // per round, ceil(p / 16) dependent rounds; this kernel loads every rank in
-// one round, and its CTAs ran at full speed up to about 4 per SM (p = 48:
-// 480 CTAs 7.6 us, 624 CTAs 11.1 us; p = 72: 504 -> 7.7 us, 648 -> 10.6 us,
-// all-reduce fp32).  So it takes the call when
+// one round.  It takes the call when
 //  * 17 - 32 ranks (two rounds): a chunk holds at most 2048 of the ranks'
 //    elements (p = 32 with chunks of 128 - 240 fp32 lost, 2.8 -> 4.0 us);
 //  * more than 32 ranks: chunks of at most kSmallMaxLen elements and at
-//    most 4 CTAs per SM for every two of the vector kernels' rounds.
+//    most 4 CTAs per SM for every two of the vector kernels' rounds (one
+//    wave, 8 per SM, at p = 72; four at p = 128).
 // Measured on GB300 against the vector kernels (us per call, one call after
-// another; chunk = elements per chunk):
+// another; chunk = elements per chunk; the late dependent launch above in
+// place):
 //   all-reduce fp32 p = 72 at 1 / 16 / 64 KiB per rank  4.9 / 9.1 / 10.1 -> 2.2 / 5.6 / 6.8
-//   all-reduce p = 72, chunk 300 / 768, fp32            9.9 / 11.5 -> 6.9 / 11.0
-//                                       bf16            12.1 / 12.1 -> 6.5 / 11.2
-//   all-reduce fp32 p = 72, chunk 1024 (1,368 CTAs)     12.5 -> 15.1 (not taken)
-//   all-reduce fp32 p = 128, chunk 300 / 512            18.4 / 20.6 -> 14.2 / 19.4
-//   all-reduce fp32 p = 128, chunk 640 (2,688 CTAs)     22.0 -> 24.6 (not taken)
-//   all-reduce p = 48, chunk 768, fp32 / bf16           7.3 / 7.9 -> 7.6 / 7.3
+//   all-reduce p = 72, chunk 300 / 455 / 768, fp32      9.9 / 10.1 / 11.5 -> 6.9 / 8.2 / 10.1
+//                                             bf16      12.1 / 11.9 / 12.1 -> 6.5 / 7.8 / 9.8
+//   reduce-scatter p = 72, chunk 300 / 455 / 768, fp32  8.6 / 8.8 / 9.1 -> 5.5 / 6.1 / 7.6
+//                                                 bf16  9.4 / 9.4 / 9.6 -> 5.1 / 5.7 / 7.4
+//   all-reduce fp32 p = 72, chunk 1024 (1,368 CTAs)     12.5 -> 15.5 (not taken)
+//   all-reduce fp32 p = 128, chunk 300 / 512            18.4 / 20.6 -> 14.1 / 19.3
+//   all-reduce fp32 p = 128, chunk 768 (3,200 CTAs)     23.5 -> 27.9 (not taken)
+//   p = 48, chunk 768, all-reduce fp32 / bf16           7.3 / 7.9 -> 7.6 / 7.3
+//   p = 48, chunk 1024 (624 CTAs), all-reduce fp32      7.9 -> 8.4 (not taken;
+//                                  reduce-scatter bf16  6.4 -> 5.8)
 //   all-reduce p = 33, chunk 1024, fp32 / bf16          6.6 / 7.1 -> 6.1 / 5.7
-//   reduce-scatter p = 72, chunk 300 / 768, fp32        8.6 / 9.1 -> 5.5 / 8.6
-//                                           bf16        9.4 / 9.6 -> 5.1 / 8.1
-//   reduce-scatter p = 128, chunk 512, fp32 / bf16      14.6 / 15.2 -> 13.3 / 12.9
 bool fold_small(int p, uint64_t q, int sms) {
   if (p <= 16) return false;
   if (p <= 32) return static_cast<uint64_t>(p) * (q + 1) <= 2048;
