@@ -375,7 +375,7 @@ unsigned fold_small_segments(int p, uint64_t q) {
 //    elements (p = 32 with chunks of 128 - 240 fp32 lost, 2.8 -> 4.0 us);
 //  * more than 32 ranks: chunks of at most kSmallMaxLen elements and at
 //    most 4 CTAs per SM for every two of the vector kernels' rounds (one
-//    wave, 8 per SM, at p = 72; four at p = 128).
+//    wave, 8 per SM, at p = 72; two waves at p = 128).
 // Measured on GB300 against the vector kernels (us per call, one call after
 // another; chunk = elements per chunk; the late dependent launch above in
 // place):
