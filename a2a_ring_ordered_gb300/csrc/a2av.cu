@@ -10,12 +10,12 @@
 // the table's column for cs on the device.  Nothing is allocated and any
 // p <= 85 is one launch (the plain all-to-all: any p).
 //
-// Work is cut into 32 KB tiles of destination space (tile boundaries on 512
-// bytes of the destination's address), one CTA per tile, so the work is
-// balanced by bytes however skewed the counts are.  The CTA puts the
-// destination's block bounds in shared memory, and each thread writes whole
-// aligned 16-byte destination units (a warp's 32 stores fill whole 128-byte
-// lines):
+// Work is cut into tiles of destination space (4 - 32 KB by the call's
+// size; boundaries on 512 bytes of the destination's address), one CTA per
+// tile, so the work is balanced by bytes however skewed the counts are.
+// The CTA puts the destination's block bounds in shared memory, and each
+// thread writes whole aligned 16-byte destination units (a warp's 32 stores
+// fill whole 128-byte lines):
 //  * a unit inside one block is one aligned 16-byte source load when source
 //    and destination share the 16-byte phase, else two aligned source
 //    granules whose bytes are funnel-shifted into place;
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 4) a2a_kernel(const __grid_constant_
   const uint64_t rb = a.row_bytes;
   const uint64_t total_tiles = a.tile0[a.ndest];
   // Tile size and 16-byte units per thread (8 for 32 KB tiles, 1 for 4 KB
-  // ones).  The phase-shifting kernels take it from the template (one
+  // ones, 2 and 4 between).  The phase-shifting kernels take it from the template (one
   // instantiation per tile size), the others from the parameters: measured
   // on GB300, the other way round cost up to 10 % (the template form of the
   // unshifted kernel spilled 16 bytes: p = 8 all-to-all at 8 MiB per rank
@@ -371,8 +371,11 @@ __global__ void __launch_bounds__(kThreads, 4) a2a_kernel(const __grid_constant_
 template <class P, bool STAGE>
 cudaError_t launch_staged(const P& a, bool shift, const dim3& grid, cudaStream_t s) {
   constexpr uint32_t kBig = static_cast<uint32_t>(kA2ATileBytes), kSmall = static_cast<uint32_t>(kA2ASmallTileBytes);
+  constexpr uint32_t k8 = static_cast<uint32_t>(kA2AMidTileBytes[0]), k16 = static_cast<uint32_t>(kA2AMidTileBytes[1]);
   if (!shift) return launch_kernel(a2a_kernel<P, false, STAGE, kBig>, grid, dim3(kThreads), s, a);  // tile size at run time
   if (a.tile_bytes == kSmall) return launch_kernel(a2a_kernel<P, true, STAGE, kSmall>, grid, dim3(kThreads), s, a);
+  if (a.tile_bytes == k8) return launch_kernel(a2a_kernel<P, true, STAGE, k8>, grid, dim3(kThreads), s, a);
+  if (a.tile_bytes == k16) return launch_kernel(a2a_kernel<P, true, STAGE, k16>, grid, dim3(kThreads), s, a);
   return launch_kernel(a2a_kernel<P, true, STAGE, kBig>, grid, dim3(kThreads), s, a);
 }
 

@@ -958,12 +958,23 @@ extern "C" ccl_status_t ccl_all_to_all_heads(const void* const* send, void* cons
 namespace {
 
 // Destination tiles of one launch: tile0[c] = tiles before destination
-// j0 + c; returns the launch's total.  Small calls take 4 KB tiles when
-// those still fit in one wave of the kernel (4 CTAs per SM), else 32 KB.
-// Measured on GB300 (fp32, one call, 32 KB -> 4 KB tiles): p = 2 at 64 KiB
-// per rank 2.21 -> 1.28 us, p = 16 at 64 KiB 3.75 -> 2.53 us, p = 72 at
-// 16 KiB 9.05 -> 4.49 us; with the 4 KB grid past one wave it lost (p = 8
-// at 1 MiB, 2,048 CTAs: 3.9 -> 8.6 us).
+// j0 + c; returns the launch's total.  The tile follows the launch's bytes
+// per SM (b): 4 KB below 5 KiB, 8 KB below 24 KiB, 16 KB below 64 KiB, else
+// 32 KB.  Measured on GB300 with each tile forced (us per call, back to
+// back, fp32; bf16 alike), the chosen tile against the next larger one and
+// against the rule before (4 KB tiles while they fit one wave, else 32 KB):
+//   p = 2 at 512 KiB per rank (b = 6.7 KiB)    8 KB 1.61, 16 KB 1.86, before 1.80
+//   p = 8 at 256 KiB (b = 13.5)                8 KB 2.14, 16 KB 2.01, before 2.56
+//   p = 72 at 32 KiB (b = 15.2)                8 KB 5.00, 16 KB 5.17, before 8.07
+//   p = 16 at 256 KiB (b = 27)                 16 KB 2.50, 32 KB 3.14, before 3.14
+//   p = 72 at 64 KiB (b = 30)                  16 KB 5.44, 32 KB 7.21, before 7.21
+//   p = 72 at 128 KiB (b = 61)                 16 KB 6.59, 32 KB 7.41
+//   p = 16 at 512 KiB (b = 54)                 16 KB 3.46, 32 KB 3.32
+//   p = 40 at 256 KiB (b = 67)                 32 KB 7.72 (16 KB 8.60)
+//   p = 40 at 16 KiB (b = 4.2)                 4 KB 3.04 (8 KB 3.31)
+// Fewer, larger tiles cost a round of latency per tile; more, smaller ones
+// the per-tile set-up (block bounds, barriers); from 64 KiB per SM on the
+// 32 KB tiles' grid is several waves deep.
 template <class P>
 uint64_t fill_tiles(P& a, void* const* recv, const uint64_t* out_bytes, int sms) {
   auto fill = [&](uint64_t tile) {
@@ -976,8 +987,12 @@ uint64_t fill_tiles(P& a, void* const* recv, const uint64_t* out_bytes, int sms)
     a.tile0[a.ndest] = total;
     return total;
   };
-  if (fill(kA2ASmallTileBytes) <= 4ull * static_cast<uint64_t>(sms > 0 ? sms : 1))
-    return a.tile0[a.ndest];
+  uint64_t bytes = 0;
+  for (int c = 0; c < a.ndest; ++c) bytes += out_bytes[a.j0 + c];
+  const uint64_t per_sm = bytes / static_cast<uint64_t>(sms > 0 ? sms : 1);
+  if (per_sm < 5 * 1024) return fill(kA2ASmallTileBytes);
+  if (per_sm < 24 * 1024) return fill(kA2AMidTileBytes[0]);
+  if (per_sm < 64 * 1024) return fill(kA2AMidTileBytes[1]);
   return fill(kA2ATileBytes);
 }
 

@@ -85,10 +85,10 @@ cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, 
 
 // ------------------------------------------------------------- all-to-allv
 // Destination j's buffer holds one block per source i in source order; work
-// is cut into tiles of tile_bytes of destination space (kA2ATileBytes, or
-// kA2ASmallTileBytes for calls too small to fill the GPU; boundaries on 512
-// bytes of the destination's address), tile0[c] = first tile of destination
-// j0 + c in this launch, tile0[ndest] = the launch's tiles.
+// is cut into tiles of tile_bytes of destination space (4, 8, 16 or 32 KB
+// by the launch's bytes per SM; boundaries on 512 bytes of the
+// destination's address), tile0[c] = first tile of destination j0 + c in
+// this launch, tile0[ndest] = the launch's tiles.
 //  plain = 1: the all-to-all of the chunk rule, one element per row:
 //    block i of destination j has len(j) rows and starts at row off(j) of
 //    send[i] (n = q * p + rem elements per rank).
@@ -97,6 +97,7 @@ cudaError_t launch_broadcast(int dt, bool vec, const GatherArgs& a, uint64_t n, 
 //    destination's start, or source i's total rows when j0 + ndest = p).
 constexpr uint64_t kA2ATileBytes = 32768;
 constexpr uint64_t kA2ASmallTileBytes = 4096;
+constexpr uint64_t kA2AMidTileBytes[2] = {8192, 16384};
 // Calls with a block edge off the 16-byte grid take the small-block stage
 // while their blocks average at most this many bytes (larger blocks leave a
 // tile one edge or none, which the element path handles at less cost).
@@ -113,7 +114,7 @@ struct A2AParamsT {
   uint64_t q, rem;     // plain: the chunk rule of n
   int p, j0, ndest, plain;
   int elem;            // element bytes (2 or 4)
-  uint32_t tile_bytes; // kA2ATileBytes or kA2ASmallTileBytes
+  uint32_t tile_bytes; // 4096, 8192, 16384 or 32768
   TT table[TCAP];
 };
 // p <= 16, any geometry (a table of 16 x 17 entries): under the classic 4 KB

@@ -303,7 +303,8 @@ ccl_status_t ccl_all_to_allv(const void* const* send, const size_t* counts, void
  *   stage       the units that straddle blocks go through the small-block
  *               stage in shared memory
  *   launches    kernel launches of the call (0: nothing to move)
- *   tile_bytes  destination tile of the first launch (4096 or 32768)
+ *   tile_bytes  destination tile of the first launch (4096, 8192, 16384 or
+ *               32768: by the launch's destination bytes per SM)
  * Errors: as the call's own argument checks (p, dt, NULL pointers, sizes)
  * -> CCL_ERR_INVALID_ARG. */
 typedef enum { CCL_A2A_SMALL = 0, CCL_A2A_PLAIN = 1, CCL_A2A_TABLE32 = 2, CCL_A2A_TABLE64 = 3 } ccl_a2a_form_t;

@@ -135,13 +135,15 @@ def test_stage_follows_the_block_size_and_the_grid():
     assert lib.ccl_all_to_all_plan(s, r, 4 * p * 100 + 1, "f32", sm_count=152)[1:3] == (True, True)
 
 
-def test_small_calls_take_4kb_tiles_while_they_fit_one_wave():
+def test_tile_follows_the_bytes_per_sm():
+    """4 KB tiles below 5 KiB of destination bytes per SM, 8 KB below 24 KiB,
+    16 KB below 64 KiB, else 32 KB."""
     lib = _lib()
     p = 16
     s, r = _addresses(p, 0, 4), _addresses(p, 0, 4, base=256)
-    # 16 destinations of 64 KB: 256 tiles of 4 KB, within one wave (4 CTAs x 152 SMs)
-    assert lib.ccl_all_to_all_plan(s, r, 16 * 1024, "f32", sm_count=152)[4] == 4096
-    # 16 of 256 KB: 1,024 tiles of 4 KB, past one wave: 32 KB tiles
-    assert lib.ccl_all_to_all_plan(s, r, 16 * 4096, "f32", sm_count=152)[4] == 32768
-    # the same call on a device of twice the SMs keeps 4 KB tiles
-    assert lib.ccl_all_to_all_plan(s, r, 16 * 4096, "f32", sm_count=304)[4] == 4096
+    tile = lambda n, sms=152: lib.ccl_all_to_all_plan(s, r, n, "f32", sm_count=sms)[4]
+    kib = lambda b: b * 1024 * 152 // (4 * p)  # n per rank for b KiB per SM at 152 SMs
+    assert tile(kib(5) - 1) == 4096 and tile(kib(5)) == 8192
+    assert tile(kib(24) - 1) == 8192 and tile(kib(24)) == 16384
+    assert tile(kib(64) - 1) == 16384 and tile(kib(64)) == 32768
+    assert tile(kib(64), sms=304) == 16384  # the same call on twice the SMs
