@@ -76,9 +76,11 @@ def test_every_reachable_all_to_all_variant_has_a_gpu_case():
     covered = {case[-1] for case in av.CASES}
     missing = reach - covered
     assert not missing, f"variants {sorted(missing)} have no GPU parity case"
-    # the p <= 16 form with the stage and 32 KB tiles cannot occur: blocks of
-    # 8 KB on average fill at most 2 MB, which 4 KB tiles cover in one wave
-    assert ("small", False, True, 32768) not in reach and ("small", True, True, 32768) not in reach
+    # the p <= 16 form with the stage cannot take 16 or 32 KB tiles: blocks
+    # of 8 KB on average fill at most 16 x 16 x 8 KB = 2 MB, 13.5 KiB per SM
+    # of a 152-SM device, which takes 4 or 8 KB tiles
+    for tile in (16384, 32768):
+        assert ("small", False, True, tile) not in reach and ("small", True, True, tile) not in reach
 
 
 def test_row_prefix_width_follows_the_largest_source():
